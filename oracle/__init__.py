@@ -1,0 +1,133 @@
+"""fp64 CPU oracle for paged draft-block attention.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``.  The product library never
+imports, links or calls it, and it imports nothing from the product package.
+
+The arithmetic lives in ``dflash_oracle.cpp`` (plain C++, double precision,
+one ``std::thread`` worker per host core); this module only compiles it with
+the host C++ compiler and marshals numpy arrays.  Semantics (TensorRT-LLM
+PR #21130 "Non-causal windowed DSpark draft block", description and change 2;
+PR #20374 "Non-causal unwindowed DFlash draft block", description):
+
+* query token ``i`` of request ``b`` (position ``L+i``, ``L = ctx_lens[b]``)
+  sees context positions ``[max(0, L+i-W+1), L)`` when ``window = W > 0``
+  (all of ``[0, L)`` when ``W = 0``) and block positions ``L+j`` for every
+  ``j < K`` (``future_keys=1``) or ``j <= i`` (``future_keys=0``);
+* every key/value row is read through ``page_table`` from HND pages
+  ``[num_pages, Hkv, P, D]``; query head ``hq`` reads kv head ``hq // G``;
+* ``out`` is the softmax-weighted mean of the visible values and ``lse2`` the
+  base-2 log-sum-exp of ``scale * q.k`` over the visible keys.
+
+Pinned by ``tests/test_oracle_pins.py`` (dense brute force, causal decode,
+LSE merge of disjoint key sets, page-permutation invariance, closed forms).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dflash_oracle.cpp")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (host C++ only)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    if fresh and not force:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Open a compiled oracle (``liboracle.so`` or a test's variant of it)."""
+    lib = ctypes.CDLL(path)
+    f = lib.oracle_block_attn
+    f.restype = ctypes.c_int
+    i32, vp = ctypes.c_int, ctypes.c_void_p
+    f.argtypes = [i32] * 10 + [ctypes.c_double] + [vp] * 6 + [i32] + [vp, vp, i32]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window, future_keys,
+               scale, req_ids=None, nthreads=0, lib=None):
+    """Return ``(out, lse2)`` in float64 for requests ``req_ids`` (all when None).
+
+    ``q``: uint16 bf16 bits ``[B, K, Hq, D]``; ``k_pages``/``v_pages``: uint16
+    ``[num_pages, Hkv, P, D]``; ``page_table``: int32 ``[B, max_pages]``;
+    ``ctx_lens``: int32 ``[B]``.  ``out`` is ``[n, K, Hq, D]``, ``lse2``
+    ``[n, K, Hq]`` with ``n = len(req_ids)`` (or B).
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_pages = np.ascontiguousarray(k_pages, dtype=np.uint16)
+    v_pages = np.ascontiguousarray(v_pages, dtype=np.uint16)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    ctx_lens = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    B, K, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_pages.shape
+    if K != block_size or D2 != D or v_pages.shape != k_pages.shape:
+        raise ValueError("inconsistent shapes")
+    if page_table.shape[0] != B or ctx_lens.shape != (B,):
+        raise ValueError("inconsistent batch")
+    if req_ids is not None:
+        req_ids = np.ascontiguousarray(req_ids, dtype=np.int32)
+        n = int(req_ids.shape[0])
+    else:
+        n = B
+    out = np.zeros((n, K, Hq, D), dtype=np.float64)
+    lse2 = np.zeros((n, K, Hq), dtype=np.float64)
+    rc = (lib or _load()).oracle_block_attn(
+        B, Hq, Hkv, D, P, page_table.shape[1], num_pages, K, int(window), int(future_keys),
+        float(scale), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(ctx_lens),
+        _ptr(req_ids), n, _ptr(out), _ptr(lse2), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_block_attn failed with status {rc}")
+    return out, lse2
+
+
+def bf16_bits_from_float(x) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even) and return the bits.
+
+    Used by tests to build exactly representable inputs; not part of the
+    attention arithmetic.
+    """
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    nan = np.isnan(f)
+    out = rounded.astype(np.uint16)
+    out[nan] = 0x7FC0
+    return out
+
+
+def bf16_bits_to_float(bits) -> np.ndarray:
+    """Widen bf16 bit patterns exactly to float32."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32)

@@ -1,0 +1,163 @@
+// Oracle for paged draft-block attention: plain, slow, fp64, CPU.
+//
+// TEST INFRASTRUCTURE ONLY.  The product path never links, loads or calls
+// this file; only the tests, the smoke check and the benchmark's CPU-baseline
+// leg do.  It shares no code, header, table or constant with the CUDA library.
+//
+// What it computes is the plain definition of the attention a draft block
+// takes in a DFlash / DSpark drafter (TensorRT-LLM PR #21130, "Non-causal
+// windowed DSpark draft block": description, "Why" and change 2; PR #20374,
+// "Non-causal unwindowed DFlash draft block": description).  For request b
+// with L = ctx_lens[b] context tokens and a block of K draft tokens stored in
+// the same pages at logical positions L .. L+K-1, query token i of the block
+// (position L+i) of query head hq, which reads kv head hq / G (G = Hq / Hkv),
+// sees
+//   * context positions p in [lo_i, L), lo_i = max(0, L+i-W+1) when a window
+//     W > 0 is given (the causal window (L+i-W, L+i]), else lo_i = 0;
+//   * block positions L+j for every j in [0, K) in the non-causal form
+//     (future_keys = 1), or for j in [0, i] in the causal form.
+// Every key row is read through the page table: the row of logical position p
+// is pages[page_table[b][p / P]][h][p % P][:] (HND page layout, PR #20374
+// kernel sweep: "page 32, HND").  Then, in double precision,
+//   s_p  = scale * sum_d q_d k_{p,d}
+//   m    = max_p s_p,   Z = sum_p exp(s_p - m)
+//   out  = sum_p exp(s_p - m) v_p / Z
+//   lse2 = (m + ln Z) / ln 2         (the base-2 log-sum-exp, PR #21130 change 1)
+// No blocking, splitting, merging or reordering beyond that definition.
+//
+// Inputs are bf16 bit patterns (uint16), widened exactly to double.
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+double bf16_to_double(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof(f));
+  return static_cast<double>(f);
+}
+
+struct Problem {
+  int B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys;
+  double scale;
+  const uint16_t* q;
+  const uint16_t* k_pages;
+  const uint16_t* v_pages;
+  const int32_t* page_table;
+  const int32_t* ctx_lens;
+};
+
+// Address of the key/value row of logical position p of request b, head h;
+// returns -1 when the page-table entry does not name a page of the pool.
+int64_t row_offset(const Problem& pr, int b, int h, int64_t p) {
+  const int64_t slot = p / pr.P;
+  if (slot < 0 || slot >= pr.max_pages) return -1;
+  const int32_t page = pr.page_table[static_cast<int64_t>(b) * pr.max_pages + slot];
+  if (page < 0 || page >= pr.num_pages) return -1;
+  return ((static_cast<int64_t>(page) * pr.Hkv + h) * pr.P + (p % pr.P)) * pr.D;
+}
+
+// One (request, query token, query head) row.  Returns 0 or a negative error.
+int attend_row(const Problem& pr, int b, int i, int hq, double* out_row, double* lse_row) {
+  const int G = pr.Hq / pr.Hkv;
+  const int h = hq / G;
+  const int64_t L = pr.ctx_lens[b];
+  if (L < 0) return -2;
+
+  // Visible logical positions, in increasing order.
+  std::vector<int64_t> pos;
+  const int64_t lo = (pr.W > 0) ? std::max<int64_t>(0, L + i - pr.W + 1) : 0;
+  for (int64_t p = lo; p < L; ++p) pos.push_back(p);
+  const int j_end = pr.future_keys ? pr.K : i + 1;
+  for (int j = 0; j < j_end; ++j) pos.push_back(L + j);
+
+  const uint16_t* qrow = pr.q + ((static_cast<int64_t>(b) * pr.K + i) * pr.Hq + hq) * pr.D;
+  std::vector<double> qd(pr.D);
+  for (int d = 0; d < pr.D; ++d) qd[d] = bf16_to_double(qrow[d]);
+
+  std::vector<double> s(pos.size());
+  std::vector<int64_t> off(pos.size());
+  for (size_t t = 0; t < pos.size(); ++t) {
+    off[t] = row_offset(pr, b, h, pos[t]);
+    if (off[t] < 0) return -3;
+    double acc = 0.0;
+    for (int d = 0; d < pr.D; ++d) acc += qd[d] * bf16_to_double(pr.k_pages[off[t] + d]);
+    s[t] = pr.scale * acc;
+  }
+
+  double m = -INFINITY;
+  for (double x : s) m = std::max(m, x);
+  double Z = 0.0;
+  for (double x : s) Z += std::exp(x - m);
+  for (int d = 0; d < pr.D; ++d) out_row[d] = 0.0;
+  for (size_t t = 0; t < pos.size(); ++t) {
+    const double w = std::exp(s[t] - m);
+    for (int d = 0; d < pr.D; ++d) out_row[d] += w * bf16_to_double(pr.v_pages[off[t] + d]);
+  }
+  for (int d = 0; d < pr.D; ++d) out_row[d] /= Z;
+  *lse_row = (m + std::log(Z)) / std::log(2.0);
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Computes out[n, i, hq, :] and lse2[n, i, hq] for the requests req_ids[0..n_req)
+// (every request 0..B-1 when req_ids is NULL, n_req then ignored and taken as B).
+// Threads: nthreads workers over (request, kv head) items; nthreads <= 0 means
+// std::thread::hardware_concurrency().  Returns 0, or -1 for bad sizes, -2 for a
+// negative context length, -3 for a visible position whose page-table entry is
+// out of range.
+int oracle_block_attn(int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
+                      int K, int W, int future_keys, double scale,
+                      const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                      const int32_t* page_table, const int32_t* ctx_lens,
+                      const int32_t* req_ids, int n_req,
+                      double* out, double* lse2, int nthreads) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0 || K <= 0 ||
+      W < 0 || max_pages <= 0 || num_pages <= 0)
+    return -1;
+  Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, scale,
+             q, k_pages, v_pages, page_table, ctx_lens};
+  if (req_ids == nullptr) n_req = B;
+  const int G = Hq / Hkv;
+  const int64_t n_items = static_cast<int64_t>(n_req) * Hkv;
+  std::atomic<int64_t> next{0};
+  std::atomic<int> status{0};
+
+  auto worker = [&]() {
+    for (;;) {
+      const int64_t it = next.fetch_add(1);
+      if (it >= n_items) return;
+      const int n = static_cast<int>(it / Hkv);
+      const int h = static_cast<int>(it % Hkv);
+      const int b = req_ids ? req_ids[n] : n;
+      if (b < 0 || b >= B) { status.store(-1); continue; }
+      for (int i = 0; i < K; ++i)
+        for (int g = 0; g < G; ++g) {
+          const int hq = h * G + g;
+          const int64_t row = (static_cast<int64_t>(n) * K + i) * Hq + hq;
+          const int rc = attend_row(pr, b, i, hq, out + row * D, lse2 + row);
+          if (rc != 0) status.store(rc);
+        }
+    }
+  };
+
+  if (nthreads <= 0) nthreads = static_cast<int>(std::thread::hardware_concurrency());
+  if (nthreads <= 0) nthreads = 1;
+  if (nthreads > n_items) nthreads = static_cast<int>(n_items > 0 ? n_items : 1);
+  std::vector<std::thread> pool;
+  for (int t = 1; t < nthreads; ++t) pool.emplace_back(worker);
+  worker();
+  for (auto& th : pool) th.join();
+  return status.load();
+}
+
+}  // extern "C"

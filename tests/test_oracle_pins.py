@@ -1,0 +1,381 @@
+"""Pins for the fp64 oracle: checks against what the pages and mathematics fix.
+
+None of these compares the oracle with itself re-typed: the dense cases use
+torch's own ``scaled_dot_product_attention`` and ``logsumexp`` (float64, CPU)
+over contiguous sequences with no page table; the merge pin composes two
+independent attentions; the closed forms are counted or averaged directly;
+the hand fixtures in ``tests/golden`` were derived on paper.
+"""
+
+import glob
+import json
+import math
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+
+from tests._paged import permute_pool, random_bf16, scatter_to_pages
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+LN2 = math.log(2.0)
+
+
+# ----------------------------------------------------------------------------
+# Dense library references (torch float64 on CPU, contiguous keys, no paging)
+# ----------------------------------------------------------------------------
+
+def visible_mask(L, K, W, future_keys):
+    """Boolean [K, L+K] mask of the pages' visible set, by position.
+
+    Query i sits at position L+i.  Causal window: (L+i-W, L+i] (all of
+    [0, L+i] when W = 0).  Non-causal form: every block key L..L+K-1 too.
+    """
+    pos = np.arange(L + K)
+    qpos = L + np.arange(K)[:, None]
+    causal = pos[None, :] <= qpos
+    if W > 0:
+        causal &= pos[None, :] > qpos - W
+    if future_keys:
+        return causal | (pos[None, :] >= L)
+    return causal
+
+
+def dense_attention(q_bits, k_bits, v_bits, scale, mask):
+    """torch SDPA + logsumexp in float64.  q [K,Hq,D], k/v [T,Hkv,D], mask [K,T]."""
+    import oracle
+
+    q = torch.from_numpy(oracle.bf16_bits_to_float(q_bits).astype(np.float64))
+    k = torch.from_numpy(oracle.bf16_bits_to_float(k_bits).astype(np.float64))
+    v = torch.from_numpy(oracle.bf16_bits_to_float(v_bits).astype(np.float64))
+    Hq, Hkv = q.shape[1], k.shape[1]
+    G = Hq // Hkv
+    qh = q.permute(1, 0, 2)                                  # [Hq, K, D]
+    kh = k.permute(1, 0, 2).repeat_interleave(G, dim=0)      # [Hq, T, D]
+    vh = v.permute(1, 0, 2).repeat_interleave(G, dim=0)
+    m = torch.from_numpy(mask)
+    out = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=m, scale=scale)
+    logits = (qh @ kh.transpose(1, 2)) * scale
+    logits = logits.masked_fill(~m, float("-inf"))
+    lse2 = torch.logsumexp(logits, dim=-1) / LN2              # [Hq, K]
+    return out.permute(1, 0, 2).numpy(), lse2.T.numpy()      # [K,Hq,D], [K,Hq]
+
+
+def make_case(rng, B, Hq, Hkv, D, K, P, lens, sigma=1.0, extra_pages=2, extra_slots=1):
+    q = random_bf16(rng, (B, K, Hq, D), sigma)
+    dk = [random_bf16(rng, (L + K, Hkv, D), sigma) for L in lens]
+    dv = [random_bf16(rng, (L + K, Hkv, D), sigma) for L in lens]
+    kp, vp, tab = scatter_to_pages(rng, dk, dv, P, Hkv, D, extra_pages, extra_slots)
+    return q, dk, dv, kp, vp, tab, np.asarray(lens, dtype=np.int32)
+
+
+TINY_SHAPES = [  # (Hq, Hkv, D, P)
+    (1, 1, 4, 1), (2, 1, 8, 4), (4, 2, 4, 8), (6, 3, 8, 3), (4, 4, 8, 5),
+]
+
+
+@pytest.mark.parametrize("shape", TINY_SHAPES)
+@pytest.mark.parametrize("K", [1, 2, 4])
+def test_unwindowed_equals_dense_full_attention(oracle_mod, shape, K):
+    """Unwindowed non-causal = textbook full attention over context + block."""
+    Hq, Hkv, D, P = shape
+    rng = np.random.default_rng(100 + 7 * K + D + P)
+    lens = [0, 1, 5, 17, 40][: 3 + K % 3]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    scale = 0.37
+    out, lse2 = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=0, future_keys=1,
+                                      scale=scale)
+    for b, L in enumerate(lens):
+        mask = np.ones((K, L + K), dtype=bool)
+        ro, rl = dense_attention(q[b], dk[b], dv[b], scale, mask)
+        np.testing.assert_allclose(out[b], ro, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("W", [0, 1, 3, 6, 50])
+@pytest.mark.parametrize("K", [1, 3, 4])
+def test_causal_block_equals_windowed_decode(oracle_mod, W, K):
+    """future_keys=0 (and K=1 in any form) is causal windowed decode, by position mask.
+
+    Only for W = 0 or W >= K: below that the causal window would drop block
+    keys the pages' non-causal definition keeps, and the library rejects it.
+    """
+    if 0 < W < K:
+        pytest.skip("0 < W < K is outside the defined range")
+    rng = np.random.default_rng(200 + W * 5 + K)
+    Hq, Hkv, D, P = 4, 2, 8, 4
+    lens = [0, 2, 7, 23, 31]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    forms = [0] + ([1] if K == 1 else [])
+    for fk in forms:
+        out, lse2 = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W,
+                                          future_keys=fk, scale=0.5)
+        for b, L in enumerate(lens):
+            ro, rl = dense_attention(q[b], dk[b], dv[b], 0.5, visible_mask(L, K, W, 0))
+            np.testing.assert_allclose(out[b], ro, rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("W", [4, 5, 9, 64])
+@pytest.mark.parametrize("K", [2, 4])
+def test_noncausal_window_equals_masked_dense(oracle_mod, W, K):
+    """Non-causal windowed: window (L+i-W, L+i] plus every block key."""
+    rng = np.random.default_rng(300 + W + K)
+    Hq, Hkv, D, P = 6, 2, 8, 4
+    lens = [0, 3, 9, 21, 40]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    out, lse2 = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W, future_keys=1,
+                                      scale=0.41)
+    for b, L in enumerate(lens):
+        ro, rl = dense_attention(q[b], dk[b], dv[b], 0.41, visible_mask(L, K, W, 1))
+        np.testing.assert_allclose(out[b], ro, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("W", [0, 5, 12])
+def test_lse_merge_of_disjoint_key_sets(oracle_mod, W):
+    """Non-causal = causal part merged with the later block keys by base-2 LSE.
+
+    Checks both the log-sum-exp form and the sigmoid/lerp form of the same
+    two-way merge (PR #21130, formulation table: einsum + sigmoid/lerp).
+    """
+    rng = np.random.default_rng(400 + W)
+    Hq, Hkv, D, P, K = 4, 1, 8, 4, 4
+    lens = [1, 6, 19, 30]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    s = 0.6
+    full, full_lse = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W,
+                                           future_keys=1, scale=s)
+    part, part_lse = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W,
+                                           future_keys=0, scale=s)
+    for b, L in enumerate(lens):
+        for i in range(K - 1):
+            fmask = np.zeros((K, L + K), dtype=bool)
+            fmask[:, L + i + 1:] = True
+            ob, lb = dense_attention(q[b], dk[b], dv[b], s, fmask)
+            oa, la = part[b, i], part_lse[b, i]
+            ob, lb = ob[i], lb[i]
+            lse = np.logaddexp2(la, lb)
+            merged = oa * np.exp2(la - lse)[:, None] + ob * np.exp2(lb - lse)[:, None]
+            np.testing.assert_allclose(full[b, i], merged, rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(full_lse[b, i], lse, rtol=1e-12, atol=1e-12)
+            sig = 1.0 / (1.0 + np.exp(-(lb - la) * LN2))
+            lerp = oa + sig[:, None] * (ob - oa)
+            np.testing.assert_allclose(full[b, i], lerp, rtol=1e-10, atol=1e-11)
+        # The last row has no later key: both forms agree exactly.
+        np.testing.assert_array_equal(full[b, K - 1], part[b, K - 1])
+        np.testing.assert_array_equal(full_lse[b, K - 1], part_lse[b, K - 1])
+
+
+@pytest.mark.parametrize("W", [0, 7])
+def test_page_permutation_invariance_bitwise(oracle_mod, W):
+    rng = np.random.default_rng(500 + W)
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, 3, 8, 2, 8, 3, 4, [5, 13, 22], extra_pages=5)
+    a = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=3, window=W, future_keys=1, scale=0.3)
+    kp2, vp2, tab2 = permute_pool(rng, kp, vp, tab)
+    b = oracle_mod.block_attn(q, kp2, vp2, tab2, ctx, block_size=3, window=W, future_keys=1,
+                              scale=0.3)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_thread_count_invariance_bitwise(oracle_mod):
+    rng = np.random.default_rng(600)
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, 5, 6, 3, 8, 2, 4, [0, 4, 9, 15, 33])
+    a = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=2, window=6, future_keys=1,
+                              scale=0.3, nthreads=1)
+    b = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=2, window=6, future_keys=1,
+                              scale=0.3, nthreads=7)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_request_subset_matches_full_batch(oracle_mod):
+    rng = np.random.default_rng(601)
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, 5, 4, 2, 8, 3, 4, [3, 4, 9, 15, 33])
+    full = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=3, window=0, future_keys=1,
+                                 scale=0.3)
+    ids = np.array([4, 1], dtype=np.int32)
+    sub = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=3, window=0, future_keys=1,
+                                scale=0.3, req_ids=ids)
+    np.testing.assert_array_equal(sub[0], full[0][ids])
+    np.testing.assert_array_equal(sub[1], full[1][ids])
+
+
+# ----------------------------------------------------------------------------
+# Closed forms
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("W,fk", [(0, 1), (0, 0), (6, 1), (6, 0), (3, 1)])
+def test_zero_query_gives_mean_and_log2_count(oracle_mod, W, fk):
+    """q = 0: uniform weights, out = mean of the visible V rows, lse2 = log2(count)."""
+    rng = np.random.default_rng(700 + W + fk)
+    K, Hq, Hkv, D, P = 3, 2, 1, 4, 4
+    lens = [0, 2, 5, 11]
+    _, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    q = np.zeros((len(lens), K, Hq, D), dtype=np.uint16)
+    out, lse2 = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W,
+                                      future_keys=fk, scale=1.0)
+    import oracle
+
+    for b, L in enumerate(lens):
+        vals = oracle.bf16_bits_to_float(dv[b]).astype(np.float64)   # [L+K, Hkv, D]
+        for i in range(K):
+            lo = max(0, L + i - W + 1) if W > 0 else 0
+            block = list(range(L, L + K)) if fk else list(range(L, L + i + 1))
+            rows = list(range(lo, L)) + block
+            n = (L - lo) + (K if fk else i + 1)
+            assert len(rows) == n
+            np.testing.assert_allclose(out[b, i, :, :], np.broadcast_to(vals[rows, 0].mean(0), (Hq, D)),
+                                       rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(lse2[b, i], np.full(Hq, math.log2(n)), rtol=0, atol=1e-12)
+
+
+def test_constant_values_give_constant_output(oracle_mod):
+    rng = np.random.default_rng(800)
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, 3, 4, 2, 8, 3, 4, [0, 6, 17])
+    import oracle
+
+    c = oracle.bf16_bits_from_float(np.float32(1.5))
+    vp = np.where(vp == 0x7FC0, vp, c).astype(np.uint16)
+    out, _ = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=3, window=5, future_keys=1,
+                                   scale=0.7)
+    np.testing.assert_allclose(out, 1.5, rtol=1e-14, atol=0)
+
+
+def test_short_context_window_equals_unwindowed(oracle_mod):
+    """With L <= W-K no window edge is inside the sequence: the two forms coincide."""
+    rng = np.random.default_rng(900)
+    K, W = 3, 12
+    lens = [0, 4, 9]                     # all <= W - K
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, 3, 4, 1, 8, K, 4, lens)
+    a = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W, future_keys=1, scale=0.5)
+    b = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=0, future_keys=1, scale=0.5)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_empty_context_is_attention_over_the_block(oracle_mod):
+    rng = np.random.default_rng(901)
+    K = 4
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, 1, 4, 2, 8, K, 3, [0])
+    out, lse2 = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=7, future_keys=1,
+                                      scale=0.9)
+    ro, rl = dense_attention(q[0], dk[0], dv[0], 0.9, np.ones((K, K), dtype=bool))
+    np.testing.assert_allclose(out[0], ro, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse2[0], rl, rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# Hand-derived fixtures
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(GOLDEN, "*.json"))))
+def test_hand_derived_fixture(oracle_mod, path):
+    import oracle
+
+    fx = json.load(open(path))
+    P, Hkv, D = fx["P"], fx["Hkv"], fx["D"]
+    table = np.asarray(fx["page_table"], dtype=np.int32)
+    num_pages = int(table.max()) + 1
+    kp = np.full((num_pages, Hkv, P, D), 0x7FC0, dtype=np.uint16)   # unused slots are NaN
+    vp = kp.copy()
+    kpos = np.asarray(fx["kv_positions"]["k"], dtype=np.float32)
+    vpos = np.asarray(fx["kv_positions"]["v"], dtype=np.float32)
+    for p in range(kpos.shape[0]):
+        pg = table[0, p // P]
+        kp[pg, 0, p % P] = oracle.bf16_bits_from_float(kpos[p])
+        vp[pg, 0, p % P] = oracle.bf16_bits_from_float(vpos[p])
+    q = oracle.bf16_bits_from_float(np.asarray(fx["q"], dtype=np.float32))
+    out, lse2 = oracle_mod.block_attn(q, kp, vp, table, np.asarray(fx["ctx_lens"], dtype=np.int32),
+                                      block_size=fx["K"], window=fx["window"],
+                                      future_keys=fx["future_keys"], scale=fx["scale"])
+    np.testing.assert_allclose(out, np.asarray(fx["expected_out"]), rtol=0, atol=fx["tolerance"])
+    np.testing.assert_allclose(lse2, np.asarray(fx["expected_lse2"]), rtol=0, atol=fx["tolerance"])
+
+
+# ----------------------------------------------------------------------------
+# Errors
+# ----------------------------------------------------------------------------
+
+def test_errors(oracle_mod):
+    rng = np.random.default_rng(950)
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, 2, 2, 1, 4, 2, 4, [3, 6])
+    bad = tab.copy()
+    bad[1, 0] = kp.shape[0] + 3
+    with pytest.raises(ValueError, match="-3"):
+        oracle_mod.block_attn(q, kp, vp, bad, ctx, block_size=2, window=0, future_keys=1, scale=1.0)
+    with pytest.raises(ValueError, match="-2"):
+        oracle_mod.block_attn(q, kp, vp, tab, np.array([3, -1], np.int32), block_size=2, window=0,
+                              future_keys=1, scale=1.0)
+    # A table entry only outside the window is never read.
+    tw = tab.copy()
+    tw[1, 0] = -1          # positions 0..3 of request 1 (L=6); W=2 reads from position 5 on
+    oracle_mod.block_attn(q, kp, vp, tw, ctx, block_size=2, window=2, future_keys=1, scale=1.0)
+
+
+# ----------------------------------------------------------------------------
+# Sensitivity: plausible mistakes planted in a copy of the oracle must fail a pin
+# ----------------------------------------------------------------------------
+
+MUTANTS = [
+    ("window off by one", "L + i - pr.W + 1", "L + i - pr.W"),
+    ("future keys include only j < i", "pr.future_keys ? pr.K : i + 1", "pr.future_keys ? pr.K : i"),
+    ("wrong GQA head map", "const int h = hq / G;", "const int h = hq % pr.Hkv;"),
+    ("page slot / offset swapped", "(p % pr.P)) * pr.D", "(p / pr.P) % pr.P) * pr.D"),
+    ("scale dropped", "s[t] = pr.scale * acc;", "s[t] = acc;"),
+    ("natural-log LSE", "/ std::log(2.0)", "/ 1.0"),
+    ("max not subtracted in numerator", "const double w = std::exp(s[t] - m);",
+     "const double w = std::exp(s[t]);"),
+]
+
+
+def _pins_pass(lib) -> bool:
+    """A compact set of the pins above, run against an arbitrary oracle build."""
+    import oracle
+
+    rng = np.random.default_rng(1234)
+    try:
+        for (Hq, Hkv, D, P, K, W, fk, lens) in [
+            (4, 2, 8, 4, 3, 0, 1, [0, 5, 14]),
+            (4, 2, 8, 4, 3, 5, 0, [2, 9, 20]),
+            (6, 3, 8, 3, 4, 6, 1, [1, 7, 25]),
+        ]:
+            q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+            out, lse2 = oracle.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W,
+                                          future_keys=fk, scale=0.45, lib=lib)
+            for b, L in enumerate(lens):
+                ro, rl = dense_attention(q[b], dk[b], dv[b], 0.45, visible_mask(L, K, W, fk))
+                if not (np.allclose(out[b], ro, rtol=1e-10, atol=1e-11) and
+                        np.allclose(lse2[b], rl, rtol=1e-10, atol=1e-11)):
+                    return False
+        # closed form: q = 0, large-magnitude keys do not matter, lse2 = log2(count)
+        q = np.zeros((1, 2, 2, 4), dtype=np.uint16)
+        kbig = oracle.bf16_bits_from_float(np.full((12, 1, 4), 40.0, np.float32))
+        kp, vp, tab = scatter_to_pages(rng, [kbig], [kbig], 4, 1, 4)
+        out, lse2 = oracle.block_attn(q, kp, vp, tab, np.array([10], np.int32), block_size=2,
+                                      window=0, future_keys=1, scale=1.0, lib=lib)
+        if not (np.allclose(lse2, math.log2(12), atol=1e-12) and np.allclose(out, 40.0)):
+            return False
+    except ValueError:
+        return False
+    return True
+
+
+def test_pins_reject_planted_mistakes(oracle_mod, tmp_path):
+    import oracle
+
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "dflash_oracle.cpp")).read()
+    assert _pins_pass(oracle._load()), "the unmodified oracle must pass the compact pins"
+    for name, old, new in MUTANTS:
+        assert src.count(old) == 1, name
+        path = tmp_path / (name.replace(" ", "_").replace("/", "") + ".cpp")
+        path.write_text(src.replace(old, new))
+        so = str(path) + ".so"
+        subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-pthread", str(path), "-o", so],
+                       check=True)
+        lib = oracle.load_library(so)
+        assert not _pins_pass(lib), f"planted mistake not caught: {name}"
