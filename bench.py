@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark of paged draft-block attention (one call = split kernel + combine).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  ``value`` is the algorithmic KV-read
+bandwidth of the whole job in GB/s (K and V rows each read once per call,
+summed over ranks, divided by the slowest rank's device time); ``us_per_call``
+is the mean device time of one call.  Inputs are resident in HBM when the
+timed region starts and L2 is flushed (a 512 MiB write) before every timed
+call, outside its CUDA-event pair.
+
+Workloads (``--workload``): ``tiny``, ``minimax_B{B}_K{K}_L{L}`` (16/1 heads,
+D=128, W=4096, page 64), ``adp_B{B}_K{K}_L{L}`` (64/4 heads, 1 % key outliers),
+``longctx_{8|12}x2_B{B}_L{L}`` (D=64, page 32, unwindowed),
+``ragged_B{B}`` (64/16 heads, contexts uniform in [1K, 128K]).  The default is
+the MiniMax-style windowed TP rank at its largest point: B=64, K=7, L=16384.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores (the slow baseline arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft-block attention µs/call and KV-read HBM GB/s (% of GB300 peak)"
+DEFAULT_WORKLOAD = "minimax_B64_K7_L16384"
+L2_FLUSH_BYTES = 512 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def workload_spec(name: str, seed_offset: int = 0):
+    from speculative_decoding_draft_paged_gb300 import workloads as W
+
+    if name == "tiny":
+        return W.tiny(seed=1001 + seed_offset)
+    m = re.fullmatch(r"minimax_B(\d+)_K(\d+)_L(\d+)", name)
+    if m:
+        return W.minimax(B=int(m[1]), K=int(m[2]), L=int(m[3]), seed=1002 + seed_offset)
+    m = re.fullmatch(r"adp_B(\d+)_K(\d+)_L(\d+)", name)
+    if m:
+        return W.adp(B=int(m[1]), K=int(m[2]), L=int(m[3]), seed=1003 + seed_offset)
+    m = re.fullmatch(r"longctx_(\d+)x2_B(\d+)_L(\d+)", name)
+    if m:
+        return W.longctx(B=int(m[2]), L=int(m[3]), Hq=int(m[1]), seed=1004 + seed_offset)
+    m = re.fullmatch(r"ragged_B(\d+)", name)
+    if m:
+        return W.ragged(B=int(m[1]), seed=1005 + seed_offset)
+    raise SystemExit(f"unknown workload {name!r}")
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_sha() -> str:
+    from speculative_decoding_draft_paged_gb300 import build as B
+
+    h = hashlib.sha256()
+    for p in sorted(B._deps()):
+        if p.endswith("build.py"):
+            continue
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources are unchanged since it was taken."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_oracle_sample(spec, budget_s: float = 15.0, device_inputs=None):
+    """Run the oracle on a bounded sample of the workload's requests.
+
+    Returns (kv_bytes_per_s, seconds, n_requests, threads, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from speculative_decoding_draft_paged_gb300 import workloads as W
+
+    threads = os.cpu_count() or 1
+    # Estimated oracle cost: ~4 flops per (row, key, dim), ~0.5 GFLOP/s per core.
+    per_req = [spec.Hq * spec.K * (spec.visible_ctx(L) + spec.K) * spec.D * 4 for L in spec.ctx_lens]
+    rate = 0.5e9 * threads
+    ids, cost = [], 0.0
+    for b in range(spec.B):
+        if ids and cost + per_req[b] / rate > budget_s:
+            break
+        ids.append(b)
+        cost += per_req[b] / rate
+    sub = W.CaseSpec(spec.name + "_sample", B=len(ids), Hq=spec.Hq, Hkv=spec.Hkv, D=spec.D, K=spec.K,
+                     P=spec.P, window=spec.window, future_keys=spec.future_keys,
+                     ctx_lens=[spec.ctx_lens[b] for b in ids], sigma=spec.sigma,
+                     outlier_frac=spec.outlier_frac, seed=spec.seed)
+    inp = W.make_inputs(sub, "cpu")
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    args = (bits(inp["q"]), bits(inp["k_pages"]), bits(inp["v_pages"]), inp["page_table"].numpy(),
+            inp["ctx_lens"].numpy())
+    t0 = time.perf_counter()
+    oracle.block_attn(*args, block_size=sub.K, window=sub.window, future_keys=sub.future_keys,
+                      scale=sub.softmax_scale, nthreads=threads)
+    dt = time.perf_counter() - t0
+    desc = f"{len(ids)} of {spec.B} requests (same shapes and lengths), fp64, {threads} threads"
+    return sub.kv_bytes() / dt, dt, len(ids), threads, desc
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    spec = workload_spec(args.workload)
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    vals, times = [], []
+    cores = None
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        v, dt, n, cores, desc = time_oracle_sample(spec, budget_s=budget)
+        if i >= args.warmup:
+            vals.append(v)
+            times.append(dt)
+    gbs = sum(vals) / len(vals) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(spec.describe(), parallelism="replicas"),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_draft_paged_gb300 as dflash
+    from speculative_decoding_draft_paged_gb300 import build as B
+    from speculative_decoding_draft_paged_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+
+    # Weak scaling: every rank runs the same-sized workload on its own GPU with
+    # its own seed; the attention has no cross-request exchange.
+    spec = workload_spec(args.workload, seed_offset=100 * rank)
+    inp = W.make_inputs(spec, dev)
+    p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K,
+                          window=spec.window, future_keys=spec.future_keys,
+                          scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len)
+    plan = dflash.plan(p)
+    ws_bytes = dflash.workspace_size(p)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty(inp["q"].shape[:3], dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        rc = dflash.block_attn_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
+                                   inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(),
+                                   inp["ctx_lens"].data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   ws.data_ptr(), ws_bytes, torch.cuda.current_stream().cuda_stream)
+        if rc != 0:
+            raise dflash.DflashError(rc)
+
+    # Capture one call in a CUDA graph (the grid depends on the parameters only).
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        call()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        graph.replay()
+    torch.cuda.synchronize()
+    if dflash.read_device_status(ws) != 0:
+        raise SystemExit("device status flags set during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        starts[k].record(stream)
+        graph.replay()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(call_ms) / len(call_ms)
+
+    # Split-kernel duration (the dominant kernel) with events on its stream.
+    k_ms = []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for k in range(max(3, min(args.steps, 20))):
+        flush.fill_(k & 0xFF)
+        rc = dflash.block_attn_timed_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
+                                         inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(),
+                                         inp["ctx_lens"].data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                         ws.data_ptr(), ws_bytes, stream.cuda_stream, e0, e1)
+        if rc != 0:
+            raise dflash.DflashError(rc)
+        e1.synchronize()
+        k_ms.append(e0.elapsed_time(e1))
+    split_ms = sorted(k_ms)[len(k_ms) // 2]
+
+    # End to end through the public API: per step, copy q / page table /
+    # lengths from pinned host memory, run the call, read out and lse2 back.
+    h_q = inp["q"].cpu().pin_memory()
+    h_tab = inp["page_table"].cpu().pin_memory()
+    h_len = inp["ctx_lens"].cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = h_q.numel() * 2 + h_tab.numel() * 4 + h_len.numel() * 4
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for k in range(args.warmup + args.steps):
+        flush.fill_(k & 0xFF)
+        if k >= args.warmup:
+            ee[k - args.warmup][0].record(stream)
+        inp["q"].copy_(h_q, non_blocking=True)
+        inp["page_table"].copy_(h_tab, non_blocking=True)
+        inp["ctx_lens"].copy_(h_len, non_blocking=True)
+        call()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        if k >= args.warmup:
+            ee[k - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ee) / len(ee)
+
+    # Max over ranks (time) and sum (bytes) for the whole-job figures.
+    kv_bytes = spec.kv_bytes()
+    vals = torch.tensor([ms, split_ms, e2e_ms, float(kv_bytes)], dtype=torch.float64, device=dev)
+    if world > 1:
+        t = vals[:3].clone()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        s = vals[3:].clone()
+        dist.all_reduce(s, op=dist.ReduceOp.SUM)
+        vals = torch.cat([t, s])
+    ms, split_ms, e2e_ms, total_bytes = [float(x) for x in vals.tolist()]
+
+    peaks = measured_peaks()
+    gbs = total_bytes / (ms * 1e-3) / 1e9
+    split_gbs = kv_bytes / (split_ms * 1e-3) / 1e9
+    kernel = "split_tc" if plan["path"] == dflash.PATH_TCGEN05 else "split_mma"
+    traffic = stored_traffic(spec.name, kernel)
+
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_call": ms * 1e3,
+        "pct_of_peak_hbm": 100.0 * gbs / world / peaks["hbm_gbs"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 pages, random page permutation)",
+        "config": dict(spec.describe(), parallelism=f"replicas{world}",
+                       l2="flushed before every timed call (512 MiB write)",
+                       kv_bytes_per_call=kv_bytes, path=kernel, split_tiles=plan["split_tiles"],
+                       max_splits=plan["max_splits"], ctas=plan["units"], cuda_graph=True),
+        "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": split_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": kernel, "kernel_us": split_ms * 1e3,
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
+                     if peaks["source"] == "measured" else "fallback 6.8 TB/s"},
+        "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, n, cores, desc = time_oracle_sample(spec)
+        line["cpu_baseline"] = {"value": v / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,170 @@
+/*
+ * dflash.h -- paged draft-block attention for block speculative decoding
+ * (DFlash / DSpark drafters), GB300 (sm_103a).
+ *
+ * One call computes, for every request of a batch, the attention of the K
+ * draft-block query tokens of every query head over the request's paged
+ * context keys plus the K block keys, and returns the bf16 output and the
+ * fp32 base-2 log-sum-exp.  The operation is the one the TensorRT-LLM pages
+ * describe:
+ *   - non-causal unwindowed block (PR #20374 "Non-causal unwindowed DFlash
+ *     draft block", description): every block query sees the whole context
+ *     and the whole block;
+ *   - non-causal windowed block (PR #21130 "Non-causal windowed DSpark draft
+ *     block", description "Why" and change 2): query i at position L+i sees
+ *     the context keys of the causal window (L+i-W, L+i] plus every block key;
+ *     the block keys after i are folded in by a base-2 log-sum-exp merge,
+ *     which is skipped exactly when no later key exists (K = 1, or the causal
+ *     form);
+ *   - the causal block (future_keys = 0): the causal (windowed) decode alone.
+ * The softmax statistics are returned as base-2 LSE (PR #21130 change 1) and
+ * the caller sizes a workspace that includes the partial softmax statistics
+ * (PR #21130 change 3); sequence lengths stay on the device so one captured
+ * CUDA graph serves every step (PR #20374, "The batch size is static inside a
+ * captured CUDA graph"; PR #16150 "Read the draft context K/V directly from
+ * the target KV cache manager's paged pool": device-resident lengths).
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no device
+ * or host memory, keeps no state beyond cached device attributes and the
+ * per-kernel shared-memory opt-in, is thread-safe, and issues only
+ * stream-ordered work (no host synchronisation) in dflash_block_attn.
+ *
+ * Errors are host-side return codes; nothing is launched when a code other
+ * than DFLASH_OK is returned by validation.  Bad data found on the device (a
+ * page id outside the pool, a context length outside [0, max_ctx_len]) never
+ * traps: the kernels substitute zeros or clamp, record a flag in the
+ * workspace status word and finish.
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define DFLASH_OK                    0
+#define DFLASH_ERR_INVALID          -1  /* bad sizes, null or misaligned pointer */
+#define DFLASH_ERR_WORKSPACE        -2  /* workspace smaller than dflash_workspace_size */
+#define DFLASH_ERR_DEVICE           -3  /* current device is not compute capability 10.3 */
+#define DFLASH_ERR_LAUNCH           -4  /* a CUDA call or kernel launch failed */
+
+/* Device status flags (OR-ed into the workspace status word by the kernels). */
+#define DFLASH_STATUS_BAD_PAGE       1  /* a visible position's page id is outside [0, num_pages) */
+#define DFLASH_STATUS_BAD_CTX_LEN    2  /* ctx_lens[b] < 0 or > max_ctx_len (clamped) */
+#define DFLASH_STATUS_TIMEOUT        4  /* a pipeline wait ran out (never expected) */
+
+/* Kernel-path selection for dflash_params.force_path. */
+#define DFLASH_PATH_AUTO             0
+#define DFLASH_PATH_MMA              1  /* warp-level mma.sync tiles (any R <= 128) */
+#define DFLASH_PATH_TCGEN05          2  /* tcgen05 / TMEM, one 128-row tile per kv head */
+
+typedef struct dflash_params {
+  int32_t batch;             /* B >= 1 requests */
+  int32_t num_q_heads;       /* Hq; Hq % Hkv == 0 */
+  int32_t num_kv_heads;      /* Hkv >= 1; G = Hq / Hkv query heads share one kv head */
+  int32_t head_dim;          /* D: 64 or 128 */
+  int32_t page_size;         /* P tokens per page: 16, 32 or 64 */
+  int32_t max_pages_per_req; /* row stride of page_table */
+  int32_t num_pages;         /* pages in the K pool (and in the V pool) */
+  int32_t block_size;        /* K draft tokens per request, 1..16; G*K <= 128 */
+  int32_t window;            /* W: 0 = unwindowed; W >= K = causal window (L+i-W, L+i] */
+  int32_t future_keys;       /* 1: non-causal block (all K block keys); 0: causal block */
+  float   scale;             /* softmax scale, applied to q.k in fp32 */
+  int32_t max_ctx_len;       /* host bound on every ctx_lens[b]; sizes the plan */
+  int32_t force_path;        /* DFLASH_PATH_*; 0 picks by the packed row count */
+  int32_t force_split_tiles; /* > 0: key tiles per split unit (tests); 0 = planner */
+  int32_t reserved[4];       /* must be zero */
+} dflash_params;
+
+/* What the planner chose for a parameter set (for tests and benchmarks). */
+typedef struct dflash_plan_info {
+  int32_t path;              /* DFLASH_PATH_MMA or DFLASH_PATH_TCGEN05 */
+  int32_t rows;              /* R = G*K packed query rows per kv head */
+  int32_t rows_padded;       /* R rounded up to the kernel's row granule */
+  int32_t tile_keys;         /* T: keys per pipeline stage */
+  int32_t split_tiles;       /* C: key tiles per split unit */
+  int32_t max_splits;        /* split units per (request, kv head) */
+  int64_t units;             /* B * Hkv * max_splits CTAs of the split kernel */
+  int32_t threads;           /* threads per CTA of the split kernel */
+  int32_t smem_bytes;        /* dynamic shared memory per CTA of the split kernel */
+  int32_t num_sms;           /* SM count the plan was sized for */
+  int32_t reserved[3];
+} dflash_plan_info;
+
+/*
+ * Workspace bytes dflash_block_attn needs for *p on the current device: a
+ * 256-byte header (status word) plus the fp32 partial softmax state of every
+ * split unit (normalised output [units, R, D] and base-2 LSE [units, R]).
+ * Returns 0 when *p is invalid.  Deterministic for a given device model.
+ */
+size_t dflash_workspace_size(const dflash_params* p);
+
+/* Fills *info with the plan for *p.  Returns DFLASH_OK or DFLASH_ERR_INVALID. */
+int dflash_plan(const dflash_params* p, dflash_plan_info* info);
+
+/*
+ * The attention call.  All pointers are device pointers on the current
+ * device, 16-byte aligned; `stream` is a cudaStream_t (NULL = legacy default
+ * stream).
+ *   q          bf16 [B, K, Hq, D]              query rows, token-major
+ *   k_pages    bf16 [num_pages, Hkv, P, D]     key pool (HND pages)
+ *   v_pages    bf16 [num_pages, Hkv, P, D]     value pool (HND pages)
+ *   page_table int32 [B, max_pages_per_req]    page id of each P-token slot;
+ *              only slots holding a visible position are read
+ *   ctx_lens   int32 [B]                       L_b: context tokens before the
+ *              block; the block's K/V are already stored at positions
+ *              L_b .. L_b+K-1 of the same pages.  Read on the device only.
+ *   out        bf16 [B, K, Hq, D]              softmax(q.k * scale) v, RNE
+ *   lse2       fp32 [B, K, Hq]                 log2 sum exp(scale q.k) over
+ *              the visible keys (including the merged later block keys)
+ *   workspace  device scratch of workspace_bytes >= dflash_workspace_size(p);
+ *              contents need not be initialised; the status word in it is
+ *              OR-ed, never cleared, by this call.
+ * Returns DFLASH_OK, or an error code with nothing launched (validation) or
+ * DFLASH_ERR_LAUNCH.  Capturable in a CUDA graph: the grid depends on *p
+ * only, never on the values of ctx_lens or page_table.
+ */
+int dflash_block_attn(const dflash_params* p, const void* q, const void* k_pages,
+                      const void* v_pages, const int32_t* page_table, const int32_t* ctx_lens,
+                      void* out, float* lse2, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
+ * dflash_block_attn with per-kernel timing marks: `split_start` and
+ * `split_done` (cudaEvent_t, or NULL) are recorded on `stream` immediately
+ * before the split kernel and between the split kernel and the combine
+ * kernel.  The computation is the same; with `split_done` given the combine
+ * kernel starts after the event instead of overlapping the split kernel's
+ * tail (no programmatic dependent launch).  Same return codes.
+ */
+int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k_pages,
+                            const void* v_pages, const int32_t* page_table,
+                            const int32_t* ctx_lens, void* out, float* lse2, void* workspace,
+                            size_t workspace_bytes, void* stream, void* split_start,
+                            void* split_done);
+
+/* Static text for a return code. */
+const char* dflash_status_string(int status);
+
+/*
+ * Reads the device status word of a workspace (DFLASH_STATUS_* flags) with a
+ * stream-ordered copy and a synchronisation of `stream`.  Returns the flags,
+ * or a negative DFLASH_ERR_* code.
+ */
+int dflash_read_device_status(const void* workspace, void* stream);
+
+/* Clears the device status word of a workspace (stream-ordered memset). */
+int dflash_clear_device_status(void* workspace, void* stream);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int dflash_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H_ */

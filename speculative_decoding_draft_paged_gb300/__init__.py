@@ -1,0 +1,163 @@
+"""Paged draft-block attention for block speculative decoding on GB300.
+
+Thin Python binding over the C ABI of ``include/dflash.h`` (``libdflash.so``):
+it marshals torch tensors' device pointers and the current stream; every step
+of the computation runs in the library's CUDA kernels.  torch is used for
+device memory and streams only.
+
+    out, lse2 = block_attn(q, k_pages, v_pages, page_table, ctx_lens,
+                           block_size=K, window=W, future_keys=1, scale=s,
+                           max_ctx_len=Lmax)
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+from . import _lib
+from ._lib import (DFLASH_ERR_DEVICE, DFLASH_ERR_INVALID, DFLASH_ERR_LAUNCH, DFLASH_ERR_WORKSPACE,
+                   DFLASH_OK, DFLASH_STATUS_BAD_CTX_LEN, DFLASH_STATUS_BAD_PAGE,
+                   DFLASH_STATUS_TIMEOUT, PATH_AUTO, PATH_MMA, PATH_TCGEN05, Params, PlanInfo)
+
+__all__ = [
+    "Params", "PlanInfo", "DflashError", "make_params", "workspace_size", "plan", "block_attn",
+    "block_attn_raw", "block_attn_timed_raw", "read_device_status", "clear_device_status", "version", "PATH_AUTO",
+    "PATH_MMA", "PATH_TCGEN05", "DFLASH_OK", "DFLASH_ERR_INVALID", "DFLASH_ERR_WORKSPACE",
+    "DFLASH_ERR_DEVICE", "DFLASH_ERR_LAUNCH", "DFLASH_STATUS_BAD_PAGE",
+    "DFLASH_STATUS_BAD_CTX_LEN", "DFLASH_STATUS_TIMEOUT",
+]
+
+
+class DflashError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(f"dflash_block_attn: {_lib.status_string(code)} ({code})")
+
+
+def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_req,
+                num_pages, block_size, window, future_keys, scale, max_ctx_len, force_path=0,
+                force_split_tiles=0) -> Params:
+    p = Params()
+    p.batch = batch
+    p.num_q_heads = num_q_heads
+    p.num_kv_heads = num_kv_heads
+    p.head_dim = head_dim
+    p.page_size = page_size
+    p.max_pages_per_req = max_pages_per_req
+    p.num_pages = num_pages
+    p.block_size = block_size
+    p.window = window
+    p.future_keys = future_keys
+    p.scale = scale
+    p.max_ctx_len = max_ctx_len
+    p.force_path = force_path
+    p.force_split_tiles = force_split_tiles
+    return p
+
+
+def params_for(q, k_pages, page_table, *, block_size, window, future_keys, scale, max_ctx_len,
+               force_path=0, force_split_tiles=0) -> Params:
+    B, K, Hq, D = q.shape
+    num_pages, Hkv, P, _ = k_pages.shape
+    if K != block_size:
+        raise ValueError(f"q has {K} block tokens, block_size is {block_size}")
+    return make_params(batch=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P,
+                       max_pages_per_req=page_table.shape[1], num_pages=num_pages,
+                       block_size=block_size, window=window, future_keys=future_keys, scale=scale,
+                       max_ctx_len=max_ctx_len, force_path=force_path,
+                       force_split_tiles=force_split_tiles)
+
+
+def workspace_size(p: Params) -> int:
+    return int(_lib.load().dflash_workspace_size(ctypes.byref(p)))
+
+
+def plan(p: Params) -> dict:
+    info = PlanInfo()
+    rc = _lib.load().dflash_plan(ctypes.byref(p), ctypes.byref(info))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+    return {f: getattr(info, f) for f, _ in PlanInfo._fields_ if f != "reserved"}
+
+
+def version() -> int:
+    return int(_lib.load().dflash_version())
+
+
+def _stream_handle(stream) -> int:
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def block_attn_raw(p: Params, q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, out_ptr, lse_ptr, ws_ptr,
+                   ws_bytes, stream_handle) -> int:
+    """Direct C-ABI call with integer device pointers; returns the status code."""
+    return int(_lib.load().dflash_block_attn(ctypes.byref(p), q_ptr, k_ptr, v_ptr, table_ptr,
+                                             lens_ptr, out_ptr, lse_ptr, ws_ptr, ws_bytes,
+                                             stream_handle))
+
+
+def block_attn_timed_raw(p: Params, q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, out_ptr, lse_ptr,
+                         ws_ptr, ws_bytes, stream_handle, start_event, done_event) -> int:
+    """C-ABI call that records ``start_event``/``done_event`` (torch.cuda.Event)
+    around the split kernel; returns the status code."""
+    return int(_lib.load().dflash_block_attn_timed(
+        ctypes.byref(p), q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, out_ptr, lse_ptr, ws_ptr,
+        ws_bytes, stream_handle, start_event.cuda_event, done_event.cuda_event))
+
+
+def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size: int, window: int,
+               future_keys: int, scale: float, max_ctx_len: int, out=None, lse2=None,
+               workspace=None, stream=None, force_path: int = 0, force_split_tiles: int = 0):
+    """Draft-block attention over a paged bf16 KV cache.  Returns ``(out, lse2)``.
+
+    ``q [B,K,Hq,D]`` bf16, ``k_pages``/``v_pages [num_pages,Hkv,P,D]`` bf16,
+    ``page_table [B,max_pages]`` int32, ``ctx_lens [B]`` int32 (device),
+    all contiguous on the current CUDA device.  ``out``/``lse2``/``workspace``
+    are allocated when not given (``workspace``: uint8, ``workspace_size``
+    bytes).
+    """
+    import torch
+
+    p = params_for(q, k_pages, page_table, block_size=block_size, window=window,
+                   future_keys=future_keys, scale=scale, max_ctx_len=max_ctx_len,
+                   force_path=force_path, force_split_tiles=force_split_tiles)
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_pages", k_pages, torch.bfloat16),
+                        ("v_pages", v_pages, torch.bfloat16), ("page_table", page_table, torch.int32),
+                        ("ctx_lens", ctx_lens, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages differ in shape")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse2 is None:
+        lse2 = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    need = workspace_size(p)
+    if need == 0:
+        raise DflashError(DFLASH_ERR_INVALID)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    rc = block_attn_raw(p, q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                        page_table.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
+                        lse2.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+    return out, lse2
+
+
+def read_device_status(workspace, stream=None) -> int:
+    rc = int(_lib.load().dflash_read_device_status(workspace.data_ptr(), _stream_handle(stream)))
+    if rc < 0:
+        raise DflashError(rc)
+    return rc
+
+
+def clear_device_status(workspace, stream=None) -> None:
+    rc = int(_lib.load().dflash_clear_device_status(workspace.data_ptr(), _stream_handle(stream)))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)

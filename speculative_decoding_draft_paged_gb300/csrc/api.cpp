@@ -1,0 +1,338 @@
+// C ABI of the paged draft-block attention library (include/dflash.h):
+// argument validation, the split planner, workspace sizing, TMA descriptors
+// and the two launches (split kernel, combine kernel).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "dflash.h"
+#include "dflash_internal.h"
+
+namespace dflash {
+
+int split_mma_kpw(int D, int R_pad);
+int split_mma_tile_keys(int D);
+int split_tc_tile_keys(int D);
+int split_tc_threads();
+bool split_tc_available();
+
+namespace {
+
+constexpr int kDefaultSms = 152;       // GB300, used when no device can be queried
+constexpr int kMaxDevices = 64;
+constexpr int kSmemPerSm = 228 * 1024;
+
+struct DeviceInfo {
+  int sms = 0;
+  int cc = 0;  // major * 10 + minor
+  bool ok = false;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+DeviceInfo current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return DeviceInfo{};
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_dev[dev].ok) {
+    int sms = 0, major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return DeviceInfo{};
+    }
+    g_dev[dev].sms = sms;
+    g_dev[dev].cc = major * 10 + minor;
+    g_dev[dev].ok = true;
+  }
+  return g_dev[dev];
+}
+
+int plan_sms() {
+  const DeviceInfo d = current_device();
+  return d.ok ? d.sms : kDefaultSms;
+}
+
+bool params_valid(const dflash_params* p) {
+  if (p == nullptr) return false;
+  for (int r : p->reserved)
+    if (r != 0) return false;
+  if (p->batch < 1 || p->num_kv_heads < 1 || p->num_q_heads < p->num_kv_heads) return false;
+  if (p->num_q_heads % p->num_kv_heads != 0) return false;
+  if (p->head_dim != 64 && p->head_dim != 128) return false;
+  if (p->page_size != 16 && p->page_size != 32 && p->page_size != 64) return false;
+  if (p->block_size < 1 || p->block_size > kMaxBlock) return false;
+  const int64_t G = p->num_q_heads / p->num_kv_heads;
+  if (G * p->block_size > kMaxRows) return false;
+  if (p->window < 0 || (p->window > 0 && p->window < p->block_size)) return false;
+  if (p->future_keys != 0 && p->future_keys != 1) return false;
+  if (!std::isfinite(p->scale)) return false;
+  // Positions are 32-bit on the device: keep L + K + a tile well inside int32.
+  if (p->max_ctx_len < 0 || p->max_ctx_len > (1 << 30)) return false;
+  if (p->max_pages_per_req < 1 || p->num_pages < 1) return false;
+  if (static_cast<int64_t>(p->max_ctx_len) + p->block_size >
+      static_cast<int64_t>(p->max_pages_per_req) * p->page_size)
+    return false;
+  // One (page, head) slice of the pool is addressed with 32-bit TMA
+  // coordinates and a stride below 2^40 bytes.
+  if (static_cast<int64_t>(p->num_kv_heads) * p->page_size * p->head_dim * 2 >= (int64_t(1) << 40))
+    return false;
+  if (p->force_path < DFLASH_PATH_AUTO || p->force_path > DFLASH_PATH_TCGEN05) return false;
+  if (p->force_split_tiles < 0) return false;
+  return true;
+}
+
+// The planner.  The split kernel's grid is (max_splits, Hkv, B): it depends on
+// the parameters only, never on the device-resident lengths, so a captured
+// graph replays for any lengths up to max_ctx_len.  Each request's visible
+// key range is cut into units of C tiles; C is chosen so that the units of the
+// largest possible batch fill the GPU about twice over, but never so small
+// that the partial state written per unit outweighs the keys it covers.
+bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
+  if (!params_valid(p)) return false;
+  KernelPlan k{};
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const int D = p->head_dim;
+  k.R = G * p->block_size;
+  k.num_sms = num_sms;
+  int path = p->force_path;
+  if (path == DFLASH_PATH_AUTO)
+    path = (k.R > 64 && split_tc_available()) ? DFLASH_PATH_TCGEN05 : DFLASH_PATH_MMA;
+  if (path == DFLASH_PATH_TCGEN05 && !split_tc_available()) return false;
+  k.path = path;
+  if (path == DFLASH_PATH_MMA) {
+    k.R_pad = (k.R + 15) / 16 * 16;
+    k.T = split_mma_tile_keys(D);
+    k.kpw = split_mma_kpw(D, k.R_pad);
+    const int consumer_warps = (k.R_pad / 16) * (k.T / k.kpw);
+    k.threads = 32 * (1 + consumer_warps);
+    k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw);
+  } else {
+    k.R_pad = 128;
+    k.T = split_tc_tile_keys(D);
+    k.kpw = 0;
+    k.threads = split_tc_threads();
+    k.smem_bytes = split_tc_smem_bytes(D);
+  }
+  const int mt = max_tiles(p->max_ctx_len, p->block_size, p->window, k.T);
+  int C = p->force_split_tiles;
+  if (C <= 0) {
+    int ctas_per_sm = kSmemPerSm / (k.smem_bytes + 1024);
+    if (ctas_per_sm < 1) ctas_per_sm = 1;
+    const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 2;
+    const int64_t total = static_cast<int64_t>(p->batch) * p->num_kv_heads * mt;
+    int64_t c = (total + target - 1) / target;
+    // Partial state per unit is about R*D*4 bytes, written and read once
+    // (2*R*D*4), against C*T*D*4 bytes of K and V: keep it under 1/8 of them.
+    const int64_t c_min = (16 * static_cast<int64_t>(k.R) + k.T - 1) / k.T;
+    if (c < c_min) c = c_min;
+    if (c > 64) c = 64;
+    if (c > mt) c = mt;
+    if (c < 1) c = 1;
+    C = static_cast<int>(c);
+  }
+  k.C = C;
+  k.S = (mt + C - 1) / C;
+  k.units = static_cast<int64_t>(p->batch) * p->num_kv_heads * k.S;
+  if (k.S > 65535 || p->num_kv_heads > 65535 || p->batch > 65535) return false;
+  *out = k;
+  return true;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t workspace_bytes_for(const dflash_params* p, const KernelPlan& k) {
+  const size_t lse = align_up(static_cast<size_t>(k.units) * k.R * sizeof(float), 256);
+  const size_t o = static_cast<size_t>(k.units) * k.R * p->head_dim * sizeof(float);
+  return kHeaderBytes + lse + o;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode;
+}
+
+// 4-D view [num_pages][Hkv][P][D] of a page pool, box = (64 columns, P rows,
+// one head, one page), 128-byte swizzle, zero fill outside the pool.
+bool encode_pool(CUtensorMap* map, const void* pool, const dflash_params* p) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(p->head_dim),
+                              static_cast<cuuint64_t>(p->page_size),
+                              static_cast<cuuint64_t>(p->num_kv_heads),
+                              static_cast<cuuint64_t>(p->num_pages)};
+  const cuuint64_t row = static_cast<cuuint64_t>(p->head_dim) * 2;
+  const cuuint64_t strides[3] = {row, row * p->page_size, row * p->page_size * p->num_kv_heads};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(p->page_size), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+}  // namespace
+}  // namespace dflash
+
+using namespace dflash;
+
+extern "C" {
+
+size_t dflash_workspace_size(const dflash_params* p) {
+  KernelPlan k;
+  if (!make_plan(p, plan_sms(), &k)) return 0;
+  return workspace_bytes_for(p, k);
+}
+
+int dflash_plan(const dflash_params* p, dflash_plan_info* info) {
+  KernelPlan k;
+  if (info == nullptr || !make_plan(p, plan_sms(), &k)) return DFLASH_ERR_INVALID;
+  std::memset(info, 0, sizeof(*info));
+  info->path = k.path;
+  info->rows = k.R;
+  info->rows_padded = k.R_pad;
+  info->tile_keys = k.T;
+  info->split_tiles = k.C;
+  info->max_splits = k.S;
+  info->units = k.units;
+  info->threads = k.threads;
+  info->smem_bytes = k.smem_bytes;
+  info->num_sms = k.num_sms;
+  return DFLASH_OK;
+}
+
+int dflash_block_attn(const dflash_params* p, const void* q, const void* k_pages,
+                      const void* v_pages, const int32_t* page_table, const int32_t* ctx_lens,
+                      void* out, float* lse2, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return dflash_block_attn_timed(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2,
+                                 workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k_pages,
+                            const void* v_pages, const int32_t* page_table,
+                            const int32_t* ctx_lens, void* out, float* lse2, void* workspace,
+                            size_t workspace_bytes, void* stream, void* split_start,
+                            void* split_done) {
+  if (!params_valid(p)) return DFLASH_ERR_INVALID;
+  if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !out || !lse2 || !workspace)
+    return DFLASH_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+      !aligned(page_table, 4) || !aligned(ctx_lens, 4) || !aligned(lse2, 4) ||
+      !aligned(workspace, 256))
+    return DFLASH_ERR_INVALID;
+  const DeviceInfo dev = current_device();
+  if (!dev.ok) return DFLASH_ERR_LAUNCH;
+  if (dev.cc != 103) return DFLASH_ERR_DEVICE;
+  KernelPlan k;
+  if (!make_plan(p, dev.sms, &k)) return DFLASH_ERR_INVALID;
+  if (workspace_bytes < workspace_bytes_for(p, k)) return DFLASH_ERR_WORKSPACE;
+
+  CUtensorMap tm_k, tm_v;
+  if (!encode_pool(&tm_k, k_pages, p) || !encode_pool(&tm_v, v_pages, p)) return DFLASH_ERR_LAUNCH;
+
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_pages = static_cast<const uint16_t*>(k_pages);
+  a.v_pages = static_cast<const uint16_t*>(v_pages);
+  a.page_table = page_table;
+  a.ctx_lens = ctx_lens;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse2 = lse2;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.part_lse = reinterpret_cast<float*>(ws + kHeaderBytes);
+  a.part_o = reinterpret_cast<float*>(
+      ws + kHeaderBytes + align_up(static_cast<size_t>(k.units) * k.R * sizeof(float), 256));
+  a.B = p->batch;
+  a.Hq = p->num_q_heads;
+  a.Hkv = p->num_kv_heads;
+  a.G = p->num_q_heads / p->num_kv_heads;
+  a.D = p->head_dim;
+  a.P = p->page_size;
+  a.max_pages = p->max_pages_per_req;
+  a.num_pages = p->num_pages;
+  a.K = p->block_size;
+  a.W = p->window;
+  a.future_keys = p->future_keys;
+  a.max_ctx_len = p->max_ctx_len;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.R = k.R;
+  a.R_pad = k.R_pad;
+  a.T = k.T;
+  a.C = k.C;
+  a.S = k.S;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (split_start != nullptr &&
+      cudaEventRecord(static_cast<cudaEvent_t>(split_start), s) != cudaSuccess)
+    return DFLASH_ERR_LAUNCH;
+  int err = (k.path == DFLASH_PATH_TCGEN05) ? launch_split_tc(a, k, tm_k, tm_v, s)
+                                            : launch_split_mma(a, k, tm_k, tm_v, s);
+  if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  if (split_done != nullptr &&
+      cudaEventRecord(static_cast<cudaEvent_t>(split_done), s) != cudaSuccess)
+    return DFLASH_ERR_LAUNCH;
+  err = launch_combine(a, s, split_done == nullptr);
+  if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  return DFLASH_OK;
+}
+
+const char* dflash_status_string(int status) {
+  switch (status) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID: return "invalid argument";
+    case DFLASH_ERR_WORKSPACE: return "workspace too small";
+    case DFLASH_ERR_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case DFLASH_ERR_LAUNCH: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+int dflash_read_device_status(const void* workspace, void* stream) {
+  if (workspace == nullptr) return DFLASH_ERR_INVALID;
+  uint32_t v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return DFLASH_ERR_LAUNCH;
+  return static_cast<int>(v & 0x7fffffffu);
+}
+
+int dflash_clear_device_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return DFLASH_ERR_INVALID;
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return DFLASH_ERR_LAUNCH;
+  return DFLASH_OK;
+}
+
+int dflash_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Internal declarations shared by the host API (api.cpp) and the kernels.
+// Not installed; the public interface is include/dflash.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "dflash.h"
+
+#ifdef __CUDACC__
+#define DF_HD __host__ __device__ __forceinline__
+#else
+#define DF_HD inline
+#endif
+
+namespace dflash {
+
+constexpr int kHeaderBytes = 256;      // workspace header: status word + padding
+constexpr int kMaxRows = 128;          // packed query rows per kv head (G*K)
+constexpr int kMaxBlock = 16;          // draft block size K
+constexpr int kStages = 4;             // TMA pipeline depth of the split kernels
+
+// Everything a kernel needs, by value (kernel parameter).
+struct AttnArgs {
+  const uint16_t* q;          // bf16 [B, K, Hq, D]
+  const uint16_t* k_pages;    // bf16 [num_pages, Hkv, P, D]
+  const uint16_t* v_pages;
+  const int32_t* page_table;  // [B, max_pages]
+  const int32_t* ctx_lens;    // [B]
+  uint16_t* out;              // bf16 [B, K, Hq, D]
+  float* lse2;                // [B, K, Hq]
+  float* part_o;              // [units, R, D]  normalised partial output
+  float* part_lse;            // [units, R]     partial base-2 LSE
+  uint32_t* status;           // workspace status word
+  int B, Hq, Hkv, G, D, P, max_pages, num_pages, K, W, future_keys, max_ctx_len;
+  float scale_log2;           // scale * log2(e), applied to q.k in fp32
+  int R;                      // G * K packed rows
+  int R_pad;                  // rows rounded to the kernel granule
+  int T;                      // keys per tile (pipeline stage)
+  int C;                      // tiles per split unit
+  int S;                      // split units per (request, kv head)
+};
+
+// Per-(request, kv head) key-range geometry of the split kernel, which covers
+// the causal part of every row: row i reads [lo_i, L+i+1); the union over the
+// block's rows is [lo_min, L+K).  Tiles are T-aligned in logical position.
+struct Geometry {
+  int L;        // context length after clamping to [0, max_ctx_len]
+  int lo_min;   // first position any row reads
+  int hi_max;   // one past the last position any row reads (L+K)
+  int t_begin;  // first tile index
+  int n_tiles;  // tiles in [t_begin, ceil(hi_max/T))
+  int n_splits; // ceil(n_tiles / C)
+};
+
+DF_HD Geometry make_geometry(int L_raw, int max_ctx_len, int K, int W, int T, int C) {
+  Geometry g;
+  int L = L_raw < 0 ? 0 : (L_raw > max_ctx_len ? max_ctx_len : L_raw);
+  g.L = L;
+  int lo = 0;
+  if (W > 0) {
+    lo = L - W + 1;
+    if (lo < 0) lo = 0;
+  }
+  g.lo_min = lo;
+  g.hi_max = L + K;
+  g.t_begin = lo / T;
+  const int t_end = (g.hi_max + T - 1) / T;
+  g.n_tiles = t_end - g.t_begin;
+  g.n_splits = (g.n_tiles + C - 1) / C;
+  return g;
+}
+
+// Upper bound of Geometry::n_tiles over every L in [0, max_ctx_len].
+DF_HD int max_tiles(int max_ctx_len, int K, int W, int T) {
+  if (W <= 0) return (max_ctx_len + K + T - 1) / T;
+  const int span = (max_ctx_len < W - 1 ? max_ctx_len : W - 1) + K;
+  return (span + T - 1) / T + 1;
+}
+
+// Host-side launch plan.
+struct KernelPlan {
+  int path;         // DFLASH_PATH_MMA / DFLASH_PATH_TCGEN05
+  int R, R_pad, T, C, S;
+  int64_t units;
+  int threads, smem_bytes;
+  int kpw;          // mma path: keys per warp per tile
+  int num_sms;
+};
+
+// Launchers (defined in the .cu files).  Return a cudaError_t value.
+int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
+                     const CUtensorMap& tm_v, cudaStream_t stream);
+int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
+                    const CUtensorMap& tm_v, cudaStream_t stream);
+int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl);
+
+// Shared-memory bytes of each split kernel for a plan (used by the planner).
+int split_mma_smem_bytes(int D, int R_pad, int kpw);
+int split_tc_smem_bytes(int D);
+
+}  // namespace dflash

@@ -1,0 +1,449 @@
+// Split-KV kernel, warp-level tensor-core form (mma.sync m16n8k16, bf16 in,
+// fp32 accumulate), for packed row counts that do not fill a 128-row tcgen05
+// tile.
+//
+// One CTA = one split unit (request b, kv head h, split s): a contiguous range
+// of T-key tiles of the causal part of the draft block's attention (context
+// window plus block keys j <= i, TensorRT-LLM PR #21130, change 2: "the causal
+// decode is the exact result" for that part).  The G*K query rows that share
+// kv head h are packed into one tile (row r = i*G + g), so every K/V byte of
+// the unit is read from HBM once (PR #16150, split-KV rework: one tile of
+// packed query rows per kv head).
+//
+// Roles: warp 0 lane 0 is the producer: it looks page ids up in the page table
+// and issues one 128-byte-swizzled TMA box per (page, 64-column half) for K and
+// V into a 4-stage ring (full/empty mbarriers).  Pages outside the unit's
+// visible range are fetched with page coordinate -1, which the TMA unit fills
+// with zeros.  Consumer warps form an (R_pad/16) x (T/KPW) grid: warp (wr, wk)
+// owns query rows [16 wr, 16 wr + 16) and keys [wk KPW, (wk+1) KPW) of every
+// tile, keeps its own online-softmax state in registers (base 2), and the
+// warps of a row group merge their states through shared memory at the end.
+// Output: the unit's normalised partial O and base-2 LSE in the workspace.
+
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace dflash {
+namespace {
+
+template <int D>
+struct MmaTile {
+  static constexpr int T = (D == 64) ? 128 : 64;          // keys per stage
+  static constexpr int kTileBytes = T * D * 2;             // one of K or V
+  static constexpr int kStageBytes = 2 * kTileBytes;
+};
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+template <int D, int KPW>
+__global__ void __launch_bounds__(288, 1)
+    split_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v) {
+  constexpr int T = MmaTile<D>::T;
+  constexpr int NWK = T / KPW;              // key-slice warps per row group
+  constexpr int NS = kStages;
+  constexpr int kTileBytes = MmaTile<D>::kTileBytes;
+  constexpr int kStageBytes = MmaTile<D>::kStageBytes;
+  constexpr int NT = KPW / 8;               // 8-key accumulator tiles per warp
+  static_assert(KPW % 16 == 0 && T % KPW == 0, "bad key slice");
+
+  const int s = blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+
+  const int L_raw = __ldg(&a.ctx_lens[b]);
+  const Geometry geo = make_geometry(L_raw, a.max_ctx_len, a.K, a.W, T, a.C);
+  if (threadIdx.x == 0 && s == 0 && h == 0 && (L_raw < 0 || L_raw > a.max_ctx_len))
+    flag_status(a.status, DFLASH_STATUS_BAD_CTX_LEN);
+  if (s >= geo.n_splits) return;  // empty split unit (uniform over the CTA)
+
+  const int tile0 = geo.t_begin + s * a.C;
+  int ntiles = geo.n_tiles - s * a.C;
+  if (ntiles > a.C) ntiles = a.C;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const uint32_t q_u32 = base_u32 + NS * kStageBytes;
+  uint8_t* q_smem = base + NS * kStageBytes;
+  const uint32_t bar_u32 = q_u32 + a.R_pad * D * 2;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + a.R_pad * D * 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS);
+  volatile int* issued_count = abort_flag + 1;
+  auto full_bar = [&](int st) { return bar_u32 + 8u * st; };
+  auto empty_bar = [&](int st) { return bar_u32 + 8u * (NS + st); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_consumer_warps = (a.R_pad / 16) * NWK;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(full_bar(st), 1);
+      mbar_init(empty_bar(st), n_consumer_warps);
+    }
+    *abort_flag = 0;
+    *issued_count = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+
+  // Packed query tile: row r = i*G + g  <-  q[b, i, h*G + g, :]; rows >= R are zero.
+  {
+    constexpr int CPR = D / 8;  // 16-byte chunks per row
+    const int chunks = a.R_pad * CPR;
+    for (int idx = threadIdx.x; idx < chunks; idx += blockDim.x) {
+      const int row = idx / CPR;
+      const int c = idx - row * CPR;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (row < a.R) {
+        const int i = row / a.G;
+        const int g = row - i * a.G;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + ((static_cast<size_t>(b) * a.K + i) * a.Hq + static_cast<size_t>(h) * a.G + g) * D);
+        v = __ldg(src + c);
+      }
+      *reinterpret_cast<uint4*>(q_smem + swz_offset(row, c, a.R_pad)) = v;
+    }
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const int pages_per_tile = T / a.P;
+      const int slot_lo = geo.lo_min / a.P;
+      const int slot_hi = (geo.hi_max + a.P - 1) / a.P;
+      const int32_t* table_row = a.page_table + static_cast<size_t>(b) * a.max_pages;
+      for (int it = 0; it < ntiles; ++it) {
+        const int st = it % NS;
+        if (it >= NS) {
+          if (!mbar_wait(empty_bar(st), ((it / NS) - 1) & 1)) {
+            flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+        }
+        if (*abort_flag) break;
+        mbar_arrive_expect_tx(full_bar(st), kStageBytes);
+        const uint32_t k_dst = base_u32 + st * kStageBytes;
+        const uint32_t v_dst = k_dst + kTileBytes;
+        const int slot0 = (tile0 + it) * pages_per_tile;
+        for (int j = 0; j < pages_per_tile; ++j) {
+          const int slot = slot0 + j;
+          int page = -1;
+          if (slot >= slot_lo && slot < slot_hi) {
+            page = __ldg(&table_row[slot]);
+            if (page < 0 || page >= a.num_pages) {
+              flag_status(a.status, DFLASH_STATUS_BAD_PAGE);
+              page = -1;
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < D / 64; ++x) {
+            const uint32_t off = x * T * 128 + j * a.P * 128;
+            tma_load_4d(k_dst + off, &tm_k, x * 64, 0, h, page, full_bar(st));
+            tma_load_4d(v_dst + off, &tm_v, x * 64, 0, h, page, full_bar(st));
+          }
+        }
+        *issued_count = it + 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int cw = warp - 1;
+    const int wr = cw / NWK;
+    const int wk = cw - wr * NWK;
+    const int kb = wk * KPW;  // first key of this warp's slice within a tile
+
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      ldmatrix_x4(q_u32 + swz_offset(16 * wr + (lane & 15), kk * 2 + (lane >> 4), a.R_pad),
+                  qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+
+    // Visible interval [lo, hi) of the two rows this lane accumulates.
+    const int L = geo.L;
+    int lo_r[2], hi_r[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 16 * wr + (lane >> 2) + 8 * e;
+      if (r < a.R) {
+        const int i = r / a.G;
+        int lo = 0;
+        if (a.W > 0) {
+          lo = L + i - a.W + 1;
+          if (lo < 0) lo = 0;
+        }
+        lo_r[e] = lo;
+        hi_r[e] = L + i + 1;
+      } else {
+        lo_r[e] = 0x7fffffff;
+        hi_r[e] = -0x7fffffff;
+      }
+    }
+    int lo_rows_max = 0;  // largest row lower bound (row i = K-1)
+    if (a.W > 0) {
+      lo_rows_max = L + a.K - a.W;
+      if (lo_rows_max < 0) lo_rows_max = 0;
+    }
+    const int hi_rows_min = L + 1;  // smallest row upper bound (row i = 0)
+
+    float m_run[2] = {neg_inf(), neg_inf()};
+    float l_run[2] = {0.f, 0.f};
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+    bool aborted = false;
+    for (int it = 0; it < ntiles; ++it) {
+      const int st = it % NS;
+      if (!mbar_wait(full_bar(st), (it / NS) & 1)) {
+        flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+        *abort_flag = 1;
+        aborted = true;
+        break;
+      }
+      const uint32_t k_st = base_u32 + st * kStageBytes;
+      const uint32_t v_st = k_st + kTileBytes;
+      const int p0 = (tile0 + it) * T + kb;  // logical position of the slice's first key
+
+      // S = Q K^T over this warp's 16 rows x KPW keys.
+      float sacc[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+        for (int np = 0; np < KPW / 16; ++np) {
+          uint32_t b0, b1, b2, b3;
+          const int key = kb + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+          ldmatrix_x4(k_st + swz_offset(key, kk * 2 + ((lane >> 3) & 1), T), b0, b1, b2, b3);
+          mma_bf16_16816(sacc[2 * np], qa[kk], b0, b1);
+          mma_bf16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+        }
+      }
+
+      // Scale in fp32 to the base-2 domain and mask by select.
+      const bool need_mask = (p0 < lo_rows_max) || (p0 + KPW > hi_rows_min);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float x = sacc[n][e] * a.scale_log2;
+          if (need_mask) {
+            const int pos = p0 + n * 8 + 2 * (lane & 3) + (e & 1);
+            const int ri = e >> 1;
+            if (pos < lo_r[ri] || pos >= hi_r[ri]) x = neg_inf();
+          }
+          sacc[n][e] = x;
+        }
+      }
+
+      // Online softmax, base 2.  Each row's 8 lanes-quads hold disjoint keys.
+      float corr[2];
+#pragma unroll
+      for (int ri = 0; ri < 2; ++ri) {
+        float mx = neg_inf();
+#pragma unroll
+        for (int n = 0; n < NT; ++n) mx = fmaxf(mx, fmaxf(sacc[n][2 * ri], sacc[n][2 * ri + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run[ri], mx);
+        const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
+        corr[ri] = fast_exp2(m_run[ri] - m_use);
+        m_run[ri] = m_new;
+        float rs = 0.f;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const float p_a = fast_exp2(sacc[n][2 * ri] - m_use);
+          const float p_b = fast_exp2(sacc[n][2 * ri + 1] - m_use);
+          sacc[n][2 * ri] = p_a;
+          sacc[n][2 * ri + 1] = p_b;
+          rs += p_a + p_b;
+        }
+        l_run[ri] = l_run[ri] * corr[ri] + rs;
+      }
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= corr[0];
+        o[n][1] *= corr[0];
+        o[n][2] *= corr[1];
+        o[n][3] *= corr[1];
+      }
+
+      // O += P V.  Value rows outside the unit's visible range may hold
+      // anything (page tails, recycled slots): zero them in registers so a
+      // zero probability never meets a NaN.
+      const bool sanitize = (p0 < geo.lo_min) || (p0 + KPW > geo.hi_max);
+#pragma unroll
+      for (int k2 = 0; k2 < KPW / 16; ++k2) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(sacc[2 * k2][0], sacc[2 * k2][1]);
+        pa[1] = pack_bf16x2(sacc[2 * k2][2], sacc[2 * k2][3]);
+        pa[2] = pack_bf16x2(sacc[2 * k2 + 1][0], sacc[2 * k2 + 1][1]);
+        pa[3] = pack_bf16x2(sacc[2 * k2 + 1][2], sacc[2 * k2 + 1][3]);
+        uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+        if (sanitize) {
+          const int kp = p0 + k2 * 16 + 2 * (lane & 3);
+          const bool v0 = kp >= geo.lo_min && kp < geo.hi_max;
+          const bool v1 = kp + 1 >= geo.lo_min && kp + 1 < geo.hi_max;
+          const bool v8 = kp + 8 >= geo.lo_min && kp + 8 < geo.hi_max;
+          const bool v9 = kp + 9 >= geo.lo_min && kp + 9 < geo.hi_max;
+          keep_lo = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
+          keep_hi = (v8 ? 0x0000ffffu : 0u) | (v9 ? 0xffff0000u : 0u);
+        }
+        const int vkey = kb + k2 * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int dn = 0; dn < D / 16; ++dn) {
+          uint32_t v0, v1, v2, v3;
+          ldmatrix_x4_trans(v_st + swz_offset(vkey, dn * 2 + (lane >> 4), T), v0, v1, v2, v3);
+          v0 &= keep_lo;
+          v2 &= keep_lo;
+          v1 &= keep_hi;
+          v3 &= keep_hi;
+          mma_bf16_16816(o[2 * dn], pa, v0, v1);
+          mma_bf16_16816(o[2 * dn + 1], pa, v2, v3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(st));
+    }
+
+    // Row sums: the four lanes of a quad hold disjoint keys of the same rows.
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+      l_run[ri] += __shfl_xor_sync(0xffffffffu, l_run[ri], 1);
+      l_run[ri] += __shfl_xor_sync(0xffffffffu, l_run[ri], 2);
+    }
+
+    const size_t unit = (static_cast<size_t>(b) * a.Hkv + h) * a.S + s;
+    float* part_o = a.part_o + unit * a.R * D;
+    float* part_lse = a.part_lse + unit * a.R;
+    (void)aborted;
+
+    if constexpr (NWK == 1) {
+#pragma unroll
+      for (int ri = 0; ri < 2; ++ri) {
+        const int r = 16 * wr + (lane >> 2) + 8 * ri;
+        if (r < a.R) {
+          const float l = l_run[ri];
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            float2 v = make_float2(o[n][2 * ri] * inv, o[n][2 * ri + 1] * inv);
+            *reinterpret_cast<float2*>(part_o + static_cast<size_t>(r) * D + n * 8 + 2 * (lane & 3)) = v;
+          }
+          if ((lane & 3) == 0) part_lse[r] = l > 0.f ? m_run[ri] + log2f(l) : neg_inf();
+        }
+      }
+    } else {
+      // Merge the NWK key-slice states of each row group through shared
+      // memory (the stage ring is free: every issued tile was consumed).
+      const int n_ct = n_consumer_warps * 32;
+      named_barrier(1, n_ct);
+      float* sc_o = reinterpret_cast<float*>(base);              // [cw][16][D]
+      float* sc_m = sc_o + n_consumer_warps * 16 * D;            // [cw][16]
+      float* sc_l = sc_m + n_consumer_warps * 16;                // [cw][16]
+#pragma unroll
+      for (int ri = 0; ri < 2; ++ri) {
+        const int rr = (lane >> 2) + 8 * ri;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+          *reinterpret_cast<float2*>(sc_o + (cw * 16 + rr) * D + n * 8 + 2 * (lane & 3)) =
+              make_float2(o[n][2 * ri], o[n][2 * ri + 1]);
+        if ((lane & 3) == 0) {
+          sc_m[cw * 16 + rr] = m_run[ri];
+          sc_l[cw * 16 + rr] = l_run[ri];
+        }
+      }
+      named_barrier(1, n_ct);
+      const int ct = threadIdx.x - 32;
+      for (int e = ct; e < a.R * D; e += n_ct) {
+        const int r = e / D;
+        const int d = e - r * D;
+        const int g = r >> 4;
+        const int rr = r & 15;
+        float M = neg_inf();
+#pragma unroll
+        for (int w = 0; w < NWK; ++w) M = fmaxf(M, sc_m[(g * NWK + w) * 16 + rr]);
+        float num = 0.f, den = 0.f;
+        if (M != neg_inf()) {
+#pragma unroll
+          for (int w = 0; w < NWK; ++w) {
+            const int cwi = g * NWK + w;
+            const float wt = exp2f(sc_m[cwi * 16 + rr] - M);
+            num += wt * sc_o[(cwi * 16 + rr) * D + d];
+            den += wt * sc_l[cwi * 16 + rr];
+          }
+        }
+        part_o[static_cast<size_t>(r) * D + d] = den > 0.f ? num / den : 0.f;
+        if (d == 0) part_lse[r] = den > 0.f ? M + log2f(den) : neg_inf();
+      }
+    }
+  }
+
+  pdl_launch_dependents();
+
+  // If a wait gave up, let every copy already issued land before the CTA's
+  // shared memory is released.
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) {
+    const int issued = *issued_count;
+    for (int it = issued > NS ? issued - NS : 0; it < issued; ++it)
+      (void)mbar_wait(full_bar(it % NS), (it / NS) & 1);
+  }
+}
+
+int kpw_for(int D, int R_pad) {
+  const int mt = R_pad / 16;
+  if (D == 64) return mt == 1 ? 16 : (mt == 2 ? 32 : (mt <= 4 ? 64 : 128));
+  return mt == 1 ? 16 : (mt == 2 ? 32 : 64);
+}
+
+template <int D, int KPW>
+int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
+             const CUtensorMap& tm_v, cudaStream_t stream) {
+  auto kern = split_mma_kernel<D, KPW>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         plan.smem_bytes);
+  if (err != cudaSuccess) return err;
+  dim3 grid(plan.S, a.Hkv, a.B);
+  kern<<<grid, plan.threads, plan.smem_bytes, stream>>>(a, tm_k, tm_v);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int split_mma_smem_bytes(int D, int R_pad, int /*kpw*/) {
+  const int stage = (D == 64) ? MmaTile<64>::kStageBytes : MmaTile<128>::kStageBytes;
+  return 1024 + kStages * stage + R_pad * D * 2 + 8 * 2 * kStages + 16;
+}
+
+int split_mma_kpw(int D, int R_pad) { return kpw_for(D, R_pad); }
+
+int split_mma_tile_keys(int D) { return D == 64 ? MmaTile<64>::T : MmaTile<128>::T; }
+
+int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
+                     const CUtensorMap& tm_v, cudaStream_t stream) {
+  if (a.D == 64) {
+    switch (plan.kpw) {
+      case 16: return launch_t<64, 16>(a, plan, tm_k, tm_v, stream);
+      case 32: return launch_t<64, 32>(a, plan, tm_k, tm_v, stream);
+      case 64: return launch_t<64, 64>(a, plan, tm_k, tm_v, stream);
+      case 128: return launch_t<64, 128>(a, plan, tm_k, tm_v, stream);
+    }
+  } else if (a.D == 128) {
+    switch (plan.kpw) {
+      case 16: return launch_t<128, 16>(a, plan, tm_k, tm_v, stream);
+      case 32: return launch_t<128, 32>(a, plan, tm_k, tm_v, stream);
+      case 64: return launch_t<128, 64>(a, plan, tm_k, tm_v, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dflash

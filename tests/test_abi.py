@@ -1,0 +1,164 @@
+"""Host-side checks of the C ABI: exports, struct layout, validation, planner.
+
+No kernel is launched here; these run without a GPU.
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dflash_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(dflash_lib):
+    from speculative_decoding_draft_paged_gb300 import _lib
+
+    lib = ctypes.CDLL(_lib.library_path())
+    names = declared_functions()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in dflash.h but not exported"
+    assert set(names) == set(_lib.EXPORTS)
+
+
+def test_struct_layout_matches_header(dflash_lib, tmp_path):
+    """Compile a C program against the header and compare sizes/offsets."""
+    from speculative_decoding_draft_paged_gb300 import _lib
+
+    prog = tmp_path / "layout.c"
+    fields_p = [f for f, _ in _lib.Params._fields_]
+    fields_i = [f for f, _ in _lib.PlanInfo._fields_]
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dflash.h"', "int main(void){",
+             'printf("%zu\\n", sizeof(dflash_params));',
+             'printf("%zu\\n", sizeof(dflash_plan_info));']
+    lines += [f'printf("%zu\\n", offsetof(dflash_params, {f}));' for f in fields_p]
+    lines += [f'printf("%zu\\n", offsetof(dflash_plan_info, {f}));' for f in fields_i]
+    lines += ["return 0;}"]
+    prog.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(_lib.Params)
+    assert vals[1] == ctypes.sizeof(_lib.PlanInfo)
+    off = vals[2:]
+    assert off[: len(fields_p)] == [getattr(_lib.Params, f).offset for f in fields_p]
+    assert off[len(fields_p):] == [getattr(_lib.PlanInfo, f).offset for f in fields_i]
+
+
+def base_params(**kw):
+    import speculative_decoding_draft_paged_gb300 as d
+
+    args = dict(batch=4, num_q_heads=16, num_kv_heads=2, head_dim=64, page_size=32,
+                max_pages_per_req=40, num_pages=200, block_size=7, window=0, future_keys=1,
+                scale=0.125, max_ctx_len=1200)
+    args.update(kw)
+    return d.make_params(**args)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(batch=0), dict(num_kv_heads=0), dict(num_q_heads=12, num_kv_heads=5),
+    dict(head_dim=96), dict(head_dim=256), dict(page_size=8), dict(page_size=48),
+    dict(block_size=0), dict(block_size=17), dict(num_q_heads=64, num_kv_heads=2, block_size=5),
+    dict(window=-1), dict(window=3), dict(future_keys=2), dict(scale=float("inf")),
+    dict(scale=float("nan")), dict(max_ctx_len=-1), dict(max_ctx_len=40 * 32 - 6),
+    dict(num_pages=0), dict(force_path=3), dict(force_split_tiles=-1),
+])
+def test_invalid_params_rejected(dflash_lib, bad):
+    d = dflash_lib
+    p = base_params(**bad)
+    assert d.workspace_size(p) == 0
+    with pytest.raises(d.DflashError) as e:
+        d.plan(p)
+    assert e.value.code == d.DFLASH_ERR_INVALID
+    rc = d.block_attn_raw(p, 16, 16, 16, 16, 16, 16, 16, 256, 1 << 30, 0)
+    assert rc == d.DFLASH_ERR_INVALID
+
+
+def test_reserved_must_be_zero(dflash_lib):
+    p = base_params()
+    p.reserved[2] = 1
+    assert dflash_lib.workspace_size(p) == 0
+
+
+def test_boundary_params_accepted(dflash_lib):
+    d = dflash_lib
+    for kw in [dict(max_ctx_len=40 * 32 - 7), dict(window=7), dict(window=4096),
+               dict(num_q_heads=128, num_kv_heads=8, block_size=8), dict(block_size=1, window=1),
+               dict(head_dim=128, page_size=64, max_pages_per_req=30), dict(page_size=16,
+                                                                            max_pages_per_req=90)]:
+        assert d.workspace_size(base_params(**kw)) > 0, kw
+
+
+def test_null_and_misaligned_pointers_rejected(dflash_lib):
+    d = dflash_lib
+    p = base_params()
+    ws = d.workspace_size(p)
+    good = [1 << 20] * 8
+    for i in range(8):
+        ptrs = list(good)
+        ptrs[i] = 0
+        assert d.block_attn_raw(p, *ptrs, ws, 0) == d.DFLASH_ERR_INVALID
+    for i, off in [(0, 8), (1, 2), (2, 4), (3, 2), (4, 1), (5, 8), (6, 2), (7, 128)]:
+        ptrs = list(good)
+        ptrs[i] += off
+        assert d.block_attn_raw(p, *ptrs, ws, 0) == d.DFLASH_ERR_INVALID
+
+
+def test_status_strings(dflash_lib):
+    from speculative_decoding_draft_paged_gb300 import _lib
+
+    assert _lib.status_string(0) == "ok"
+    assert "workspace" in _lib.status_string(-2)
+    assert "10.3" in _lib.status_string(-3)
+    assert _lib.status_string(123) == "unknown status"
+    assert dflash_lib.version() >= 100
+
+
+def touched_tiles(L, K, W, T):
+    lo = max(0, L - W + 1) if W > 0 else 0
+    return (L + K + T - 1) // T - lo // T
+
+
+@pytest.mark.parametrize("kw", [
+    dict(), dict(window=4096, head_dim=128, page_size=64, num_q_heads=16, num_kv_heads=1,
+                 max_ctx_len=16384, max_pages_per_req=260, batch=64),
+    dict(window=100, max_ctx_len=1000), dict(batch=1, max_ctx_len=32768, max_pages_per_req=1030),
+    dict(force_split_tiles=1), dict(force_split_tiles=3, window=50),
+    dict(num_q_heads=64, num_kv_heads=16, batch=256, max_ctx_len=131072, max_pages_per_req=4100),
+])
+def test_planner_covers_every_length(dflash_lib, kw):
+    """For every context length up to max_ctx_len the units cover all tiles,
+    and the workspace holds every unit's partial state."""
+    d = dflash_lib
+    p = base_params(**kw)
+    pl = d.plan(p)
+    T, C, S = pl["tile_keys"], pl["split_tiles"], pl["max_splits"]
+    assert pl["units"] == p.batch * p.num_kv_heads * S
+    worst = max(touched_tiles(L, p.block_size, p.window, T) for L in range(0, p.max_ctx_len + 1))
+    assert S * C >= worst
+    assert (S - 1) * C < worst + C
+    R = p.num_q_heads // p.num_kv_heads * p.block_size
+    assert pl["rows"] == R and pl["rows_padded"] >= R
+    ws = d.workspace_size(p)
+    assert ws >= 256 + pl["units"] * R * (p.head_dim + 1) * 4
+    if kw.get("force_split_tiles"):
+        assert C == kw["force_split_tiles"]
+
+
+def test_plan_independent_of_lengths_and_pool_contents(dflash_lib):
+    """The grid is a function of the parameters only (graph capture)."""
+    d = dflash_lib
+    a = d.plan(base_params())
+    b = d.plan(base_params(num_pages=5000))
+    assert a == b

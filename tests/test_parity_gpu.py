@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA library through its C ABI against the fp64 oracle.
+
+Every case draws seeded synthetic inputs, runs ``dflash_block_attn`` on the
+GPU and the oracle on the host, and checks the bar in ``_gpu_cases``.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_draft_paged_gb300 as dflash
+from speculative_decoding_draft_paged_gb300 import workloads as W
+from tests._gpu_cases import (assert_parity, check_case, compact_requests, metrics, run_lib,
+                              run_oracle)
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_config(cuda_device):
+    m, _, _ = check_case(W.tiny(), cuda_device)
+    assert m["rel_l2"] < 5e-3
+
+
+@pytest.mark.parametrize("K", [1, 3, 7])
+@pytest.mark.parametrize("L", [100, 2048, 5000, 9000])
+def test_minimax_shape(cuda_device, K, L):
+    check_case(W.minimax(B=3, K=K, ctx_lens=[L, max(0, L - 77), L // 2 + 5]), cuda_device)
+
+
+@pytest.mark.parametrize("K", [3, 7])
+@pytest.mark.parametrize("L", [3000, 8200])
+def test_adp_shape_with_outliers(cuda_device, K, L):
+    check_case(W.adp(B=2, K=K, ctx_lens=[L, L - 1000]), cuda_device)
+
+
+@pytest.mark.parametrize("Hq", [8, 12])
+@pytest.mark.parametrize("L", [5000, 20000])
+def test_longctx_shape(cuda_device, Hq, L):
+    check_case(W.longctx(B=2, L=L, Hq=Hq), cuda_device)
+
+
+def test_ragged_shape(cuda_device):
+    spec = W.ragged(B=5, lo=1, hi=20000)
+    check_case(spec, cuda_device)
+
+
+@pytest.mark.parametrize("D,P", [(64, 16), (64, 32), (128, 64), (128, 16)])
+@pytest.mark.parametrize("window,fk", [(0, 1), (0, 0), (300, 1), (300, 0)])
+def test_edge_lengths(cuda_device, D, P, window, fk):
+    K = 5
+    lens = [0, 1, P - 1, P, P + 1, 2 * P - K, 2 * P - K + 1]
+    if window:
+        lens += [window - 1, window, window + K, window + P + 3]
+    spec = W.CaseSpec(f"edges_D{D}_P{P}_W{window}_fk{fk}", B=len(lens), Hq=8, Hkv=2, D=D, K=K, P=P,
+                      window=window, future_keys=fk, ctx_lens=lens, seed=77, poison=True,
+                      extra_pages=3, extra_table_slots=2)
+    check_case(spec, cuda_device)
+
+
+@pytest.mark.parametrize("G,K", [(1, 1), (4, 3), (16, 1), (3, 5), (4, 7), (6, 7), (16, 3), (5, 13),
+                                 (16, 7), (8, 16)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_packed_row_counts(cuda_device, G, K, D):
+    spec = W.CaseSpec(f"rows_G{G}_K{K}_D{D}", B=2, Hq=2 * G, Hkv=2, D=D, K=K, P=32, window=0,
+                      future_keys=1, ctx_lens=[700, 261], seed=5)
+    check_case(spec, cuda_device)
+
+
+@pytest.mark.parametrize("path", [dflash.PATH_MMA])
+def test_forced_path_and_tiny_splits(cuda_device, path):
+    """force_split_tiles=1 gives one tile per unit: many empty units for the
+    short requests of a ragged batch, and the combine over many partials."""
+    spec = W.CaseSpec("empty_splits", B=4, Hq=8, Hkv=2, D=64, K=7, P=32, window=0, future_keys=1,
+                      ctx_lens=[3000, 0, 130, 1000], seed=9, poison=True)
+    m1, o1, l1 = check_case(spec, cuda_device, force_path=path, force_split_tiles=1)
+    m2, o2, l2 = check_case(spec, cuda_device, force_path=path, force_split_tiles=5)
+    assert m1["rel_l2"] < 5e-3 and m2["rel_l2"] < 5e-3
+
+
+@pytest.mark.parametrize("window", [0, 1000])
+def test_page_permutation_bitwise(cuda_device, window):
+    spec = W.CaseSpec("perm", B=3, Hq=16, Hkv=2, D=64, K=7, P=32, window=window, future_keys=1,
+                      ctx_lens=[2500, 777, 4000], seed=11, extra_pages=5)
+    inp = {k: v.to(cuda_device) for k, v in W.make_inputs(spec, "cpu").items()}
+    out1, lse1 = run_lib(spec, inp)
+    g = torch.Generator().manual_seed(3)
+    perm = torch.randperm(spec.num_pages, generator=g).to(cuda_device)
+    kp = torch.empty_like(inp["k_pages"])
+    vp = torch.empty_like(inp["v_pages"])
+    kp[perm] = inp["k_pages"]
+    vp[perm] = inp["v_pages"]
+    tab = inp["page_table"].clone()
+    m = tab >= 0
+    tab[m] = perm[tab[m].long()].to(torch.int32)
+    inp2 = dict(inp, k_pages=kp, v_pages=vp, page_table=tab)
+    out2, lse2 = run_lib(spec, inp2)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+    assert torch.equal(lse1, lse2)
+
+
+def test_deterministic(cuda_device):
+    spec = W.longctx(B=2, L=9000, Hq=12)
+    inp = {k: v.to(cuda_device) for k, v in W.make_inputs(spec, "cpu").items()}
+    a = run_lib(spec, inp)
+    b = run_lib(spec, inp)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_guard_bands_untouched(cuda_device):
+    spec = W.CaseSpec("guards", B=3, Hq=16, Hkv=2, D=128, K=7, P=64, window=0, future_keys=1,
+                      ctx_lens=[1500, 64, 3333], seed=12)
+    inp = {k: v.to(cuda_device) for k, v in W.make_inputs(spec, "cpu").items()}
+    p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K,
+                          window=0, future_keys=1, scale=spec.softmax_scale,
+                          max_ctx_len=spec.max_ctx_len)
+    ws_bytes = dflash.workspace_size(p)
+    G = 4096
+    out_buf = torch.full((G + inp["q"].numel() * 2 + G,), 0xA5, dtype=torch.uint8, device=cuda_device)
+    lse_buf = torch.full((G + spec.B * spec.K * spec.Hq * 4 + G,), 0x5A, dtype=torch.uint8,
+                         device=cuda_device)
+    ws_buf = torch.full((G + ws_bytes + G,), 0x3C, dtype=torch.uint8, device=cuda_device)
+    ws_buf[G:G + 4] = 0
+    rc = dflash.block_attn_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
+                               inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(),
+                               inp["ctx_lens"].data_ptr(), out_buf.data_ptr() + G,
+                               lse_buf.data_ptr() + G, ws_buf.data_ptr() + G, ws_bytes,
+                               torch.cuda.current_stream().cuda_stream)
+    assert rc == dflash.DFLASH_OK
+    torch.cuda.synchronize()
+    for buf, val, n in ((out_buf, 0xA5, inp["q"].numel() * 2), (lse_buf, 0x5A, spec.B * spec.K * spec.Hq * 4),
+                        (ws_buf, 0x3C, ws_bytes)):
+        assert bool((buf[:G] == val).all()), "guard band before the buffer was written"
+        assert bool((buf[G + n:] == val).all()), "guard band after the buffer was written"
+    out = out_buf[G:G + inp["q"].numel() * 2].view(torch.bfloat16).view(inp["q"].shape)
+    lse = lse_buf[G:G + spec.B * spec.K * spec.Hq * 4].view(torch.float32).view(spec.B, spec.K, spec.Hq)
+    ro, rl = run_oracle(spec, {k: v.cpu() for k, v in inp.items()})
+    assert_parity(metrics(out, lse, ro, rl), "guards")
+
+
+def test_workspace_too_small_refused(cuda_device):
+    spec = W.tiny()
+    inp = {k: v.to(cuda_device) for k, v in W.make_inputs(spec, "cpu").items()}
+    p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=3, window=0,
+                          future_keys=1, scale=spec.softmax_scale, max_ctx_len=100)
+    need = dflash.workspace_size(p)
+    ws = torch.zeros(need, dtype=torch.uint8, device=cuda_device)
+    out = torch.full_like(inp["q"], 7.0)
+    lse = torch.full((1, 3, 4), 7.0, device=cuda_device)
+    rc = dflash.block_attn_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
+                               inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(),
+                               inp["ctx_lens"].data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               ws.data_ptr(), need - 256, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == dflash.DFLASH_ERR_WORKSPACE
+    assert bool((out == 7.0).all()) and bool((lse == 7.0).all())
+
+
+def test_bad_device_data_flags_status_without_fault(cuda_device):
+    spec = W.CaseSpec("baddata", B=3, Hq=8, Hkv=2, D=64, K=3, P=32, window=0, future_keys=1,
+                      ctx_lens=[500, 300, 900], seed=13)
+    inp = {k: v.to(cuda_device) for k, v in W.make_inputs(spec, "cpu").items()}
+    p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=3, window=0,
+                          future_keys=1, scale=spec.softmax_scale, max_ctx_len=900)
+    ws = torch.zeros(dflash.workspace_size(p), dtype=torch.uint8, device=cuda_device)
+    run_lib(spec, inp, workspace=ws)
+    assert dflash.read_device_status(ws) == 0
+    bad = dict(inp)
+    bad["page_table"] = inp["page_table"].clone()
+    bad["page_table"][1, 2] = spec.num_pages + 1000
+    bad["page_table"][2, 0] = -7
+    out, lse = run_lib(spec, bad, workspace=ws)
+    st = dflash.read_device_status(ws)
+    assert st & dflash.DFLASH_STATUS_BAD_PAGE
+    assert not (st & dflash.DFLASH_STATUS_TIMEOUT)
+    assert not torch.isnan(out[0].float()).any()
+    dflash.clear_device_status(ws)
+    assert dflash.read_device_status(ws) == 0
+    bad2 = dict(inp, ctx_lens=torch.tensor([500, 5000, -4], dtype=torch.int32, device=cuda_device))
+    run_lib(spec, bad2, workspace=ws)
+    st = dflash.read_device_status(ws)
+    assert st & dflash.DFLASH_STATUS_BAD_CTX_LEN
+    assert not (st & dflash.DFLASH_STATUS_TIMEOUT)
+    torch.cuda.synchronize()
+    # Request 0 was untouched by the bad data of the others.
+    ro, rl = run_oracle(spec, {k: v.cpu() for k, v in inp.items()}, req_ids=np.array([0], np.int32))
+    assert_parity(metrics(out[:1], lse[:1], ro, rl), "bad-data neighbour")
+
+
+def test_cuda_graph_replay_with_new_lengths(cuda_device):
+    # Tables cover 5000 context tokens for every request; the lengths change
+    # between replays of one captured graph.
+    spec = W.CaseSpec("graph", B=4, Hq=16, Hkv=2, D=64, K=7, P=32, window=2048, future_keys=1,
+                      ctx_lens=[5000] * 4, seed=14)
+    inp = {k: v.to(cuda_device) for k, v in W.make_inputs(spec, "cpu").items()}
+    inp["ctx_lens"].copy_(torch.tensor([5000, 4000, 3000, 100], dtype=torch.int32))
+    p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=7, window=2048,
+                          future_keys=1, scale=spec.softmax_scale, max_ctx_len=5000)
+    ws = torch.zeros(dflash.workspace_size(p), dtype=torch.uint8, device=cuda_device)
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty(inp["q"].shape[:3], dtype=torch.float32, device=cuda_device)
+    lens = inp["ctx_lens"]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run_lib(spec, inp, out=out, lse2=lse, workspace=ws)   # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_lib(spec, inp, out=out, lse2=lse, workspace=ws)
+    for new in ([5000, 4000, 3000, 100], [17, 4999, 2048, 0], [3333, 64, 4567, 2047]):
+        lens.copy_(torch.tensor(new, dtype=torch.int32))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ro, rl = run_oracle(spec, {k: v.cpu() for k, v in inp.items()}, ctx_lens=np.array(new, np.int32))
+        assert_parity(metrics(out, lse, ro, rl), f"graph replay {new}")
+
+
+# ----------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the benchmark times.
+# ----------------------------------------------------------------------------
+
+def test_full_minimax_headline(cuda_device):
+    """B=64, K=7, L=16384, W=4096, 16/1 heads, D=128, page 64: every row."""
+    spec = W.minimax(B=64, K=7, L=16384)
+    inp = W.make_inputs(spec, cuda_device)
+    out, lse = run_lib(spec, inp)
+    torch.cuda.synchronize()
+    host = {k: v.cpu() for k, v in inp.items()}
+    ro, rl = run_oracle(spec, host)
+    assert_parity(metrics(out, lse, ro, rl), spec.name)
+
+
+@pytest.mark.parametrize("Hq", [8, 12])
+def test_full_longctx_sampled(cuda_device, Hq):
+    """B=32 at 128K: the oracle checks 3 of the requests."""
+    spec = W.longctx(B=32, L=131072, Hq=Hq)
+    inp = W.make_inputs(spec, cuda_device)
+    out, lse = run_lib(spec, inp)
+    torch.cuda.synchronize()
+    ids = [0, 17, 31]
+    sub = compact_requests(inp, ids)
+    ro, rl = run_oracle(spec, sub)
+    assert_parity(metrics(out[ids], lse[ids], ro, rl), spec.name)
+
+
+def test_full_ragged_sampled(cuda_device):
+    """B=256, contexts uniform in [1K, 128K]: shortest, longest and 10 more."""
+    spec = W.ragged(B=256)
+    inp = W.make_inputs(spec, cuda_device)
+    out, lse = run_lib(spec, inp)
+    torch.cuda.synchronize()
+    lens = np.asarray(spec.ctx_lens)
+    rng = np.random.default_rng(5)
+    ids = sorted(set([int(lens.argmin()), int(lens.argmax())] + rng.choice(256, 10, replace=False).tolist()))
+    sub = compact_requests(inp, ids)
+    ro, rl = run_oracle(spec, sub)
+    assert_parity(metrics(out[ids], lse[ids], ro, rl), spec.name)
+    del inp
+    torch.cuda.empty_cache()
