@@ -160,6 +160,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def reduce_over_ranks(times, nbytes, device):
+    """Slowest rank's times (MAX) and the job's bytes (SUM); identity on one rank."""
+    import torch
+    import torch.distributed as dist
+
+    vals = torch.tensor(list(times) + [float(nbytes)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        t = vals[:-1].clone()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        b = vals[-1:].clone()
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+        vals = torch.cat([t, b])
+    out = [float(x) for x in vals.tolist()]
+    return out[:-1], out[-1]
+
+
 def time_oracle_sample(spec, budget_s: float = 15.0, device_inputs=None):
     """Run the oracle on a bounded sample of the workload's requests.
 
@@ -323,6 +339,8 @@ def main():
     k_ms = []
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)   # torch creates the CUDA events on first record
+    e1.record(stream)
     for k in range(max(3, min(args.steps, 20))):
         flush.fill_(k & 0xFF)
         rc = dflash.block_attn_timed_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
@@ -363,14 +381,7 @@ def main():
 
     # Max over ranks (time) and sum (bytes) for the whole-job figures.
     kv_bytes = spec.kv_bytes()
-    vals = torch.tensor([ms, split_ms, e2e_ms, float(kv_bytes)], dtype=torch.float64, device=dev)
-    if world > 1:
-        t = vals[:3].clone()
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        s = vals[3:].clone()
-        dist.all_reduce(s, op=dist.ReduceOp.SUM)
-        vals = torch.cat([t, s])
-    ms, split_ms, e2e_ms, total_bytes = [float(x) for x in vals.tolist()]
+    (ms, split_ms, e2e_ms), total_bytes = reduce_over_ranks([ms, split_ms, e2e_ms], kv_bytes, dev)
 
     peaks = measured_peaks()
     gbs = total_bytes / (ms * 1e-3) / 1e9

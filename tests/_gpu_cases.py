@@ -2,9 +2,16 @@
 seeded inputs and compare them.
 
 Tolerances (from the stated bar for bf16 outputs, with the readings recorded
-in the design doc): relative L2 error of ``out`` against the unrounded fp64 oracle
-< 5e-3; max abs error of ``out`` against the oracle rounded once to bf16
-(nearest-even) <= 1e-2; max abs error of the base-2 LSE <= 1e-3.
+in DESIGN.md):
+* relative L2 error of ``out`` against the unrounded fp64 oracle < 5e-3;
+* max abs error of ``out`` beyond the bf16 format's own rounding <= 1e-2:
+  ``max_i (|gpu_i - oracle_i| - ulp_bf16(oracle_i) / 2) <= 1e-2``.  Any bf16
+  output is off by up to half an ulp from the exact value (0.0078 at
+  |x| in [2, 4)), and a value near a rounding midpoint may round either way,
+  so the bound is applied to the error the computation adds;
+* the pages' own form, max abs <= 8 bf16 ulp at the largest expected
+  magnitude (PR #20374, test coverage), on the raw error;
+* max abs error of the base-2 LSE <= 1e-3.
 """
 
 import numpy as np
@@ -44,15 +51,27 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
 
 
+def ulp_bf16(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |x| (8 significant bits); 2^-133 below the normals."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
 def metrics(gpu_out, gpu_lse, ora_out, ora_lse) -> dict:
     g = gpu_out.detach().cpu().to(torch.float64).numpy()
     gl = gpu_lse.detach().cpu().to(torch.float64).numpy()
-    diff = g - ora_out
+    diff = np.abs(g - ora_out)
+    if g.size == 0:
+        return {"rel_l2": 0.0, "max_abs_excess": 0.0, "max_abs_vs_bf16": 0.0, "max_abs_raw": 0.0,
+                "ulp_at_max": 0.0, "lse_abs": 0.0, "nan": False}
     return {
-        "rel_l2": float(np.linalg.norm(diff) / max(np.linalg.norm(ora_out), 1e-300)),
-        "max_abs_vs_bf16": float(np.max(np.abs(g - bf16_round(ora_out)))) if g.size else 0.0,
-        "max_abs_raw": float(np.max(np.abs(diff))) if g.size else 0.0,
-        "lse_abs": float(np.max(np.abs(gl - ora_lse))) if gl.size else 0.0,
+        "rel_l2": float(np.linalg.norm(g - ora_out) / max(np.linalg.norm(ora_out), 1e-300)),
+        "max_abs_excess": float(np.max(diff - ulp_bf16(ora_out) / 2)),
+        "max_abs_vs_bf16": float(np.max(np.abs(g - bf16_round(ora_out)))),
+        "max_abs_raw": float(np.max(diff)),
+        "ulp_at_max": float(ulp_bf16(np.array([np.max(np.abs(ora_out))]))[0]),
+        "lse_abs": float(np.max(np.abs(gl - ora_lse))),
         "nan": bool(np.isnan(g).any() or np.isnan(gl).any()),
     }
 
@@ -60,7 +79,8 @@ def metrics(gpu_out, gpu_lse, ora_out, ora_lse) -> dict:
 def assert_parity(m: dict, what: str = ""):
     assert not m["nan"], f"{what}: NaN in output {m}"
     assert m["rel_l2"] < REL_L2_MAX, f"{what}: {m}"
-    assert m["max_abs_vs_bf16"] <= MAX_ABS_MAX, f"{what}: {m}"
+    assert m["max_abs_excess"] <= MAX_ABS_MAX, f"{what}: {m}"
+    assert m["max_abs_raw"] <= 8 * m["ulp_at_max"], f"{what}: {m}"
     assert m["lse_abs"] <= LSE_ABS_MAX, f"{what}: {m}"
 
 
