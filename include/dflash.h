@@ -147,6 +147,39 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
                             size_t workspace_bytes, void* stream, void* split_start,
                             void* split_done);
 
+/*
+ * Size of the scratch array compiled into the library for
+ * dflash_block_attn_static_ws: 32 MiB on every GPU that loads the library,
+ * held until the process exits.
+ */
+#define DFLASH_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * dflash_block_attn without a caller workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory where they call the attention: code running while a
+ * stream is captured under a mode that forbids cudaMalloc, plugins whose host
+ * framework owns all device memory and passes them no scratch buffer, and
+ * latency-critical paths that must not enter an allocator.  The partial
+ * softmax state lives in a file-scope device array of
+ * DFLASH_STATIC_SCRATCH_BYTES instead; the call allocates nothing and runs
+ * the same kernels as dflash_block_attn.  Inputs and outputs are as there.
+ *   - Parameter sets whose dflash_workspace_size exceeds
+ *     DFLASH_STATIC_SCRATCH_BYTES are refused with DFLASH_ERR_WORKSPACE and
+ *     nothing is launched.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress); make that first call before capturing a
+ *     stream.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  The kernels need no part of it to start at zero, and the
+ *     device status word inside it is not reported here.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on the
+ *     array: order them on one stream.
+ */
+int dflash_block_attn_static_ws(const dflash_params* p, const void* q, const void* k_pages,
+                                const void* v_pages, const int32_t* page_table,
+                                const int32_t* ctx_lens, void* out, float* lse2, void* stream);
+
 /* Static text for a return code. */
 const char* dflash_status_string(int status);
 

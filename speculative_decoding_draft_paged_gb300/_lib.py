@@ -32,6 +32,7 @@ EXPORTS = (
     "dflash_plan",
     "dflash_block_attn",
     "dflash_block_attn_timed",
+    "dflash_block_attn_static_ws",
     "dflash_status_string",
     "dflash_read_device_status",
     "dflash_clear_device_status",
@@ -104,6 +105,8 @@ def load() -> ctypes.CDLL:
             lib.dflash_block_attn.restype = i32
             lib.dflash_block_attn_timed.argtypes = lib.dflash_block_attn.argtypes + [vp, vp]
             lib.dflash_block_attn_timed.restype = i32
+            lib.dflash_block_attn_static_ws.argtypes = [ctypes.POINTER(Params)] + [vp] * 8
+            lib.dflash_block_attn_static_ws.restype = i32
             lib.dflash_status_string.argtypes = [i32]
             lib.dflash_status_string.restype = ctypes.c_char_p
             lib.dflash_read_device_status.argtypes = [vp, vp]
