@@ -73,10 +73,10 @@ typedef struct dflash_params {
   int32_t block_size;        /* K draft tokens per request, 1..16; G*K <= 128 */
   int32_t window;            /* W: 0 = unwindowed; W >= K = causal window (L+i-W, L+i] */
   int32_t future_keys;       /* 1: non-causal block (all K block keys); 0: causal block */
-  float   scale;             /* softmax scale, applied to q.k in fp32 */
+  float   scale;             /* softmax scale > 0, applied to q.k in fp32 */
   int32_t max_ctx_len;       /* host bound on every ctx_lens[b]; sizes the plan */
   int32_t force_path;        /* DFLASH_PATH_*; 0 picks by the packed row count */
-  int32_t force_split_tiles; /* > 0: key tiles per split unit (tests); 0 = planner */
+  int32_t force_split_tiles; /* 1..64: key tiles per split unit (tests); 0 = planner */
   int32_t reserved[4];       /* must be zero */
 } dflash_params;
 

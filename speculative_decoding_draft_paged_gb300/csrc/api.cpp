@@ -77,7 +77,7 @@ bool params_valid(const dflash_params* p) {
   if (G * p->block_size > kMaxRows) return false;
   if (p->window < 0 || (p->window > 0 && p->window < p->block_size)) return false;
   if (p->future_keys != 0 && p->future_keys != 1) return false;
-  if (!std::isfinite(p->scale)) return false;
+  if (!std::isfinite(p->scale) || !(p->scale > 0.f)) return false;
   // Positions are 32-bit on the device: keep L + K + a tile well inside int32.
   if (p->max_ctx_len < 0 || p->max_ctx_len > (1 << 30)) return false;
   if (p->max_pages_per_req < 1 || p->num_pages < 1) return false;
@@ -89,7 +89,7 @@ bool params_valid(const dflash_params* p) {
   if (static_cast<int64_t>(p->num_kv_heads) * p->page_size * p->head_dim * 2 >= (int64_t(1) << 40))
     return false;
   if (p->force_path < DFLASH_PATH_AUTO || p->force_path > DFLASH_PATH_TCGEN05) return false;
-  if (p->force_split_tiles < 0) return false;
+  if (p->force_split_tiles < 0 || p->force_split_tiles > kMaxSplitTiles) return false;
   return true;
 }
 
@@ -128,19 +128,31 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   const int mt = max_tiles(p->max_ctx_len, p->block_size, p->window, k.T);
   int C = p->force_split_tiles;
   if (C <= 0) {
+    // Cost in tile-times of one SM: the waves of units, each C tiles plus a
+    // pipeline fill of about two tiles, plus the partial state every unit
+    // writes and the combine reads back (2*R*D*4 bytes, 2R/T tiles' worth of
+    // K/V bytes).  Sized for every request at max_ctx_len; shorter requests
+    // leave units empty and the block scheduler fills the gaps.
     int ctas_per_sm = kSmemPerSm / (k.smem_bytes + 1024);
+    if (ctas_per_sm > 2048 / k.threads) ctas_per_sm = 2048 / k.threads;
     if (ctas_per_sm < 1) ctas_per_sm = 1;
-    const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 2;
-    const int64_t total = static_cast<int64_t>(p->batch) * p->num_kv_heads * mt;
-    int64_t c = (total + target - 1) / target;
-    // Partial state per unit is about R*D*4 bytes, written and read once
-    // (2*R*D*4), against C*T*D*4 bytes of K and V: keep it under 1/8 of them.
-    const int64_t c_min = (16 * static_cast<int64_t>(k.R) + k.T - 1) / k.T;
-    if (c < c_min) c = c_min;
-    if (c > 64) c = 64;
-    if (c > mt) c = mt;
-    if (c < 1) c = 1;
-    C = static_cast<int>(c);
+    const double slots = static_cast<double>(num_sms) * ctas_per_sm;
+    const double pairs = static_cast<double>(p->batch) * p->num_kv_heads;
+    const double partial_tiles = 2.0 * k.R / k.T;
+    double best = 1e300;
+    C = 1;
+    const int c_hi = mt < kMaxSplitTiles ? mt : kMaxSplitTiles;
+    for (int c = 1; c <= c_hi; ++c) {
+      const int S = (mt + c - 1) / c;
+      if (S > 65535) continue;
+      const double units = pairs * S;
+      const double waves = std::ceil(units / slots);
+      const double cost = waves * (c + 2.0) + units * partial_tiles / slots;
+      if (cost <= best * (1.0 + 1e-12)) {
+        best = cost;
+        C = c;
+      }
+    }
   }
   k.C = C;
   k.S = (mt + C - 1) / C;

@@ -63,87 +63,148 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) combine_kernel(const Attn
   const Geometry geo = make_geometry(active ? __ldg(&a.ctx_lens[b]) : 0, a.max_ctx_len, a.K, a.W,
                                      a.T, a.C);
 
-  // Scores of the later block keys (inputs only: overlaps the split kernel).
+  // Scores and value rows of the later block keys (inputs only: this runs
+  // while the split kernel finishes).  Lane t looks up the page of key
+  // j = i+1+t; then every key and value row is requested before any is used.
   const bool fold = active && a.future_keys && (i + 1 < a.K);
-  float sj[kMaxBlock];
-  int64_t vrow[kMaxBlock];
-  int n_fold = 0;
+  const int nf = fold ? a.K - 1 - i : 0;
+  float sj[kMaxBlock - 1];
+  float vv[kMaxBlock - 1][V];
+  bool live[kMaxBlock - 1];
   if (fold) {
+    int page = -1;
+    int off_slot = 0;
+    if (lane < nf) {
+      const int pos = geo.L + i + 1 + lane;
+      page = __ldg(&a.page_table[static_cast<size_t>(b) * a.max_pages + pos / a.P]);
+      off_slot = pos % a.P;
+      if (page < 0 || page >= a.num_pages) {
+        flag_status(a.status, DFLASH_STATUS_BAD_PAGE);
+        page = -1;
+      }
+    }
     float qv[V];
     load_bf16_slice<D>(a.q + static_cast<size_t>(row_id) * D + lane * V, qv);
-    const int32_t* table_row = a.page_table + static_cast<size_t>(b) * a.max_pages;
-    for (int j = i + 1; j < a.K; ++j) {
-      const int pos = geo.L + j;
-      const int page = __ldg(&table_row[pos / a.P]);
-      if (page < 0 || page >= a.num_pages) {
-        if (lane == 0) flag_status(a.status, DFLASH_STATUS_BAD_PAGE);
-        continue;
-      }
-      const int64_t off =
-          ((static_cast<int64_t>(page) * a.Hkv + h) * a.P + (pos % a.P)) * static_cast<int64_t>(D);
-      float kv[V];
-      load_bf16_slice<D>(a.k_pages + off + lane * V, kv);
-      float dot = 0.f;
+    float kv[kMaxBlock - 1][V];
 #pragma unroll
-      for (int e = 0; e < V; ++e) dot = fmaf(qv[e], kv[e], dot);
+    for (int t = 0; t < kMaxBlock - 1; ++t) {
+      const int pg = __shfl_sync(0xffffffffu, page, t);
+      const int sl = __shfl_sync(0xffffffffu, off_slot, t);
+      live[t] = t < nf && pg >= 0;
+      if (live[t]) {
+        const int64_t off =
+            ((static_cast<int64_t>(pg) * a.Hkv + h) * a.P + sl) * static_cast<int64_t>(D) + lane * V;
+        load_bf16_slice<D>(a.k_pages + off, kv[t]);
+        load_bf16_slice<D>(a.v_pages + off, vv[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxBlock - 1; ++t) {
+      if (t >= nf) break;  // uniform over the warp
+      float dot = 0.f;
+      if (live[t]) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) dot = fmaf(qv[e], kv[t][e], dot);
+      }
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
-      sj[n_fold] = dot * a.scale_log2;
-      vrow[n_fold] = off;
-      ++n_fold;
+      sj[t] = dot * a.scale_log2;
     }
   }
 
   pdl_wait_primary();
   if (!active) return;
 
-  // 1. Combine the split units.
+  // 1. Combine the split units.  Lanes take splits lane, lane+32, ...: their
+  //    base-2 LSEs give the row max and the weights 2^(lse_s - M) in
+  //    parallel; then every lane sums its D/32 output columns over the
+  //    splits, eight partial rows in flight at a time.
   const size_t unit0 = (static_cast<size_t>(b) * a.Hkv + h) * a.S;
+  const int ns = geo.n_splits;
+  constexpr int kW = 8;  // weights kept in registers per lane: splits < 256
+  float wreg[kW];
   float M = neg_inf_f();
-  for (int s = lane; s < geo.n_splits; s += 32)
-    M = fmaxf(M, a.part_lse[(unit0 + s) * a.R + r]);
+#pragma unroll
+  for (int k = 0; k < kW; ++k) {
+    const int sp = lane + 32 * k;
+    wreg[k] = sp < ns ? a.part_lse[(unit0 + sp) * a.R + r] : neg_inf_f();
+    M = fmaxf(M, wreg[k]);
+  }
+  for (int sp = lane + 32 * kW; sp < ns; sp += 32) M = fmaxf(M, a.part_lse[(unit0 + sp) * a.R + r]);
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+  float den = 0.f;
+#pragma unroll
+  for (int k = 0; k < kW; ++k) {
+    wreg[k] = (wreg[k] == neg_inf_f()) ? 0.f : exp2f(wreg[k] - M);
+    den += wreg[k];
+  }
+  for (int sp = lane + 32 * kW; sp < ns; sp += 32) {
+    const float ls = a.part_lse[(unit0 + sp) * a.R + r];
+    den += (ls == neg_inf_f()) ? 0.f : exp2f(ls - M);
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
 
   float acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
-  float den = 0.f;
   if (M != neg_inf_f()) {
-    for (int s = 0; s < geo.n_splits; ++s) {
-      const size_t u = unit0 + s;
-      const float ls = a.part_lse[u * a.R + r];
-      if (ls == neg_inf_f()) continue;
-      const float w = exp2f(ls - M);
-      den += w;
-      const float* po = a.part_o + (u * a.R + r) * D + lane * V;
-      if constexpr (V == 2) {
-        const float2 v = *reinterpret_cast<const float2*>(po);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-      } else {
-        const float4 v = *reinterpret_cast<const float4*>(po);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+      float ov[8][V];
+      float wv[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int sp = s0 + t;
+        const int spc = sp < ns ? sp : ns - 1;
+        const float* po = a.part_o + ((unit0 + spc) * a.R + r) * D + lane * V;
+        if constexpr (V == 2) {
+          const float2 v = *reinterpret_cast<const float2*>(po);
+          ov[t][0] = v.x;
+          ov[t][1] = v.y;
+        } else {
+          const float4 v = *reinterpret_cast<const float4*>(po);
+          ov[t][0] = v.x;
+          ov[t][1] = v.y;
+          ov[t][2] = v.z;
+          ov[t][3] = v.w;
+        }
+        float w;
+        if (sp < 32 * kW) {
+          float wk = 0.f;
+#pragma unroll
+          for (int k = 0; k < kW; ++k)
+            if ((sp >> 5) == k) wk = wreg[k];
+          w = __shfl_sync(0xffffffffu, wk, sp & 31);
+        } else {
+          const float ls = a.part_lse[(unit0 + spc) * a.R + r];
+          w = (ls == neg_inf_f()) ? 0.f : exp2f(ls - M);
+        }
+        wv[t] = sp < ns ? w : 0.f;
       }
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(wv[t], ov[t][e], acc[e]);
     }
   }
 
   // 2. Fold the later block keys: running (m, l, acc) with O = acc / l.
   float m_run = M;
   float l_run = den;
-  for (int t = 0; t < n_fold; ++t) {
-    const float m_new = fmaxf(m_run, sj[t]);
-    const float c = (m_run == neg_inf_f()) ? 0.f : exp2f(m_run - m_new);
-    const float p = exp2f(sj[t] - m_new);
-    float vv[V];
-    load_bf16_slice<D>(a.v_pages + vrow[t] + lane * V, vv);
+  if (fold) {
 #pragma unroll
-    for (int e = 0; e < V; ++e) acc[e] = fmaf(p, vv[e], acc[e] * c);
-    l_run = l_run * c + p;
-    m_run = m_new;
+    for (int t = 0; t < kMaxBlock - 1; ++t) {
+      if (t >= nf) break;
+      if (!live[t]) continue;
+      const float m_new = fmaxf(m_run, sj[t]);
+      const float c = (m_run == neg_inf_f()) ? 0.f : exp2f(m_run - m_new);
+      const float p = exp2f(sj[t] - m_new);
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = fmaf(p, vv[t][e], acc[e] * c);
+      l_run = l_run * c + p;
+      m_run = m_new;
+    }
   }
 
   // 3. Write.

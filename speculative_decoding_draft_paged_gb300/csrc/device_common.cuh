@@ -66,6 +66,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// Warp-uniform form of mbar_wait for code that continues with warp-collective
+// instructions: lane 0 waits with the bound, every lane gets its verdict, and
+// on success each lane observes the completed phase itself (acquire).  The
+// caller guarantees the barrier cannot complete a further phase meanwhile.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (ok) (void)mbar_wait(bar, parity);
+  return ok;
+}
+
 // 4-D tiled TMA load (box of the tensor map) into shared memory, completing
 // transaction bytes on `bar`.  Coordinates: (x = dim, y = slot, z = head, w = page).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -139,6 +151,29 @@ __device__ __forceinline__ uint32_t swz_offset(int row, int chunk, int rows_per_
 
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
   atomicOr(status, bits);
+}
+
+// Page ids of the unit's page-table slots [slot_first, slot_first + n_slots),
+// looked up by every thread of the CTA into shared memory before the
+// pipeline starts, so the TMA producer never waits on a table read.  Slots
+// outside [slot_lo, slot_hi) (not visible to any row) and out-of-range ids
+// become -1, which the TMA unit turns into a zero-filled box.
+__device__ __forceinline__ void load_unit_pages(const AttnArgs& a, int b, int slot_first,
+                                                int n_slots, int slot_lo, int slot_hi,
+                                                int* pg_smem) {
+  const int32_t* table_row = a.page_table + static_cast<size_t>(b) * a.max_pages;
+  for (int k = threadIdx.x; k < n_slots; k += blockDim.x) {
+    const int slot = slot_first + k;
+    int page = -1;
+    if (slot >= slot_lo && slot < slot_hi) {
+      page = __ldg(&table_row[slot]);
+      if (page < 0 || page >= a.num_pages) {
+        flag_status(a.status, DFLASH_STATUS_BAD_PAGE);
+        page = -1;
+      }
+    }
+    pg_smem[k] = page;
+  }
 }
 
 // Programmatic dependent launch controls.

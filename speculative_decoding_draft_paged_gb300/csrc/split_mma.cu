@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(288, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + a.R_pad * D * 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS);
   volatile int* issued_count = abort_flag + 1;
+  int* pg_smem = const_cast<int*>(abort_flag) + 4;  // kMaxUnitSlots page ids
   auto full_bar = [&](int st) { return bar_u32 + 8u * st; };
   auto empty_bar = [&](int st) { return bar_u32 + 8u * (NS + st); };
 
@@ -90,6 +91,10 @@ __global__ void __launch_bounds__(288, 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
   }
+
+  const int pages_per_tile = T / a.P;
+  load_unit_pages(a, b, tile0 * pages_per_tile, ntiles * pages_per_tile, geo.lo_min / a.P,
+                  (geo.hi_max + a.P - 1) / a.P, pg_smem);
 
   // Packed query tile: row r = i*G + g  <-  q[b, i, h*G + g, :]; rows >= R are zero.
   {
@@ -110,14 +115,13 @@ __global__ void __launch_bounds__(288, 1)
     }
   }
   __syncthreads();
+  // Every CTA of this grid is resident once the last one gets here: the
+  // combine kernel may launch and start on its input-only work.
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const int pages_per_tile = T / a.P;
-      const int slot_lo = geo.lo_min / a.P;
-      const int slot_hi = (geo.hi_max + a.P - 1) / a.P;
-      const int32_t* table_row = a.page_table + static_cast<size_t>(b) * a.max_pages;
       for (int it = 0; it < ntiles; ++it) {
         const int st = it % NS;
         if (it >= NS) {
@@ -131,17 +135,8 @@ __global__ void __launch_bounds__(288, 1)
         mbar_arrive_expect_tx(full_bar(st), kStageBytes);
         const uint32_t k_dst = base_u32 + st * kStageBytes;
         const uint32_t v_dst = k_dst + kTileBytes;
-        const int slot0 = (tile0 + it) * pages_per_tile;
         for (int j = 0; j < pages_per_tile; ++j) {
-          const int slot = slot0 + j;
-          int page = -1;
-          if (slot >= slot_lo && slot < slot_hi) {
-            page = __ldg(&table_row[slot]);
-            if (page < 0 || page >= a.num_pages) {
-              flag_status(a.status, DFLASH_STATUS_BAD_PAGE);
-              page = -1;
-            }
-          }
+          const int page = pg_smem[it * pages_per_tile + j];
 #pragma unroll
           for (int x = 0; x < D / 64; ++x) {
             const uint32_t off = x * T * 128 + j * a.P * 128;
@@ -201,7 +196,7 @@ __global__ void __launch_bounds__(288, 1)
     bool aborted = false;
     for (int it = 0; it < ntiles; ++it) {
       const int st = it % NS;
-      if (!mbar_wait(full_bar(st), (it / NS) & 1)) {
+      if (!mbar_wait_warp(full_bar(st), (it / NS) & 1)) {
         flag_status(a.status, DFLASH_STATUS_TIMEOUT);
         *abort_flag = 1;
         aborted = true;
@@ -227,52 +222,62 @@ __global__ void __launch_bounds__(288, 1)
         }
       }
 
-      // Scale in fp32 to the base-2 domain and mask by select.
+      // Mask by select (boundary tiles only; uniform branch), then the row
+      // max of the raw scores (the scale is positive).
       const bool need_mask = (p0 < lo_rows_max) || (p0 + KPW > hi_rows_min);
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float x = sacc[n][e] * a.scale_log2;
-          if (need_mask) {
-            const int pos = p0 + n * 8 + 2 * (lane & 3) + (e & 1);
-            const int ri = e >> 1;
-            if (pos < lo_r[ri] || pos >= hi_r[ri]) x = neg_inf();
-          }
-          sacc[n][e] = x;
-        }
-      }
-
-      // Online softmax, base 2.  Each row's 8 lanes-quads hold disjoint keys.
-      float corr[2];
-#pragma unroll
-      for (int ri = 0; ri < 2; ++ri) {
-        float mx = neg_inf();
-#pragma unroll
-        for (int n = 0; n < NT; ++n) mx = fmaxf(mx, fmaxf(sacc[n][2 * ri], sacc[n][2 * ri + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run[ri], mx);
-        const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
-        corr[ri] = fast_exp2(m_run[ri] - m_use);
-        m_run[ri] = m_new;
-        float rs = 0.f;
+      if (need_mask) {
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const float p_a = fast_exp2(sacc[n][2 * ri] - m_use);
-          const float p_b = fast_exp2(sacc[n][2 * ri + 1] - m_use);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pos = p0 + n * 8 + 2 * (lane & 3) + (e & 1);
+            const int ri = e >> 1;
+            if (pos < lo_r[ri] || pos >= hi_r[ri]) sacc[n][e] = neg_inf();
+          }
+        }
+      }
+      // Online softmax, base 2.  The reference max of a row moves only when a
+      // tile's max passes it by more than 8 (p stays <= 2^8); then O and l are
+      // rescaled, which is exact.  The four lanes of a quad share their rows.
+      float corr[2];
+      bool any_resc = false;
+#pragma unroll
+      for (int ri = 0; ri < 2; ++ri) {
+        float m4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+          m4[n & 3] = fmaxf(m4[n & 3], fmaxf(sacc[n][2 * ri], sacc[n][2 * ri + 1]));
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx *= a.scale_log2;
+        corr[ri] = 1.f;
+        if (mx > m_run[ri] + 8.f) {
+          corr[ri] = (m_run[ri] == neg_inf()) ? 0.f : fast_exp2(m_run[ri] - mx);
+          l_run[ri] *= corr[ri];
+          m_run[ri] = mx;
+          any_resc = true;
+        }
+        const float neg_m = (m_run[ri] == neg_inf()) ? 0.f : -m_run[ri];
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const float p_a = fast_exp2(fmaf(sacc[n][2 * ri], a.scale_log2, neg_m));
+          const float p_b = fast_exp2(fmaf(sacc[n][2 * ri + 1], a.scale_log2, neg_m));
           sacc[n][2 * ri] = p_a;
           sacc[n][2 * ri + 1] = p_b;
-          rs += p_a + p_b;
+          s4[n & 3] += p_a + p_b;
         }
-        l_run[ri] = l_run[ri] * corr[ri] + rs;
+        l_run[ri] += (s4[0] + s4[1]) + (s4[2] + s4[3]);
       }
+      if (__any_sync(0xffffffffu, any_resc)) {
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= corr[0];
-        o[n][1] *= corr[0];
-        o[n][2] *= corr[1];
-        o[n][3] *= corr[1];
+        for (int n = 0; n < D / 8; ++n) {
+          o[n][0] *= corr[0];
+          o[n][1] *= corr[0];
+          o[n][2] *= corr[1];
+          o[n][3] *= corr[1];
+        }
       }
 
       // O += P V.  Value rows outside the unit's visible range may hold
@@ -386,7 +391,6 @@ __global__ void __launch_bounds__(288, 1)
     }
   }
 
-  pdl_launch_dependents();
 
   // If a wait gave up, let every copy already issued land before the CTA's
   // shared memory is released.
@@ -420,7 +424,7 @@ int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
 
 int split_mma_smem_bytes(int D, int R_pad, int /*kpw*/) {
   const int stage = (D == 64) ? MmaTile<64>::kStageBytes : MmaTile<128>::kStageBytes;
-  return 1024 + kStages * stage + R_pad * D * 2 + 8 * 2 * kStages + 16;
+  return 1024 + kStages * stage + R_pad * D * 2 + 8 * 2 * kStages + 16 + 4 * kMaxUnitSlots;
 }
 
 int split_mma_kpw(int D, int R_pad) { return kpw_for(D, R_pad); }

@@ -71,8 +71,8 @@ def base_params(**kw):
     dict(head_dim=96), dict(head_dim=256), dict(page_size=8), dict(page_size=48),
     dict(block_size=0), dict(block_size=17), dict(num_q_heads=64, num_kv_heads=2, block_size=5),
     dict(window=-1), dict(window=3), dict(future_keys=2), dict(scale=float("inf")),
-    dict(scale=float("nan")), dict(max_ctx_len=-1), dict(max_ctx_len=40 * 32 - 6),
-    dict(num_pages=0), dict(force_path=3), dict(force_split_tiles=-1),
+    dict(scale=float("nan")), dict(scale=0.0), dict(scale=-0.125), dict(max_ctx_len=-1), dict(max_ctx_len=40 * 32 - 6),
+    dict(num_pages=0), dict(force_path=3), dict(force_split_tiles=-1), dict(force_split_tiles=65),
 ])
 def test_invalid_params_rejected(dflash_lib, bad):
     d = dflash_lib

@@ -36,7 +36,7 @@ def _worker(rank, world, port, results):
 
 def test_two_rank_reduction_and_replica_specs():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     results = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), results), nprocs=world, join=True)
     r0, r1 = results[0], results[1]
