@@ -336,9 +336,10 @@ def main():
     ms = sum(call_ms) / len(call_ms)
 
     # Split-kernel duration (the dominant kernel) with events on its stream.
-    k_ms = []
+    k_ms, c_ms = [], []
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e2 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)   # torch creates the CUDA events on first record
     e1.record(stream)
     for k in range(max(3, min(args.steps, 20))):
@@ -349,9 +350,12 @@ def main():
                                          ws.data_ptr(), ws_bytes, stream.cuda_stream, e0, e1)
         if rc != 0:
             raise dflash.DflashError(rc)
-        e1.synchronize()
+        e2.record(stream)
+        e2.synchronize()
         k_ms.append(e0.elapsed_time(e1))
+        c_ms.append(e1.elapsed_time(e2))
     split_ms = sorted(k_ms)[len(k_ms) // 2]
+    combine_ms = sorted(c_ms)[len(c_ms) // 2]
 
     # End to end through the public API: per step, copy q / page table /
     # lengths from pinned host memory, run the call, read out and lse2 back.
@@ -402,6 +406,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": split_gbs / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": kernel, "kernel_us": split_ms * 1e3,
+                     "combine_kernel_us": combine_ms * 1e3,
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peaks["source"] == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",

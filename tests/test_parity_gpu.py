@@ -46,17 +46,44 @@ def test_ragged_shape(cuda_device):
     check_case(spec, cuda_device)
 
 
+@pytest.mark.parametrize("path", [dflash.PATH_MMA, dflash.PATH_TCGEN05])
 @pytest.mark.parametrize("D,P", [(64, 16), (64, 32), (128, 64), (128, 16)])
 @pytest.mark.parametrize("window,fk", [(0, 1), (0, 0), (300, 1), (300, 0)])
-def test_edge_lengths(cuda_device, D, P, window, fk):
+def test_edge_lengths(cuda_device, D, P, window, fk, path):
     K = 5
-    lens = [0, 1, P - 1, P, P + 1, 2 * P - K, 2 * P - K + 1]
+    lens = [0, 1, P - 1, P, P + 1, 2 * P - K, 2 * P - K + 1, 63, 64, 65, 127, 128]
     if window:
         lens += [window - 1, window, window + K, window + P + 3]
     spec = W.CaseSpec(f"edges_D{D}_P{P}_W{window}_fk{fk}", B=len(lens), Hq=8, Hkv=2, D=D, K=K, P=P,
                       window=window, future_keys=fk, ctx_lens=lens, seed=77, poison=True,
                       extra_pages=3, extra_table_slots=2)
-    check_case(spec, cuda_device)
+    check_case(spec, cuda_device, force_path=path)
+
+
+@pytest.mark.parametrize("G,K", [(1, 1), (4, 3), (4, 7), (13, 5), (6, 11)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_tcgen05_small_row_counts(cuda_device, G, K, D):
+    """The tcgen05 tile with most of its 128 rows padding."""
+    spec = W.CaseSpec(f"tc_rows_G{G}_K{K}_D{D}", B=2, Hq=2 * G, Hkv=2, D=D, K=K, P=32, window=0,
+                      future_keys=1, ctx_lens=[900, 61], seed=6, poison=True)
+    check_case(spec, cuda_device, force_path=dflash.PATH_TCGEN05)
+
+
+def test_paths_agree(cuda_device):
+    """Both split kernels against the oracle and against each other."""
+    spec = W.minimax(B=2, K=7, ctx_lens=[6000, 2500])
+    _, o1, l1 = check_case(spec, cuda_device, force_path=dflash.PATH_MMA)
+    _, o2, l2 = check_case(spec, cuda_device, force_path=dflash.PATH_TCGEN05)
+    d = (o1.double() - o2.double()).abs().max().item()
+    assert d <= 2 * 2.0 ** -7 * max(1.0, o1.double().abs().max().item())
+    assert (l1 - l2).abs().max().item() < 1e-3
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 4, 5, 9])
+def test_tcgen05_unit_tile_counts(cuda_device, n_tiles):
+    """Units of 1..9 tiles: both softmax groups, one of them empty, uneven."""
+    spec = W.minimax(B=2, K=7, ctx_lens=[3000, 700])
+    check_case(spec, cuda_device, force_path=dflash.PATH_TCGEN05, force_split_tiles=n_tiles)
 
 
 @pytest.mark.parametrize("G,K", [(1, 1), (4, 3), (16, 1), (3, 5), (4, 7), (6, 7), (16, 3), (5, 13),
@@ -68,7 +95,7 @@ def test_packed_row_counts(cuda_device, G, K, D):
     check_case(spec, cuda_device)
 
 
-@pytest.mark.parametrize("path", [dflash.PATH_MMA])
+@pytest.mark.parametrize("path", [dflash.PATH_MMA, dflash.PATH_TCGEN05])
 def test_forced_path_and_tiny_splits(cuda_device, path):
     """force_split_tiles=1 gives one tile per unit: many empty units for the
     short requests of a ragged batch, and the combine over many partials."""
