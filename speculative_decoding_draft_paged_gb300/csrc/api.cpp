@@ -311,8 +311,12 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   if (split_done != nullptr &&
       cudaEventRecord(static_cast<cudaEvent_t>(split_done), s) != cudaSuccess)
     return DFLASH_ERR_LAUNCH;
-  err = launch_combine(a, s, split_done == nullptr);
-  if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  // With one unit per (request, kv head) the split kernel wrote the final
+  // output itself; otherwise merge the units' partial states.
+  if (k.S > 1) {
+    err = launch_combine(a, s, split_done == nullptr);
+    if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  }
   return DFLASH_OK;
 }
 

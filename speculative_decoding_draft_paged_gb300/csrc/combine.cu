@@ -1,20 +1,14 @@
-// Combine kernel: split-KV partials -> final output, with the merge of the
-// later block keys fused in.
+// Combine kernel: split-KV partials -> final output.
 //
-// One warp per output row (request b, block token i, query head hq).  Steps:
-//  1. base-2 log-sum-exp combine of the split units' partial states
-//     (lse = log2 sum_s 2^lse_s, O = sum_s 2^(lse_s - lse) O_s), the
-//     flash-decoding merge of PR #16150 (split-KV rework);
-//  2. non-causal form only: fold every block key j > i (position L+j, read
-//     through the page table) into that state, one base-2 LSE update per key.
-//     This is the merge of the block keys after the query that PR #21130
-//     performs after the causal windowed decode (description "Why", change 1);
-//     it is skipped exactly when no later key exists (K = 1, the last token,
-//     or the causal form: PR #21130 change 2);
-//  3. write out (bf16, round to nearest even) and lse2 (fp32, base 2).
-// Launched with programmatic dependent launch: everything that does not read
-// the partials (row geometry, the query row, the later block keys' scores) is
-// done before griddepcontrol.wait.
+// One warp per output row (request b, block token i, query head hq): the
+// base-2 log-sum-exp combine of the row's split units (lse = log2 sum_s
+// 2^lse_s, O = sum_s 2^(lse_s - lse) O_s), the flash-decoding merge of
+// PR #16150 (split-KV rework), then out (bf16, nearest-even) and lse2 (fp32,
+// base 2).  The later block keys of the non-causal form are already folded
+// into the partial of the unit that holds them (its last tile), so there is
+// nothing else to merge here.  Launched only when a request has more than
+// one unit, with programmatic dependent launch: the row geometry is computed
+// before griddepcontrol.wait.
 
 #include <cuda_runtime.h>
 
@@ -26,21 +20,6 @@ namespace {
 constexpr int kWarpsPerBlock = 8;
 
 __device__ __forceinline__ float neg_inf_f() { return __int_as_float(0xff800000); }
-
-template <int D>
-__device__ __forceinline__ void load_bf16_slice(const uint16_t* src, float (&dst)[D / 32]) {
-  if constexpr (D / 32 == 2) {
-    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src));
-    dst[0] = bf16_bits_to_f32(w & 0xffffu);
-    dst[1] = bf16_bits_to_f32(w >> 16);
-  } else {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
-    dst[0] = bf16_bits_to_f32(w.x & 0xffffu);
-    dst[1] = bf16_bits_to_f32(w.x >> 16);
-    dst[2] = bf16_bits_to_f32(w.y & 0xffffu);
-    dst[3] = bf16_bits_to_f32(w.y >> 16);
-  }
-}
 
 template <int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) combine_kernel(const AttnArgs a) {
@@ -62,55 +41,6 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) combine_kernel(const Attn
   const int r = i * a.G + (hq - h * a.G);
   const Geometry geo = make_geometry(active ? __ldg(&a.ctx_lens[b]) : 0, a.max_ctx_len, a.K, a.W,
                                      a.T, a.C);
-
-  // Scores and value rows of the later block keys (inputs only: this runs
-  // while the split kernel finishes).  Lane t looks up the page of key
-  // j = i+1+t; then every key and value row is requested before any is used.
-  const bool fold = active && a.future_keys && (i + 1 < a.K);
-  const int nf = fold ? a.K - 1 - i : 0;
-  float sj[kMaxBlock - 1];
-  float vv[kMaxBlock - 1][V];
-  bool live[kMaxBlock - 1];
-  if (fold) {
-    int page = -1;
-    int off_slot = 0;
-    if (lane < nf) {
-      const int pos = geo.L + i + 1 + lane;
-      page = __ldg(&a.page_table[static_cast<size_t>(b) * a.max_pages + pos / a.P]);
-      off_slot = pos % a.P;
-      if (page < 0 || page >= a.num_pages) {
-        flag_status(a.status, DFLASH_STATUS_BAD_PAGE);
-        page = -1;
-      }
-    }
-    float qv[V];
-    load_bf16_slice<D>(a.q + static_cast<size_t>(row_id) * D + lane * V, qv);
-    float kv[kMaxBlock - 1][V];
-#pragma unroll
-    for (int t = 0; t < kMaxBlock - 1; ++t) {
-      const int pg = __shfl_sync(0xffffffffu, page, t);
-      const int sl = __shfl_sync(0xffffffffu, off_slot, t);
-      live[t] = t < nf && pg >= 0;
-      if (live[t]) {
-        const int64_t off =
-            ((static_cast<int64_t>(pg) * a.Hkv + h) * a.P + sl) * static_cast<int64_t>(D) + lane * V;
-        load_bf16_slice<D>(a.k_pages + off, kv[t]);
-        load_bf16_slice<D>(a.v_pages + off, vv[t]);
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < kMaxBlock - 1; ++t) {
-      if (t >= nf) break;  // uniform over the warp
-      float dot = 0.f;
-      if (live[t]) {
-#pragma unroll
-        for (int e = 0; e < V; ++e) dot = fmaf(qv[e], kv[t][e], dot);
-      }
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
-      sj[t] = dot * a.scale_log2;
-    }
-  }
 
   pdl_wait_primary();
   if (!active) return;
@@ -189,25 +119,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) combine_kernel(const Attn
     }
   }
 
-  // 2. Fold the later block keys: running (m, l, acc) with O = acc / l.
-  float m_run = M;
-  float l_run = den;
-  if (fold) {
-#pragma unroll
-    for (int t = 0; t < kMaxBlock - 1; ++t) {
-      if (t >= nf) break;
-      if (!live[t]) continue;
-      const float m_new = fmaxf(m_run, sj[t]);
-      const float c = (m_run == neg_inf_f()) ? 0.f : exp2f(m_run - m_new);
-      const float p = exp2f(sj[t] - m_new);
-#pragma unroll
-      for (int e = 0; e < V; ++e) acc[e] = fmaf(p, vv[t][e], acc[e] * c);
-      l_run = l_run * c + p;
-      m_run = m_new;
-    }
-  }
+  const float m_run = M;
+  const float l_run = den;
 
-  // 3. Write.
+  // 2. Write.
   const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
   uint16_t* dst = a.out + static_cast<size_t>(row_id) * D + lane * V;
   if constexpr (V == 2) {

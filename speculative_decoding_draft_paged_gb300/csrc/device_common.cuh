@@ -176,6 +176,14 @@ __device__ __forceinline__ void load_unit_pages(const AttnArgs& a, int b, int sl
   }
 }
 
+// Index of packed row r = i*G + g of kv head h of request b in the output
+// layout [B, K, Hq] (times D for `out`).
+__device__ __forceinline__ size_t out_row_index(const AttnArgs& a, int b, int h, int r) {
+  const int i = r / a.G;
+  const int g = r - i * a.G;
+  return (static_cast<size_t>(b) * a.K + i) * a.Hq + static_cast<size_t>(h) * a.G + g;
+}
+
 // Programmatic dependent launch controls.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

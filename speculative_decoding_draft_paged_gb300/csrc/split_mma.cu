@@ -3,9 +3,12 @@
 // tile.
 //
 // One CTA = one split unit (request b, kv head h, split s): a contiguous range
-// of T-key tiles of the causal part of the draft block's attention (context
-// window plus block keys j <= i, TensorRT-LLM PR #21130, change 2: "the causal
-// decode is the exact result" for that part).  The G*K query rows that share
+// of T-key tiles of the keys the draft block's rows see.  Row i sees the
+// interval [lo_i, hi_i): lo_i = max(0, L+i-W+1) (0 unwindowed) and hi_i = L+K
+// in the non-causal form -- the block keys after i are merged into the row's
+// base-2 online softmax in the tile that holds them (TensorRT-LLM PR #21130,
+// "Why" and change 1) -- or L+i+1 in the causal form, where with no later key
+// the causal decode is the exact result (change 2).  The G*K query rows that share
 // kv head h are packed into one tile (row r = i*G + g), so every K/V byte of
 // the unit is read from HBM once (PR #16150, split-KV rework: one tile of
 // packed query rows per kv head).
@@ -18,7 +21,8 @@
 // owns query rows [16 wr, 16 wr + 16) and keys [wk KPW, (wk+1) KPW) of every
 // tile, keeps its own online-softmax state in registers (base 2), and the
 // warps of a row group merge their states through shared memory at the end.
-// Output: the unit's normalised partial O and base-2 LSE in the workspace.
+// Output: the unit's normalised partial O and base-2 LSE in the workspace, or,
+// with one unit per (request, kv head), the final bf16 output and LSE.
 
 #include <cuda_runtime.h>
 
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(288, 1)
           if (lo < 0) lo = 0;
         }
         lo_r[e] = lo;
-        hi_r[e] = L + i + 1;
+        hi_r[e] = a.future_keys ? L + a.K : L + i + 1;
       } else {
         lo_r[e] = 0x7fffffff;
         hi_r[e] = -0x7fffffff;
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(288, 1)
       lo_rows_max = L + a.K - a.W;
       if (lo_rows_max < 0) lo_rows_max = 0;
     }
-    const int hi_rows_min = L + 1;  // smallest row upper bound (row i = 0)
+    const int hi_rows_min = a.future_keys ? L + a.K : L + 1;  // smallest row upper bound
 
     float m_run[2] = {neg_inf(), neg_inf()};
     float l_run[2] = {0.f, 0.f};
@@ -328,6 +332,7 @@ __global__ void __launch_bounds__(288, 1)
     const size_t unit = (static_cast<size_t>(b) * a.Hkv + h) * a.S + s;
     float* part_o = a.part_o + unit * a.R * D;
     float* part_lse = a.part_lse + unit * a.R;
+    const bool direct = a.S == 1;  // one unit per (request, kv head): final output
     (void)aborted;
 
     if constexpr (NWK == 1) {
@@ -339,10 +344,21 @@ __global__ void __launch_bounds__(288, 1)
           const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
           for (int n = 0; n < D / 8; ++n) {
-            float2 v = make_float2(o[n][2 * ri] * inv, o[n][2 * ri + 1] * inv);
-            *reinterpret_cast<float2*>(part_o + static_cast<size_t>(r) * D + n * 8 + 2 * (lane & 3)) = v;
+            const float v0 = o[n][2 * ri] * inv, v1 = o[n][2 * ri + 1] * inv;
+            if (direct)
+              *reinterpret_cast<uint32_t*>(a.out + out_row_index(a, b, h, r) * D + n * 8 +
+                                           2 * (lane & 3)) = pack_bf16x2(v0, v1);
+            else
+              *reinterpret_cast<float2*>(part_o + static_cast<size_t>(r) * D + n * 8 +
+                                         2 * (lane & 3)) = make_float2(v0, v1);
           }
-          if ((lane & 3) == 0) part_lse[r] = l > 0.f ? m_run[ri] + log2f(l) : neg_inf();
+          if ((lane & 3) == 0) {
+            const float lse = l > 0.f ? m_run[ri] + log2f(l) : neg_inf();
+            if (direct)
+              a.lse2[out_row_index(a, b, h, r)] = lse;
+            else
+              part_lse[r] = lse;
+          }
         }
       }
     } else {
@@ -385,8 +401,16 @@ __global__ void __launch_bounds__(288, 1)
             den += wt * sc_l[cwi * 16 + rr];
           }
         }
-        part_o[static_cast<size_t>(r) * D + d] = den > 0.f ? num / den : 0.f;
-        if (d == 0) part_lse[r] = den > 0.f ? M + log2f(den) : neg_inf();
+        const float v = den > 0.f ? num / den : 0.f;
+        const float lse = den > 0.f ? M + log2f(den) : neg_inf();
+        if (direct) {
+          const size_t orow = out_row_index(a, b, h, r);
+          a.out[orow * D + d] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
+          if (d == 0) a.lse2[orow] = lse;
+        } else {
+          part_o[static_cast<size_t>(r) * D + d] = v;
+          if (d == 0) part_lse[r] = lse;
+        }
       }
     }
   }

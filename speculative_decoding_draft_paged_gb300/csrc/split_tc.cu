@@ -3,9 +3,10 @@
 // the attention-DP 64/4-head drafter ranks at block size 7).
 //
 // One CTA = one split unit (request b, kv head h, split s) over T = 64-key
-// tiles of the causal part of the block's attention (context window plus
-// block keys j <= i; TensorRT-LLM PR #21130, change 2), like the mma.sync
-// kernel; the packed query tile (row r = i*G + g, PR #16150: query rows of
+// tiles of the keys the block's rows see (row i: [lo_i, L+K) non-causal, the
+// later block keys merged in the tile that holds them, or [lo_i, L+i+1)
+// causal; TensorRT-LLM PR #21130), like the mma.sync kernel; the packed
+// query tile (row r = i*G + g, PR #16150: query rows of
 // one kv head packed so the KV is read once) is the A operand of QK^T.
 //
 // Warp roles (320 threads):
@@ -27,7 +28,8 @@
 //                    and writes P_j = 2^(s - m) in bf16 to its group's shared
 //                    P buffer, the A operand of the PV MMA.  At the end group 0
 //                    merges both groups' (O, m, l), like two splits, and
-//                    writes the unit's normalised partial.
+//                    writes the unit's normalised partial -- or, with one unit
+//                    per (request, kv head), the final bf16 output and LSE.
 // Every mbarrier wait is bounded (DFLASH_STATUS_TIMEOUT, then drain).
 
 #include <cuda_runtime.h>
@@ -270,14 +272,14 @@ __global__ void __launch_bounds__(320, 1)
         lo_r = L + i - a.W + 1;
         if (lo_r < 0) lo_r = 0;
       }
-      hi_r = L + i + 1;
+      hi_r = a.future_keys ? L + a.K : L + i + 1;
     }
     int lo_rows_max = 0;
     if (a.W > 0) {
       lo_rows_max = L + a.K - a.W;
       if (lo_rows_max < 0) lo_rows_max = 0;
     }
-    const int hi_rows_min = L + 1;
+    const int hi_rows_min = a.future_keys ? L + a.K : L + 1;
 
     float m_ref = ninf();
     float l_run = 0.f;
@@ -409,29 +411,46 @@ __global__ void __launch_bounds__(320, 1)
         const float l = w0 * l_run + w1 * other.y;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const size_t unit = (static_cast<size_t>(b) * a.Hkv + h) * a.S + s;
+        const bool direct = a.S == 1;  // one unit per (request, kv head): final output
+        const size_t orow = row < a.R ? out_row_index(a, b, h, row) : 0;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o0[32], o1[32];
           tmem_ld32_wait(lane_addr + C::kColO0 + cc * 32, o0);
           tmem_ld32_wait(lane_addr + C::kColO1 + cc * 32, o1);
           if (row < a.R) {
-            float4* dst = reinterpret_cast<float4*>(a.part_o + (unit * a.R + row) * D + cc * 32);
+            float v[32];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float v[4];
+            for (int e = 0; e < 32; ++e) {
+              // A group that saw no key never wrote its accumulator: select,
+              // so its uninitialised columns cannot leak in.
+              const float a0 = w0 > 0.f ? w0 * __uint_as_float(o0[e]) : 0.f;
+              const float a1 = w1 > 0.f ? w1 * __uint_as_float(o1[e]) : 0.f;
+              v[e] = (a0 + a1) * inv;
+            }
+            if (direct) {
+              uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + cc * 32);
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                // A group that saw no key never wrote its accumulator: select,
-                // so its uninitialised columns cannot leak in.
-                const float a0 = w0 > 0.f ? w0 * __uint_as_float(o0[4 * e + u]) : 0.f;
-                const float a1 = w1 > 0.f ? w1 * __uint_as_float(o1[4 * e + u]) : 0.f;
-                v[u] = (a0 + a1) * inv;
-              }
-              dst[e] = make_float4(v[0], v[1], v[2], v[3]);
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_uint4(pack_bf16x2(v[8 * e], v[8 * e + 1]),
+                                    pack_bf16x2(v[8 * e + 2], v[8 * e + 3]),
+                                    pack_bf16x2(v[8 * e + 4], v[8 * e + 5]),
+                                    pack_bf16x2(v[8 * e + 6], v[8 * e + 7]));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(a.part_o + (unit * a.R + row) * D + cc * 32);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
             }
           }
         }
-        if (row < a.R) a.part_lse[unit * a.R + row] = l > 0.f ? M + log2f(l) : ninf();
+        if (row < a.R) {
+          const float lse = l > 0.f ? M + log2f(l) : ninf();
+          if (direct)
+            a.lse2[orow] = lse;
+          else
+            a.part_lse[unit * a.R + row] = lse;
+        }
       }
     }
     tc_fence_before();
