@@ -131,7 +131,7 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
     // Cost in tile-times of one SM: the waves of units, each C tiles plus a
     // pipeline fill of about two tiles, plus the partial state every unit
     // writes and the combine reads back (2*R*D*4 bytes, 2R/T tiles' worth of
-    // K/V bytes).  Sized for every request at max_ctx_len; shorter requests
+    // K/V bytes), plus the combine's latency.  Sized for every request at max_ctx_len; shorter requests
     // leave units empty and the block scheduler fills the gaps.
     int ctas_per_sm = kSmemPerSm / (k.smem_bytes + 1024);
     if (ctas_per_sm > 2048 / k.threads) ctas_per_sm = 2048 / k.threads;
@@ -147,7 +147,10 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
       if (S > 65535) continue;
       const double units = pairs * S;
       const double waves = std::ceil(units / slots);
-      const double cost = waves * (c + 2.0) + units * partial_tiles / slots;
+      // The combine walks a row's S partials eight at a time, each round
+      // about one memory latency (~ one tile time); only when S > 1.
+      const double combine = S > 1 ? std::ceil(S / 8.0) : 0.0;
+      const double cost = waves * (c + 2.0) + units * partial_tiles / slots + combine;
       if (cost <= best * (1.0 + 1e-12)) {
         best = cost;
         C = c;

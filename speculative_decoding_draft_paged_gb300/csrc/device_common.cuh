@@ -154,15 +154,15 @@ __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
 }
 
 // Page ids of the unit's page-table slots [slot_first, slot_first + n_slots),
-// looked up by every thread of the CTA into shared memory before the
+// looked up by threads tid, tid + nthreads, ... into shared memory before the
 // pipeline starts, so the TMA producer never waits on a table read.  Slots
 // outside [slot_lo, slot_hi) (not visible to any row) and out-of-range ids
 // become -1, which the TMA unit turns into a zero-filled box.
 __device__ __forceinline__ void load_unit_pages(const AttnArgs& a, int b, int slot_first,
                                                 int n_slots, int slot_lo, int slot_hi,
-                                                int* pg_smem) {
+                                                int* pg_smem, int tid, int nthreads) {
   const int32_t* table_row = a.page_table + static_cast<size_t>(b) * a.max_pages;
-  for (int k = threadIdx.x; k < n_slots; k += blockDim.x) {
+  for (int k = tid; k < n_slots; k += nthreads) {
     const int slot = slot_first + k;
     int page = -1;
     if (slot >= slot_lo && slot < slot_hi) {

@@ -40,8 +40,8 @@ struct MmaTile {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-template <int D, int KPW>
-__global__ void __launch_bounds__(288, 1)
+template <int D, int KPW, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1)
     split_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
   constexpr int T = MmaTile<D>::T;
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(288, 1)
 
   const int pages_per_tile = T / a.P;
   load_unit_pages(a, b, tile0 * pages_per_tile, ntiles * pages_per_tile, geo.lo_min / a.P,
-                  (geo.hi_max + a.P - 1) / a.P, pg_smem);
+                  (geo.hi_max + a.P - 1) / a.P, pg_smem, threadIdx.x, blockDim.x);
 
   // Packed query tile: row r = i*G + g  <-  q[b, i, h*G + g, :]; rows >= R are zero.
   {
@@ -428,14 +428,14 @@ __global__ void __launch_bounds__(288, 1)
 
 int kpw_for(int D, int R_pad) {
   const int mt = R_pad / 16;
-  if (D == 64) return mt == 1 ? 16 : (mt == 2 ? 32 : (mt <= 4 ? 64 : 128));
+  if (D == 64) return mt == 1 ? 16 : (mt <= 3 ? 32 : (mt == 4 ? 64 : 128));
   return mt == 1 ? 16 : (mt == 2 ? 32 : 64);
 }
 
-template <int D, int KPW>
+template <int D, int KPW, int MAXT = 288>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
              const CUtensorMap& tm_v, cudaStream_t stream) {
-  auto kern = split_mma_kernel<D, KPW>;
+  auto kern = split_mma_kernel<D, KPW, MAXT>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          plan.smem_bytes);
   if (err != cudaSuccess) return err;
@@ -460,7 +460,11 @@ int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMa
   if (a.D == 64) {
     switch (plan.kpw) {
       case 16: return launch_t<64, 16>(a, plan, tm_k, tm_v, stream);
-      case 32: return launch_t<64, 32>(a, plan, tm_k, tm_v, stream);
+      case 32:
+        // Three row groups of four key-slice warps need 416 threads; keep
+        // the register budget of the 288-thread form otherwise.
+        return plan.threads > 288 ? launch_t<64, 32, 416>(a, plan, tm_k, tm_v, stream)
+                                  : launch_t<64, 32, 288>(a, plan, tm_k, tm_v, stream);
       case 64: return launch_t<64, 64>(a, plan, tm_k, tm_v, stream);
       case 128: return launch_t<64, 128>(a, plan, tm_k, tm_v, stream);
     }

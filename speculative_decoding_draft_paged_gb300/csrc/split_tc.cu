@@ -9,11 +9,14 @@
 // query tile (row r = i*G + g, PR #16150: query rows of
 // one kv head packed so the KV is read once) is the A operand of QK^T.
 //
-// Warp roles (320 threads):
-//   warp 0, lane 0   TMA producer: page ids come from shared memory (looked
-//                    up by the whole CTA up front); one 128-byte-swizzled box
-//                    per (page, 64-column half) for K and for V into a
-//                    4-stage ring with separate K and V barriers;
+// Warp roles (352 threads):
+//   warp 0, lane 0   K producer, warp 10 lane 0 V producer: page ids come from
+//                    shared memory (looked up by the whole CTA up front); one
+//                    128-byte-swizzled TMA box per (page, 64-column half) into
+//                    separate K and V rings.  A K slot is released as soon as
+//                    its QK^T has completed and a V slot after its PV, so the
+//                    V loads run just ahead of their use and the K loads far
+//                    ahead, with the same shared memory as one joint ring;
 //   warp 1           allocates 512 TMEM columns; lane 0 issues the MMAs:
 //                    S_j = Q K_j^T (M=128, N=64, K=D) into TMEM S buffer j%2,
 //                    then O_{j%2} += P_j V_j (M=128, N=D, K=64);
@@ -43,18 +46,19 @@ namespace {
 template <int D>
 struct TcCfg {
   static constexpr int T = 64;               // keys per tile
-  static constexpr int NS = 4;               // pipeline stages
+  static constexpr int NSK = 4;              // K ring stages
+  static constexpr int NSV = 4;              // V ring stages
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kTileBytes = T * D * 2;  // one K or V tile
   static constexpr int kPBytes = 128 * T * 2;   // one group's P buffer
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + NS * kTileBytes;
-  static constexpr int kOffP = kOffV + NS * kTileBytes;
+  static constexpr int kOffV = kOffK + NSK * kTileBytes;
+  static constexpr int kOffP = kOffV + NSV * kTileBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  // k_full[NS], v_full[NS], kv_empty[NS], s_full[2], s_free[2], p_full[2],
-  // pv_done[2], merge
-  static constexpr int kNumBars = 3 * NS + 9;
+  // k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
+  // s_free[2], p_full[2], pv_done[2], merge
+  static constexpr int kNumBars = 2 * NSK + 2 * NSV + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffXchg = kOffMisc + 64;            // group 1's (m, l) per row
   static constexpr int kOffPages = kOffXchg + 128 * 8;
@@ -62,18 +66,19 @@ struct TcCfg {
   static constexpr int kTmemCols = 512;   // S0 [0,64) S1 [64,128) O0 [128,128+D) O1 [256,256+D)
   static constexpr int kColO0 = 128;
   static constexpr int kColO1 = 256;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
 };
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     split_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v) {
   using C = TcCfg<D>;
   constexpr int T = C::T;
-  constexpr int NS = C::NS;
+  constexpr int NSK = C::NSK;
+  constexpr int NSV = C::NSV;
 
   const int s = blockIdx.x;
   const int h = blockIdx.y;
@@ -97,17 +102,20 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sP = base + C::kOffP;
   const uint32_t bars = base + C::kOffBar;
   auto k_full = [&](int st) { return bars + 8u * st; };
-  auto v_full = [&](int st) { return bars + 8u * (NS + st); };
-  auto kv_empty = [&](int st) { return bars + 8u * (2 * NS + st); };
-  auto s_full = [&](int g) { return bars + 8u * (3 * NS + g); };
-  auto s_free = [&](int g) { return bars + 8u * (3 * NS + 2 + g); };
-  auto p_full = [&](int g) { return bars + 8u * (3 * NS + 4 + g); };
-  auto pv_done = [&](int g) { return bars + 8u * (3 * NS + 6 + g); };
-  const uint32_t merge_bar = bars + 8u * (3 * NS + 8);
+  auto k_empty = [&](int st) { return bars + 8u * (NSK + st); };
+  auto v_full = [&](int st) { return bars + 8u * (2 * NSK + st); };
+  auto v_empty = [&](int st) { return bars + 8u * (2 * NSK + NSV + st); };
+  constexpr int kB0 = 2 * NSK + 2 * NSV;
+  auto s_full = [&](int g) { return bars + 8u * (kB0 + g); };
+  auto s_free = [&](int g) { return bars + 8u * (kB0 + 2 + g); };
+  auto p_full = [&](int g) { return bars + 8u * (kB0 + 4 + g); };
+  auto pv_done = [&](int g) { return bars + 8u * (kB0 + 6 + g); };
+  const uint32_t merge_bar = bars + 8u * (kB0 + 8);
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile uint32_t* tmem_slot = misc;          // TMEM base address from tcgen05.alloc
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  volatile int* issued = reinterpret_cast<volatile int*>(misc + 2);
+  volatile int* issued_k = reinterpret_cast<volatile int*>(misc + 2);
+  volatile int* issued_v = reinterpret_cast<volatile int*>(misc + 3);
   float2* xchg = reinterpret_cast<float2*>(gbase + C::kOffXchg);
   int* pg_smem = reinterpret_cast<int*>(gbase + C::kOffPages);
 
@@ -115,10 +123,13 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int st = 0; st < NS; ++st) {
+    for (int st = 0; st < NSK; ++st) {
       mbar_init(k_full(st), 1);
+      mbar_init(k_empty(st), 1);
+    }
+    for (int st = 0; st < NSV; ++st) {
       mbar_init(v_full(st), 1);
-      mbar_init(kv_empty(st), 1);
+      mbar_init(v_empty(st), 1);
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(s_full(g), 1);
@@ -128,7 +139,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(merge_bar, 4);
     *abort_flag = 0;
-    *issued = 0;
+    *issued_k = 0;
+    *issued_v = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
@@ -137,16 +149,27 @@ __global__ void __launch_bounds__(320, 1)
     tmem_alloc(smem_u32(misc), C::kTmemCols);
     tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();  // barrier initialisation and the TMEM address are visible
+  tc_fence_after();
+  // Every CTA of this grid is resident once the last one gets here: the
+  // combine kernel may launch and start on its input-only work.
+  pdl_launch_dependents();
 
   const int pages_per_tile = T / a.P;
-  load_unit_pages(a, b, tile0 * pages_per_tile, n * pages_per_tile, geo.lo_min / a.P,
-                  (geo.hi_max + a.P - 1) / a.P, pg_smem);
-
-  // Packed query tile, K-major with the 128-byte swizzle the MMA descriptor
-  // expects: rows r = i*G + g of kv head h; rows >= R are zero.
-  {
+  uint32_t tmem = 0;
+  if (warp == 0 || warp == 10) {
+    // The producers start as soon as warp 0 has looked the unit's page ids
+    // up; they do not wait for the query tile.
+    if (warp == 0)
+      load_unit_pages(a, b, tile0 * pages_per_tile, n * pages_per_tile, geo.lo_min / a.P,
+                      (geo.hi_max + a.P - 1) / a.P, pg_smem, lane, 32);
+    named_barrier(2, 64);
+  } else {
+    // Warps 1..9: packed query tile, K-major with the 128-byte swizzle the
+    // MMA descriptor expects: rows r = i*G + g of kv head h; rows >= R zero.
     constexpr int CPR = D / 8;
-    for (int idx = threadIdx.x; idx < 128 * CPR; idx += C::kThreads) {
+    for (int idx = threadIdx.x - 32; idx < 128 * CPR; idx += 288) {
       const int row = idx / CPR;
       const int c = idx - row * CPR;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -159,38 +182,35 @@ __global__ void __launch_bounds__(320, 1)
       }
       *reinterpret_cast<uint4*>(gbase + C::kOffQ + swz_offset(row, c, 128)) = v;
     }
+    fence_proxy_async_smem();
+    named_barrier(1, 288);
+    tmem = *tmem_slot;
   }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  // Every CTA of this grid is resident once the last one gets here: the
-  // combine kernel may launch and start on its input-only work.
-  pdl_launch_dependents();
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 10) {
+    // ------------------------------------------------------------ producers
     if (lane == 0) {
+      const bool is_v = warp == 10;
+      const int ns = is_v ? NSV : NSK;
+      const uint32_t ring = is_v ? sV : sK;
+      const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+      volatile int* issued = is_v ? issued_v : issued_k;
       for (int j = 0; j < n; ++j) {
-        const int st = j % NS;
-        if (j >= NS && !mbar_wait(kv_empty(st), ((j / NS) - 1) & 1)) {
+        const int st = j % ns;
+        const uint32_t empty = is_v ? v_empty(st) : k_empty(st);
+        const uint32_t full = is_v ? v_full(st) : k_full(st);
+        if (j >= ns && !mbar_wait(empty, ((j / ns) - 1) & 1)) {
           flag_status(a.status, DFLASH_STATUS_TIMEOUT);
           *abort_flag = 1;
         }
         if (*abort_flag) break;
-        mbar_arrive_expect_tx(k_full(st), C::kTileBytes);
-        mbar_arrive_expect_tx(v_full(st), C::kTileBytes);
-        const uint32_t k_dst = sK + st * C::kTileBytes;
-        const uint32_t v_dst = sV + st * C::kTileBytes;
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        const uint32_t dst = ring + st * C::kTileBytes;
         for (int pj = 0; pj < pages_per_tile; ++pj) {
           const int page = pg_smem[j * pages_per_tile + pj];
 #pragma unroll
-          for (int x = 0; x < D / 64; ++x) {
-            const uint32_t off = x * T * 128 + pj * a.P * 128;
-            tma_load_4d(k_dst + off, &tm_k, x * 64, 0, h, page, k_full(st));
-            tma_load_4d(v_dst + off, &tm_v, x * 64, 0, h, page, v_full(st));
-          }
+          for (int x = 0; x < D / 64; ++x)
+            tma_load_4d(dst + x * T * 128 + pj * a.P * 128, map, x * 64, 0, h, page, full);
         }
         *issued = j + 1;
       }
@@ -200,12 +220,18 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, T, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      int last_pv = -1;
+      // Descriptors differ only in the start-address field (bits 0..13,
+      // address >> 4): build each base once and add offsets >> 4.
+      const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dp = smem_desc_sw128(sP, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(sV, T * 128, 1024);
+      int last_qk = -1, last_pv = -1;
       for (int j = 0; j <= n; ++j) {
         if (*abort_flag) break;
         if (j < n) {
-          const int st = j % NS;
-          bool ok = mbar_wait(k_full(st), (j / NS) & 1);
+          const int st = j % NSK;
+          bool ok = mbar_wait(k_full(st), (j / NSK) & 1);
           if (ok && j >= 2) ok = mbar_wait(s_free(j & 1), ((j >> 1) - 1) & 1);
           if (!ok) {
             flag_status(a.status, DFLASH_STATUS_TIMEOUT);
@@ -214,48 +240,49 @@ __global__ void __launch_bounds__(320, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem + (j & 1) * T;
-          const uint32_t k_st = sK + st * C::kTileBytes;
+          const uint32_t k_off = st * C::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const int x = kk >> 2;
+            const uint32_t x = kk >> 2;
             const uint32_t within = (kk & 3) * 32;
-            const uint64_t ad = smem_desc_sw128(sQ + x * (128 * 128) + within, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(k_st + x * (T * 128) + within, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            umma_bf16(d_tmem, dq + ((x * (128 * 128) + within) >> 4),
+                      dk + ((k_off + x * (T * 128) + within) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
           }
+          umma_commit(k_empty(st));
           umma_commit(s_full(j & 1));
+          last_qk = j;
         }
         if (j >= 1) {
           const int jj = j - 1;
-          const int st = jj % NS;
+          const int st = jj % NSV;
           const int g = jj & 1;
           bool ok = mbar_wait(p_full(g), (jj >> 1) & 1);
-          if (ok) ok = mbar_wait(v_full(st), (jj / NS) & 1);
+          if (ok) ok = mbar_wait(v_full(st), (jj / NSV) & 1);
           if (!ok) {
             flag_status(a.status, DFLASH_STATUS_TIMEOUT);
             *abort_flag = 1;
             break;
           }
           tc_fence_after();
-          const uint32_t v_st = sV + st * C::kTileBytes;
+          const uint32_t v_off = st * C::kTileBytes;
           const uint32_t o_col = g ? C::kColO1 : C::kColO0;
 #pragma unroll
-          for (int kk = 0; kk < T / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(sP + g * C::kPBytes + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(v_st + kk * 16 * 128, T * 128, 1024);
-            umma_bf16(tmem + o_col, ad, bd, idesc_pv, (jj >= 2 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(kv_empty(st));
+          for (int kk = 0; kk < T / 16; ++kk)
+            umma_bf16(tmem + o_col, dp + ((g * C::kPBytes + kk * 32) >> 4),
+                      dv + ((v_off + kk * 16 * 128) >> 4), idesc_pv, (jj >= 2 || kk > 0) ? 1u : 0u);
+          umma_commit(v_empty(st));
           umma_commit(pv_done(g));
           last_pv = jj;
         }
       }
       // Let the last commits land before the CTA winds down.
-      for (int jj = last_pv - NS + 1; jj <= last_pv; ++jj)
-        if (jj >= 0) (void)mbar_wait(kv_empty(jj % NS), (jj / NS) & 1);
+      for (int jj = last_qk - NSK + 1; jj <= last_qk; ++jj)
+        if (jj >= 0) (void)mbar_wait(k_empty(jj % NSK), (jj / NSK) & 1);
+      for (int jj = last_pv - NSV + 1; jj <= last_pv; ++jj)
+        if (jj >= 0) (void)mbar_wait(v_empty(jj % NSV), (jj / NSV) & 1);
     }
   } else {
-    // ------------------------------------------------------------ softmax
+    // ------------------------------------------------------------ softmax (warps 2..9)
     const int sw = warp - 2;          // 0..7
     const int grp = sw >> 2;          // tiles j = grp, grp+2, ...
     const int quad = warp & 3;        // TMEM lane quadrant of this warp
@@ -355,8 +382,8 @@ __global__ void __launch_bounds__(320, 1)
       // Value rows outside [lo_min, L+K) may hold anything: zero them in the
       // stage before the PV MMA reads it (boundary tiles only).
       if (p0 < geo.lo_min || p0 + T > geo.hi_max) {
-        const int st = j % NS;
-        if (!mbar_wait_warp(v_full(st), (j / NS) & 1)) { ok = false; break; }
+        const int st = j % NSV;
+        if (!mbar_wait_warp(v_full(st), (j / NSV) & 1)) { ok = false; break; }
         if (gthread < T) {
           const int pos = p0 + gthread;
           if (pos < geo.lo_min || pos >= geo.hi_max) {
@@ -458,11 +485,9 @@ __global__ void __launch_bounds__(320, 1)
 
   __syncthreads();
   if (*abort_flag && threadIdx.x == 0) {
-    const int iss = *issued;
-    for (int j = iss > NS ? iss - NS : 0; j < iss; ++j) {
-      (void)mbar_wait(k_full(j % NS), (j / NS) & 1);
-      (void)mbar_wait(v_full(j % NS), (j / NS) & 1);
-    }
+    const int ik = *issued_k, iv = *issued_v;
+    for (int j = ik > NSK ? ik - NSK : 0; j < ik; ++j) (void)mbar_wait(k_full(j % NSK), (j / NSK) & 1);
+    for (int j = iv > NSV ? iv - NSV : 0; j < iv; ++j) (void)mbar_wait(v_full(j % NSV), (j / NSV) & 1);
   }
   __syncthreads();
   if (warp == 1) {
