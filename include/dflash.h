@@ -60,7 +60,8 @@ extern "C" {
 /* Kernel-path selection for dflash_params.force_path. */
 #define DFLASH_PATH_AUTO             0
 #define DFLASH_PATH_MMA              1  /* warp-level mma.sync tiles (any R <= 128) */
-#define DFLASH_PATH_TCGEN05          2  /* tcgen05 / TMEM, one 128-row tile per kv head */
+#define DFLASH_PATH_TCGEN05          2  /* tcgen05 / TMEM, one 128-row tile per kv head;
+                                           batch <= 768 */
 
 typedef struct dflash_params {
   int32_t batch;             /* B >= 1 requests */
@@ -76,19 +77,27 @@ typedef struct dflash_params {
   float   scale;             /* softmax scale > 0, applied to q.k in fp32 */
   int32_t max_ctx_len;       /* host bound on every ctx_lens[b]; sizes the plan */
   int32_t force_path;        /* DFLASH_PATH_*; 0 picks by the packed row count */
-  int32_t force_split_tiles; /* 1..64: key tiles per split unit (tests); 0 = planner */
+  int32_t force_split_tiles; /* 1..64: key tiles per split unit, or per CTA range on
+                                the tcgen05 path (tests); 0 = planner */
   int32_t reserved[4];       /* must be zero */
 } dflash_params;
 
-/* What the planner chose for a parameter set (for tests and benchmarks). */
+/*
+ * What the planner chose for a parameter set (for tests and benchmarks).
+ * mma.sync path: a grid of B * Hkv * max_splits units of split_tiles tiles.
+ * tcgen05 path: `units` persistent CTAs (at most one per SM) that share the
+ * key tiles of all (request, kv head) pairs laid end to end, split_tiles
+ * each at max_ctx_len (fewer, from the actual lengths, on the device), with
+ * max_splits = 2 partial slots per CTA.
+ */
 typedef struct dflash_plan_info {
   int32_t path;              /* DFLASH_PATH_MMA or DFLASH_PATH_TCGEN05 */
   int32_t rows;              /* R = G*K packed query rows per kv head */
   int32_t rows_padded;       /* R rounded up to the kernel's row granule */
   int32_t tile_keys;         /* T: keys per pipeline stage */
-  int32_t split_tiles;       /* C: key tiles per split unit */
-  int32_t max_splits;        /* split units per (request, kv head) */
-  int64_t units;             /* B * Hkv * max_splits CTAs of the split kernel */
+  int32_t split_tiles;       /* C: key tiles per split unit / per CTA range */
+  int32_t max_splits;        /* split units per (request, kv head) / slots per CTA */
+  int64_t units;             /* CTAs of the split kernel */
   int32_t threads;           /* threads per CTA of the split kernel */
   int32_t smem_bytes;        /* dynamic shared memory per CTA of the split kernel */
   int32_t num_sms;           /* SM count the plan was sized for */
@@ -97,9 +106,10 @@ typedef struct dflash_plan_info {
 
 /*
  * Workspace bytes dflash_block_attn needs for *p on the current device: a
- * 256-byte header (status word) plus the fp32 partial softmax state of every
- * split unit (normalised output [units, R, D] and base-2 LSE [units, R]).
- * Returns 0 when *p is invalid.  Deterministic for a given device model.
+ * 256-byte header (status word) and the fp32 partial softmax state of every
+ * split unit or CTA slot (normalised output [units, R, D] and base-2 LSE
+ * [units, R]).  Returns 0 when *p is invalid.  Deterministic for a given
+ * device model.
  */
 size_t dflash_workspace_size(const dflash_params* p);
 

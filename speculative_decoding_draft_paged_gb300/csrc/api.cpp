@@ -1,6 +1,7 @@
 // C ABI of the paged draft-block attention library (include/dflash.h):
 // argument validation, the split planner, workspace sizing, TMA descriptors
-// and the two launches (split kernel, combine kernel).
+// and the launches: a split kernel (mma.sync or tcgen05) and, where a row may
+// have several partials, the combine kernel.
 
 #include <cmath>
 #include <cstdint>
@@ -93,12 +94,12 @@ bool params_valid(const dflash_params* p) {
   return true;
 }
 
-// The planner.  The split kernel's grid is (max_splits, Hkv, B): it depends on
-// the parameters only, never on the device-resident lengths, so a captured
-// graph replays for any lengths up to max_ctx_len.  Each request's visible
-// key range is cut into units of C tiles; C is chosen so that the units of the
-// largest possible batch fill the GPU about twice over, but never so small
-// that the partial state written per unit outweighs the keys it covers.
+// The planner.  Every grid depends on the parameters only, never on the
+// device-resident lengths, so a captured graph replays for any lengths up to
+// max_ctx_len.  mma.sync kernel: grid (max_splits, Hkv, B); each request's
+// visible key range is cut into units of C tiles, C chosen by a cost model
+// (waves of units, the partial state each writes, the combine).  tcgen05
+// kernel: one CTA per SM over the flat tile sequence of all pairs.
 bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   if (!params_valid(p)) return false;
   KernelPlan k{};
@@ -106,10 +107,14 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   const int D = p->head_dim;
   k.R = G * p->block_size;
   k.num_sms = num_sms;
+  // The tcgen05 kernel keeps the requests' tile prefix in shared memory and
+  // numbers the tiles of all pairs in 32 bits.
+  const int64_t tc_tiles = static_cast<int64_t>(p->batch) * p->num_kv_heads *
+                           max_tiles(p->max_ctx_len, p->block_size, p->window, split_tc_tile_keys(D));
+  const bool tc_ok = split_tc_available() && p->batch <= kTcMaxBatch && tc_tiles <= (int64_t(1) << 30);
   int path = p->force_path;
-  if (path == DFLASH_PATH_AUTO)
-    path = (k.R > 64 && split_tc_available()) ? DFLASH_PATH_TCGEN05 : DFLASH_PATH_MMA;
-  if (path == DFLASH_PATH_TCGEN05 && !split_tc_available()) return false;
+  if (path == DFLASH_PATH_AUTO) path = (k.R > 64 && tc_ok) ? DFLASH_PATH_TCGEN05 : DFLASH_PATH_MMA;
+  if (path == DFLASH_PATH_TCGEN05 && !tc_ok) return false;
   k.path = path;
   if (path == DFLASH_PATH_MMA) {
     k.R_pad = (k.R + 15) / 16 * 16;
@@ -126,6 +131,26 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
     k.smem_bytes = split_tc_smem_bytes(D);
   }
   const int mt = max_tiles(p->max_ctx_len, p->block_size, p->window, k.T);
+  if (path == DFLASH_PATH_TCGEN05) {
+    // Flat split: one CTA per SM, each taking an equal share of all pairs'
+    // tiles (computed on the device from the actual lengths, at least
+    // kTcMinTiles), or force_split_tiles tiles per CTA and enough CTAs for
+    // every pair at max_ctx_len.  Two partial slots per CTA.
+    if (p->force_split_tiles > 0) {
+      k.C = p->force_split_tiles;
+      k.units = (tc_tiles + k.C - 1) / k.C;
+    } else {
+      int64_t ctas = (tc_tiles + kTcMinTiles - 1) / kTcMinTiles;
+      if (ctas > num_sms) ctas = num_sms;
+      k.units = ctas;
+      k.C = static_cast<int>((tc_tiles + ctas - 1) / ctas);
+      if (k.C < kTcMinTiles) k.C = kTcMinTiles;
+    }
+    k.S = 2;
+    if (k.units > 0x7fffffff) return false;
+    *out = k;
+    return true;
+  }
   int C = p->force_split_tiles;
   if (C <= 0) {
     // Cost in tile-times of one SM: the waves of units, each C tiles plus a
@@ -167,9 +192,17 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Workspace: header (status word) | partial LSEs | partial outputs, each
+// region 256-byte aligned.
+
+size_t partial_rows_for(const KernelPlan& k) {
+  return static_cast<size_t>(k.units) * (k.path == DFLASH_PATH_TCGEN05 ? k.S : 1) * k.R;
+}
+
 size_t workspace_bytes_for(const dflash_params* p, const KernelPlan& k) {
-  const size_t lse = align_up(static_cast<size_t>(k.units) * k.R * sizeof(float), 256);
-  const size_t o = static_cast<size_t>(k.units) * k.R * p->head_dim * sizeof(float);
+  const size_t rows = partial_rows_for(k);
+  const size_t lse = align_up(rows * sizeof(float), 256);
+  const size_t o = rows * p->head_dim * sizeof(float);
   return kHeaderBytes + lse + o;
 }
 
@@ -207,6 +240,26 @@ bool encode_pool(CUtensorMap* map, const void* pool, const dflash_params* p) {
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D view [B*K][Hq][D] of the queries, box = (64 columns, G heads, K
+// tokens): one box is the packed tile of one (request, kv head) pair, rows
+// r = i*G + g, for one 64-column half; 128-byte swizzle.
+bool encode_queries(CUtensorMap* map, const void* q, const dflash_params* p) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->head_dim),
+                              static_cast<cuuint64_t>(p->num_q_heads),
+                              static_cast<cuuint64_t>(p->batch) * p->block_size};
+  const cuuint64_t row = static_cast<cuuint64_t>(p->head_dim) * 2;
+  const cuuint64_t strides[2] = {row, row * p->num_q_heads};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(p->block_size)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -269,8 +322,10 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   if (!make_plan(p, dev.sms, &k)) return DFLASH_ERR_INVALID;
   if (workspace_bytes < workspace_bytes_for(p, k)) return DFLASH_ERR_WORKSPACE;
 
-  CUtensorMap tm_k, tm_v;
+  const bool tc = k.path == DFLASH_PATH_TCGEN05;
+  CUtensorMap tm_k, tm_v, tm_q;
   if (!encode_pool(&tm_k, k_pages, p) || !encode_pool(&tm_v, v_pages, p)) return DFLASH_ERR_LAUNCH;
+  if (tc && !encode_queries(&tm_q, q, p)) return DFLASH_ERR_LAUNCH;
 
   AttnArgs a{};
   a.q = static_cast<const uint16_t*>(q);
@@ -282,9 +337,9 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   a.lse2 = lse2;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
-  a.part_lse = reinterpret_cast<float*>(ws + kHeaderBytes);
-  a.part_o = reinterpret_cast<float*>(
-      ws + kHeaderBytes + align_up(static_cast<size_t>(k.units) * k.R * sizeof(float), 256));
+  const size_t off_lse = kHeaderBytes;
+  a.part_lse = reinterpret_cast<float*>(ws + off_lse);
+  a.part_o = reinterpret_cast<float*>(ws + off_lse + align_up(partial_rows_for(k) * sizeof(float), 256));
   a.B = p->batch;
   a.Hq = p->num_q_heads;
   a.Hkv = p->num_kv_heads;
@@ -303,21 +358,24 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   a.T = k.T;
   a.C = k.C;
   a.S = k.S;
+  a.ncta = tc ? static_cast<int>(k.units) : 0;
+  a.qn_force = tc ? p->force_split_tiles : 0;
+  a.qn_min = kTcMinTiles;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (split_start != nullptr &&
       cudaEventRecord(static_cast<cudaEvent_t>(split_start), s) != cudaSuccess)
     return DFLASH_ERR_LAUNCH;
-  int err = (k.path == DFLASH_PATH_TCGEN05) ? launch_split_tc(a, k, tm_k, tm_v, s)
-                                            : launch_split_mma(a, k, tm_k, tm_v, s);
+  int err = tc ? launch_split_tc(a, k, tm_k, tm_v, tm_q, s) : launch_split_mma(a, k, tm_k, tm_v, s);
   if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
   if (split_done != nullptr &&
       cudaEventRecord(static_cast<cudaEvent_t>(split_done), s) != cudaSuccess)
     return DFLASH_ERR_LAUNCH;
-  // With one unit per (request, kv head) the split kernel wrote the final
-  // output itself; otherwise merge the units' partial states.
-  if (k.S > 1) {
-    err = launch_combine(a, s, split_done == nullptr);
+  // With one unit per (request, kv head) the mma.sync kernel wrote the final
+  // output itself; otherwise merge the partial states (the flat split of the
+  // tcgen05 kernel always may cut a pair).
+  if (tc || k.S > 1) {
+    err = launch_combine(a, s, split_done == nullptr, tc);
     if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
   }
   return DFLASH_OK;

@@ -1,14 +1,20 @@
 // Combine kernel: split-KV partials -> final output.
 //
 // One warp per output row (request b, block token i, query head hq): the
-// base-2 log-sum-exp combine of the row's split units (lse = log2 sum_s
+// base-2 log-sum-exp combine of the row's partials (lse = log2 sum_s
 // 2^lse_s, O = sum_s 2^(lse_s - lse) O_s), the flash-decoding merge of
 // PR #16150 (split-KV rework), then out (bf16, nearest-even) and lse2 (fp32,
 // base 2).  The later block keys of the non-causal form are already folded
-// into the partial of the unit that holds them (its last tile), so there is
-// nothing else to merge here.  Launched only when a request has more than
-// one unit, with programmatic dependent launch: the row geometry is computed
-// before griddepcontrol.wait.
+// into the partial that holds them, so there is nothing else to merge here.
+// Launched with programmatic dependent launch: everything that depends on
+// the inputs only is done before griddepcontrol.wait.
+//   mma.sync split kernel: the row's partials are the units s of its
+//   (request, kv head) pair, when a request has more than one unit.
+//   tcgen05 flat split: the pair's tiles [g0, g0 + nb) lie in the ranges of
+//   CTAs c0..c1 (range length qn, the same tile prefix as the split kernel);
+//   partial s is CTA c0 + s, slot 1 of c0 when the pair starts inside c0's
+//   range (its last segment there), else slot 0 (the first segment of the
+//   range).  A pair inside one range was written by the split kernel itself.
 
 #include <cuda_runtime.h>
 
@@ -18,112 +24,98 @@ namespace dflash {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kThreads = kWarpsPerBlock * 32;
 
 __device__ __forceinline__ float neg_inf_f() { return __int_as_float(0xff800000); }
 
-template <int D>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) combine_kernel(const AttnArgs a) {
+// Weighted sum of a row's partials into this lane's D/32 columns.  Few
+// partials (the usual case): one LSE per lane, then the partial rows four
+// at a time with their loads in flight together.  Otherwise lanes take
+// partials lane, lane+32, ... for the max and the sum, and the rows eight
+// at a time.
+template <int D, typename UnitOf>
+__device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, UnitOf unit_of,
+                                            int lane, float (&acc)[D / 32], float& M_out,
+                                            float& den_out) {
   constexpr int V = D / 32;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const long long row_id = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
-  const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
-  const bool active = row_id < rows;
-
-  int b = 0, i = 0, hq = 0;
-  if (active) {
-    hq = static_cast<int>(row_id % a.Hq);
-    const long long t = row_id / a.Hq;
-    i = static_cast<int>(t % a.K);
-    b = static_cast<int>(t / a.K);
-  }
-  const int h = hq / a.G;
-  const int r = i * a.G + (hq - h * a.G);
-  const Geometry geo = make_geometry(active ? __ldg(&a.ctx_lens[b]) : 0, a.max_ctx_len, a.K, a.W,
-                                     a.T, a.C);
-
-  pdl_wait_primary();
-  if (!active) return;
-
-  // 1. Combine the split units.  Lanes take splits lane, lane+32, ...: their
-  //    base-2 LSEs give the row max and the weights 2^(lse_s - M) in
-  //    parallel; then every lane sums its D/32 output columns over the
-  //    splits, eight partial rows in flight at a time.
-  const size_t unit0 = (static_cast<size_t>(b) * a.Hkv + h) * a.S;
-  const int ns = geo.n_splits;
-  constexpr int kW = 8;  // weights kept in registers per lane: splits < 256
-  float wreg[kW];
-  float M = neg_inf_f();
 #pragma unroll
-  for (int k = 0; k < kW; ++k) {
-    const int sp = lane + 32 * k;
-    wreg[k] = sp < ns ? a.part_lse[(unit0 + sp) * a.R + r] : neg_inf_f();
-    M = fmaxf(M, wreg[k]);
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+  auto load_row = [&](int sp, float (&o)[V]) {
+    const float* po = a.part_o + (unit_of(sp) * a.R + r) * D + lane * V;
+    if constexpr (V == 2) {
+      const float2 v = *reinterpret_cast<const float2*>(po);
+      o[0] = v.x;
+      o[1] = v.y;
+    } else {
+      const float4 v = *reinterpret_cast<const float4*>(po);
+      o[0] = v.x;
+      o[1] = v.y;
+      o[2] = v.z;
+      o[3] = v.w;
+    }
+  };
+  if (ns <= 32) {
+    const float ls = lane < ns ? a.part_lse[unit_of(lane) * a.R + r] : neg_inf_f();
+    float M = ls;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+    const float w = (ls == neg_inf_f()) ? 0.f : exp2f(ls - M);
+    float den = w;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
+    M_out = M;
+    den_out = den;
+    if (M == neg_inf_f()) return;
+    for (int s0 = 0; s0 < ns; s0 += 4) {
+      float ov[4][V];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) load_row(s0 + t < ns ? s0 + t : ns - 1, ov[t]);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float wt = __shfl_sync(0xffffffffu, w, (s0 + t) & 31);
+        const float wv = s0 + t < ns ? wt : 0.f;
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(wv, ov[t][e], acc[e]);
+      }
+    }
+    return;
   }
-  for (int sp = lane + 32 * kW; sp < ns; sp += 32) M = fmaxf(M, a.part_lse[(unit0 + sp) * a.R + r]);
+  float M = neg_inf_f();
+  for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, a.part_lse[unit_of(sp) * a.R + r]);
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
   float den = 0.f;
-#pragma unroll
-  for (int k = 0; k < kW; ++k) {
-    wreg[k] = (wreg[k] == neg_inf_f()) ? 0.f : exp2f(wreg[k] - M);
-    den += wreg[k];
-  }
-  for (int sp = lane + 32 * kW; sp < ns; sp += 32) {
-    const float ls = a.part_lse[(unit0 + sp) * a.R + r];
+  for (int sp = lane; sp < ns; sp += 32) {
+    const float ls = a.part_lse[unit_of(sp) * a.R + r];
     den += (ls == neg_inf_f()) ? 0.f : exp2f(ls - M);
   }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
-
-  float acc[V];
+  M_out = M;
+  den_out = den;
+  if (M == neg_inf_f()) return;
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float ov[8][V];
+    float wv[8];
 #pragma unroll
-  for (int e = 0; e < V; ++e) acc[e] = 0.f;
-  if (M != neg_inf_f()) {
-    for (int s0 = 0; s0 < ns; s0 += 8) {
-      float ov[8][V];
-      float wv[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int sp = s0 + t;
-        const int spc = sp < ns ? sp : ns - 1;
-        const float* po = a.part_o + ((unit0 + spc) * a.R + r) * D + lane * V;
-        if constexpr (V == 2) {
-          const float2 v = *reinterpret_cast<const float2*>(po);
-          ov[t][0] = v.x;
-          ov[t][1] = v.y;
-        } else {
-          const float4 v = *reinterpret_cast<const float4*>(po);
-          ov[t][0] = v.x;
-          ov[t][1] = v.y;
-          ov[t][2] = v.z;
-          ov[t][3] = v.w;
-        }
-        float w;
-        if (sp < 32 * kW) {
-          float wk = 0.f;
-#pragma unroll
-          for (int k = 0; k < kW; ++k)
-            if ((sp >> 5) == k) wk = wreg[k];
-          w = __shfl_sync(0xffffffffu, wk, sp & 31);
-        } else {
-          const float ls = a.part_lse[(unit0 + spc) * a.R + r];
-          w = (ls == neg_inf_f()) ? 0.f : exp2f(ls - M);
-        }
-        wv[t] = sp < ns ? w : 0.f;
-      }
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-#pragma unroll
-        for (int e = 0; e < V; ++e) acc[e] = fmaf(wv[t], ov[t][e], acc[e]);
+    for (int t = 0; t < 8; ++t) {
+      const int sp = s0 + t < ns ? s0 + t : ns - 1;
+      load_row(sp, ov[t]);
+      const float ls = a.part_lse[unit_of(sp) * a.R + r];
+      wv[t] = (s0 + t < ns && ls != neg_inf_f()) ? exp2f(ls - M) : 0.f;
     }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = fmaf(wv[t], ov[t][e], acc[e]);
   }
+}
 
-  const float m_run = M;
-  const float l_run = den;
-
-  // 2. Write.
-  const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+template <int D>
+__device__ __forceinline__ void write_row(const AttnArgs& a, long long row_id, int lane,
+                                          const float (&acc)[D / 32], float M, float den) {
+  constexpr int V = D / 32;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
   uint16_t* dst = a.out + static_cast<size_t>(row_id) * D + lane * V;
   if constexpr (V == 2) {
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
@@ -133,16 +125,80 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) combine_kernel(const Attn
     w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
     *reinterpret_cast<uint2*>(dst) = w;
   }
-  if (lane == 0) a.lse2[row_id] = l_run > 0.f ? m_run + log2f(l_run) : neg_inf_f();
+  if (lane == 0) a.lse2[row_id] = den > 0.f ? M + log2f(den) : neg_inf_f();
+}
+
+// Row id -> (b, i, hq) for the [B, K, Hq] row order.
+__device__ __forceinline__ void row_coords(const AttnArgs& a, long long row_id, int& b, int& i,
+                                           int& hq) {
+  hq = static_cast<int>(row_id % a.Hq);
+  const long long t = row_id / a.Hq;
+  i = static_cast<int>(t % a.K);
+  b = static_cast<int>(t / a.K);
 }
 
 template <int D>
-int launch_t(const AttnArgs& a, cudaStream_t stream, bool pdl) {
+__global__ void __launch_bounds__(kThreads) combine_kernel(const AttnArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long row_id = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
+  const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
+  const bool active = row_id < rows;
+  int b = 0, i = 0, hq = 0;
+  if (active) row_coords(a, row_id, b, i, hq);
+  const int h = hq / a.G;
+  const int r = i * a.G + (hq - h * a.G);
+  const Geometry geo = make_geometry(active ? __ldg(&a.ctx_lens[b]) : 0, a.max_ctx_len, a.K, a.W,
+                                     a.T, a.C);
+  const int ns = geo.n_splits;
+  const size_t unit0 = (static_cast<size_t>(b) * a.Hkv + h) * a.S;
+
+  pdl_wait_primary();
+  if (!active) return;
+  float acc[D / 32], M, den;
+  combine_row<D>(a, r, ns, [&](int sp) -> size_t { return unit0 + sp; }, lane, acc, M, den);
+  write_row<D>(a, row_id, lane, acc, M, den);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 6) combine_flat_kernel(const AttnArgs a) {
+  __shared__ int PB[kTcMaxBatch + 1];
+  __shared__ int Lc[kTcMaxBatch];
+  __shared__ int warp_sums[kWarpsPerBlock];
+  flat_tile_prefix<kThreads>(a, PB, Lc, warp_sums, false);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long row_id = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
+  const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
+  if (row_id >= rows) return;
+  int b, i, hq;
+  row_coords(a, row_id, b, i, hq);
+  const int h = hq / a.G;
+  const int r = i * a.G + (hq - h * a.G);
+  const int qn = flat_range_tiles(a, a.Hkv * PB[a.B]);
+  const int nb = PB[b + 1] - PB[b];
+  const int g0 = a.Hkv * PB[b] + h * nb;
+  const int c0 = g0 / qn;
+  const int c1 = (g0 + nb - 1) / qn;
+  if (c0 == c1) return;  // the split kernel wrote this row
+  const int slot0 = g0 > c0 * qn ? 1 : 0;
+
+  pdl_wait_primary();
+  float acc[D / 32], M, den;
+  combine_row<D>(
+      a, r, c1 - c0 + 1,
+      [&](int sp) -> size_t { return static_cast<size_t>(c0 + sp) * 2 + (sp == 0 ? slot0 : 0); },
+      lane, acc, M, den);
+  write_row<D>(a, row_id, lane, acc, M, den);
+}
+
+template <int D>
+int launch_t(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat) {
   const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
   const unsigned grid = static_cast<unsigned>((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kWarpsPerBlock * 32, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -150,14 +206,15 @@ int launch_t(const AttnArgs& a, cudaStream_t stream, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if (flat) return cudaLaunchKernelEx(&cfg, combine_flat_kernel<D>, a);
   return cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
 }
 
 }  // namespace
 
-int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl) {
-  if (a.D == 64) return launch_t<64>(a, stream, pdl);
-  if (a.D == 128) return launch_t<128>(a, stream, pdl);
+int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat) {
+  if (a.D == 64) return launch_t<64>(a, stream, pdl, flat);
+  if (a.D == 128) return launch_t<128>(a, stream, pdl, flat);
   return cudaErrorInvalidValue;
 }
 

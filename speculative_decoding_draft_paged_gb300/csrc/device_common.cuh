@@ -89,6 +89,28 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Pull the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
+// Pull a box of a 3-D tensor map into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -182,6 +204,66 @@ __device__ __forceinline__ size_t out_row_index(const AttnArgs& a, int b, int h,
   const int i = r / a.G;
   const int g = r - i * a.G;
   return (static_cast<size_t>(b) * a.K + i) * a.Hq + static_cast<size_t>(h) * a.G + g;
+}
+
+// ---- flat split of the tcgen05 kernel (shared with the combine kernel, so
+// both derive the same CTA ranges from the lengths).
+constexpr int kFlatTileKeys = 64;
+
+// PB[b] = sum over requests b' < b of their 64-key tile counts, b in [0, B];
+// Lc[b] = context length clamped to [0, max_ctx_len].  Called by all NT
+// threads of the block (NT a multiple of 32, at most 1024); warp_sums is
+// shared scratch of NT/32 ints.  Ends with __syncthreads.
+template <int NT>
+__device__ __forceinline__ void flat_tile_prefix(const AttnArgs& a, int* PB, int* Lc, int* warp_sums,
+                                                 bool flag_bad) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ipt = (a.B + NT - 1) / NT;
+  const int b_lo = threadIdx.x * ipt;
+  const int b_hi = min(b_lo + ipt, a.B);
+  int sum = 0;
+  for (int bb = b_lo; bb < b_hi; ++bb) {
+    const int L_raw = __ldg(&a.ctx_lens[bb]);
+    if (flag_bad && (L_raw < 0 || L_raw > a.max_ctx_len)) flag_status(a.status, DFLASH_STATUS_BAD_CTX_LEN);
+    const Geometry g = make_geometry(L_raw, a.max_ctx_len, a.K, a.W, kFlatTileKeys, 1);
+    Lc[bb] = g.L;
+    sum += g.n_tiles;
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int ws = lane < NT / 32 ? warp_sums[lane] : 0;
+    int wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < NT / 32) warp_sums[lane] = wi - ws;  // exclusive over warps
+  }
+  __syncthreads();
+  int run = warp_sums[warp] + incl - sum;
+  for (int bb = b_lo; bb < b_hi; ++bb) {
+    PB[bb] = run;
+    run += make_geometry(Lc[bb], a.max_ctx_len, a.K, a.W, kFlatTileKeys, 1).n_tiles;
+  }
+  if (b_lo < b_hi && b_hi == a.B) PB[a.B] = run;
+  __syncthreads();
+}
+
+// Tiles per CTA range: forced, or an equal share of `total` over the grid
+// (at least qn_min).
+__device__ __forceinline__ int flat_range_tiles(const AttnArgs& a, int total) {
+  if (a.qn_force > 0) return a.qn_force;
+  const int q = (total + a.ncta - 1) / a.ncta;
+  return q < a.qn_min ? a.qn_min : q;
 }
 
 // Programmatic dependent launch controls.

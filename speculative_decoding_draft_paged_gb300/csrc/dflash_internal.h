@@ -24,6 +24,8 @@ constexpr int kMaxBlock = 16;          // draft block size K
 constexpr int kStages = 4;             // TMA pipeline depth of the split kernels
 constexpr int kMaxSplitTiles = 64;     // key tiles per split unit, at most
 constexpr int kMaxUnitSlots = 512;     // page-table slots one unit can touch (64 tiles x 8 pages)
+constexpr int kTcMaxBatch = 768;       // tcgen05 kernel: requests whose tile prefix fits shared memory
+constexpr int kTcMinTiles = 4;         // tcgen05 kernel: fewest tiles one CTA's range takes
 
 // Everything a kernel needs, by value (kernel parameter).
 struct AttnArgs {
@@ -44,6 +46,12 @@ struct AttnArgs {
   int T;                      // keys per tile (pipeline stage)
   int C;                      // tiles per split unit
   int S;                      // split units per (request, kv head)
+  // Flat split (tcgen05 kernel): the key tiles of all (request, kv head)
+  // pairs laid end to end and cut into one contiguous range per CTA;
+  // part_o/part_lse hold two slots per CTA.
+  int ncta;                   // CTAs of the tcgen05 split kernel
+  int qn_force;               // tiles per CTA range if > 0, else from the lengths
+  int qn_min;                 // fewest tiles per CTA range (lengths-derived case)
 };
 
 // Per-(request, kv head) key-range geometry of the split kernel, which covers
@@ -86,8 +94,10 @@ DF_HD int max_tiles(int max_ctx_len, int K, int W, int T) {
 // Host-side launch plan.
 struct KernelPlan {
   int path;         // DFLASH_PATH_MMA / DFLASH_PATH_TCGEN05
-  int R, R_pad, T, C, S;
-  int64_t units;
+  int R, R_pad, T;
+  int C;            // mma: tiles per unit; tcgen05: tiles per CTA range at full lengths
+  int S;            // mma: units per (request, kv head); tcgen05: partial slots per CTA (2)
+  int64_t units;    // mma: split units; tcgen05: CTAs
   int threads, smem_bytes;
   int kpw;          // mma path: keys per warp per tile
   int num_sms;
@@ -97,8 +107,8 @@ struct KernelPlan {
 int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
                      const CUtensorMap& tm_v, cudaStream_t stream);
 int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
-                    const CUtensorMap& tm_v, cudaStream_t stream);
-int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl);
+                    const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream);
+int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat);
 
 // Shared-memory bytes of each split kernel for a plan (used by the planner).
 int split_mma_smem_bytes(int D, int R_pad, int kpw);

@@ -2,37 +2,46 @@
 // (R = G*K <= 128 rows in one M = 128 tile: the MiniMax-style 16/1-head and
 // the attention-DP 64/4-head drafter ranks at block size 7).
 //
-// One CTA = one split unit (request b, kv head h, split s) over T = 64-key
-// tiles of the keys the block's rows see (row i: [lo_i, L+K) non-causal, the
-// later block keys merged in the tile that holds them, or [lo_i, L+i+1)
-// causal; TensorRT-LLM PR #21130), like the mma.sync kernel; the packed
-// query tile (row r = i*G + g, PR #16150: query rows of
-// one kv head packed so the KV is read once) is the A operand of QK^T.
+// Persistent flat split.  The key tiles of every (request, kv head) pair are
+// laid end to end, pairs in b-major order, each pair's T = 64-key tiles
+// covering the keys its block's rows see: row i sees [lo_i, L+K) in the
+// non-causal form -- the block keys after i merged in the tile that holds
+// them (TensorRT-LLM PR #21130, "Why" and change 1) -- or [lo_i, L+i+1) in
+// the causal form (change 2).  One CTA per SM takes an equal contiguous range
+// of that sequence, so every SM streams the same number of tiles whatever the
+// lengths.  A range covers a few segments, one per pair: a pair that lies
+// inside the range gets its final output written directly; the first and the
+// last segment of a range may hold part of a pair only and write a partial
+// state (normalised O, base-2 LSE) that the combine kernel merges.  The
+// packed query tile of a pair (row r = i*G + g of one kv head, PR #16150: the
+// query rows of one kv head packed so its KV is read once) is the A operand
+// of QK^T.
 //
-// Warp roles (352 threads):
-//   warp 0, lane 0   K producer, warp 10 lane 0 V producer: page ids come from
-//                    shared memory (looked up by the whole CTA up front); one
-//                    128-byte-swizzled TMA box per (page, 64-column half) into
-//                    separate K and V rings.  A K slot is released as soon as
-//                    its QK^T has completed and a V slot after its PV, so the
-//                    V loads run just ahead of their use and the K loads far
-//                    ahead, with the same shared memory as one joint ring;
+// Warp roles (384 threads):
+//   warp 0 / warp 10 K / V producer: the warp keeps the page ids of the next
+//                    32 page-table slots in registers (one chunk ahead); lane
+//                    0 issues one 128-byte-swizzled TMA box per (page,
+//                    64-column half) into separate K and V rings.  A K slot is
+//                    released when its QK^T has completed, a V slot after its
+//                    PV;
+//   warp 11 lane 0   query loader: the packed query tile of each segment's
+//                    pair as TMA boxes of (64 columns, G heads, K tokens), once
+//                    the previous segment's last QK^T is done; the next
+//                    segment's tile is prefetched into L2 meanwhile;
 //   warp 1           allocates 512 TMEM columns; lane 0 issues the MMAs:
 //                    S_j = Q K_j^T (M=128, N=64, K=D) into TMEM S buffer j%2,
 //                    then O_{j%2} += P_j V_j (M=128, N=D, K=64);
 //   warps 2..9       softmax, two groups of four warps: group g takes the
-//                    tiles j = g, g+2, g+4, ... with its own running state
-//                    and its own accumulator O_g in TMEM, so two independent
-//                    chains share every SM sub-partition.  A thread owns one
-//                    query row (= TMEM lane of its warp's quadrant): it reads
-//                    its row of S_j, masks by select, keeps a base-2 reference
-//                    max that moves only when a tile's max exceeds it by more
-//                    than 8 (then O_g and the row sum are rescaled, exactly),
-//                    and writes P_j = 2^(s - m) in bf16 to its group's shared
-//                    P buffer, the A operand of the PV MMA.  At the end group 0
-//                    merges both groups' (O, m, l), like two splits, and
-//                    writes the unit's normalised partial -- or, with one unit
-//                    per (request, kv head), the final bf16 output and LSE.
+//                    range's tiles j = g, g+2, ... with its own running state
+//                    and TMEM accumulator O_g.  A thread owns one query row
+//                    (= TMEM lane of its warp's quadrant): it reads its row of
+//                    S_j, masks by select, keeps a base-2 reference max that
+//                    moves only when a tile's max exceeds it by more than 8
+//                    (then O_g and the row sum are rescaled, exactly), and
+//                    writes P_j = 2^(s - m) in bf16 to its group's shared P
+//                    buffer, the A operand of the PV MMA.  At the end of each
+//                    segment both groups merge the two states, each for half
+//                    of the output columns, and write them.
 // Every mbarrier wait is bounded (DFLASH_STATUS_TIMEOUT, then drain).
 
 #include <cuda_runtime.h>
@@ -57,45 +66,189 @@ struct TcCfg {
   static constexpr int kOffP = kOffV + NSV * kTileBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
   // k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
-  // s_free[2], p_full[2], pv_done[2], merge
-  static constexpr int kNumBars = 2 * NSK + 2 * NSV + 9;
+  // s_free[2], p_full[2], pv_done[2], q_full, q_free
+  static constexpr int kNumBars = 2 * NSK + 2 * NSV + 10;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffXchg = kOffMisc + 64;            // group 1's (m, l) per row
-  static constexpr int kOffPages = kOffXchg + 128 * 8;
-  static constexpr int kSmem = kOffPages + 4 * kMaxUnitSlots + 1024;
+  static constexpr int kOffXchg = kOffMisc + 64;                 // both groups' (m, l) per row
+  static constexpr int kOffPB = kOffXchg + 2 * 128 * 8;          // tile prefix per request
+  static constexpr int kOffLc = kOffPB + 4 * (kTcMaxBatch + 1);  // clamped context lengths
+  static constexpr int kSmem = kOffLc + 4 * kTcMaxBatch + 1024;
   static constexpr int kTmemCols = 512;   // S0 [0,64) S1 [64,128) O0 [128,128+D) O1 [256,256+D)
   static constexpr int kColO0 = 128;
   static constexpr int kColO1 = 256;
-  static constexpr int kThreads = 352;
+  static constexpr int kThreads = 384;
 };
+
+constexpr int kNoPage = -0x7fffffff - 1;  // page-table slot outside the keys a pair reads
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 
+// One segment of a CTA's range: the part of pair (b, h) inside it.
+struct Seg {
+  int b, h;
+  int g0;      // global index of the pair's first tile
+  int nb;      // tiles of the pair
+  int j0, j1;  // CTA-local tiles [j0, j1) of the segment
+  int idx;     // segment number within the CTA
+};
+
+// Request whose pairs hold global tile gt: the last b with Hkv * PB[b] <= gt.
+__device__ __forceinline__ int request_of_tile(const int* PB, int B, int Hkv, int gt) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (Hkv * PB[mid] <= gt) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ Seg seg_first(const int* PB, int B, int Hkv, int start, int end) {
+  Seg s;
+  s.b = request_of_tile(PB, B, Hkv, start);
+  s.nb = PB[s.b + 1] - PB[s.b];
+  s.h = (start - Hkv * PB[s.b]) / s.nb;
+  s.g0 = Hkv * PB[s.b] + s.h * s.nb;
+  s.j0 = 0;
+  s.j1 = min(s.g0 + s.nb, end) - start;
+  s.idx = 0;
+  return s;
+}
+
+__device__ __forceinline__ void seg_next(Seg& s, const int* PB, int Hkv, int start, int end) {
+  if (s.h + 1 < Hkv) {
+    ++s.h;
+  } else {
+    ++s.b;
+    s.h = 0;
+  }
+  s.nb = PB[s.b + 1] - PB[s.b];
+  s.g0 = Hkv * PB[s.b] + s.h * s.nb;
+  s.j0 = s.j1;
+  s.j1 = min(s.g0 + s.nb, end) - start;
+  ++s.idx;
+}
+
+// Raw page-table entry for one lane of page-id chunk k of a CTA's range: the
+// chunk covers CTA-local tiles [k*tpc, (k+1)*tpc), tpc = 32 / ppt; lane l
+// takes page l % ppt of tile k*tpc + l / ppt.  kNoPage where the tile is past
+// the range or the slot lies outside the keys the pair reads.
+__device__ __forceinline__ int chunk_page(const AttnArgs& a, const int* PB, const int* Lc, int start,
+                                          int end, int k, int lane, int ppt) {
+  const int tpc = 32 / ppt;
+  const int lt = lane / ppt;
+  const int gt = start + k * tpc + lt;
+  if (gt >= end) return kNoPage;
+  const int b = request_of_tile(PB, a.B, a.Hkv, gt);
+  const int nb = PB[b + 1] - PB[b];
+  const int within = gt - a.Hkv * PB[b];
+  const int t = within - (within / nb) * nb;
+  const Geometry geo = make_geometry(Lc[b], a.max_ctx_len, a.K, a.W, 64, 1);
+  const int slot = (geo.t_begin + t) * ppt + (lane - lt * ppt);
+  if (slot < geo.lo_min / a.P || slot >= (geo.hi_max + a.P - 1) / a.P) return kNoPage;
+  return __ldg(&a.page_table[static_cast<size_t>(b) * a.max_pages + slot]);
+}
+
+// End-of-segment output of one softmax warp: its 32 rows (TMEM lanes of
+// its quadrant) x its group's half of the columns, w0 * O0 + w1 * O1 scaled
+// by inv, written as bf16 rows of the output (direct) or fp32 rows of the
+// CTA's partial slot `unit`.  The rows go through the warp's own 4 KB of the
+// idle P buffers, transposed so that a store instruction covers whole row
+// pieces instead of one 16-byte piece per row.  Row pieces in the slot:
+// bf16, 64 bytes = 4 chunks of 16 stored at c ^ ((lane >> 1) & 3); fp32,
+// 128 bytes = 8 chunks stored at c ^ (lane & 7) (conflict-free both ways).
+// Kept out of line: it runs once per segment, and inlined it would crowd
+// the tile loop's registers.
 template <int D>
-__global__ void __launch_bounds__(352, 1)
+__device__ __noinline__ void store_segment_rows(const AttnArgs& a, uint8_t* stg, uint32_t lane_addr,
+                                                int grp, int quad, int lane, float w0, float w1,
+                                                float inv, bool direct, int b, int h, size_t unit) {
+  constexpr int kColO0 = 128, kColO1 = 256;
+#pragma unroll 1
+  for (int cc = 0; cc < D / 64; ++cc) {
+    const int col = grp * (D / 2) + cc * 32;
+    __syncwarp();  // the previous chunk's reads of the staging slot are done
+    uint32_t o0[32], o1[32];
+    tmem_ld32x2_wait(lane_addr + kColO0 + col, lane_addr + kColO1 + col, o0, o1);
+    // A group that saw no key of this segment holds a stale or
+    // uninitialised accumulator: select, so it cannot leak in.
+    auto val = [&](int e) {
+      const float a0 = w0 > 0.f ? w0 * __uint_as_float(o0[e]) : 0.f;
+      const float a1 = w1 > 0.f ? w1 * __uint_as_float(o1[e]) : 0.f;
+      return (a0 + a1) * inv;
+    };
+    if (direct) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(pack_bf16x2(val(8 * c), val(8 * c + 1)), pack_bf16x2(val(8 * c + 2), val(8 * c + 3)),
+                       pack_bf16x2(val(8 * c + 4), val(8 * c + 5)), pack_bf16x2(val(8 * c + 6), val(8 * c + 7)));
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int rl = it * 8 + (lane >> 2);
+        const int c = lane & 3;
+        const uint4 x = *reinterpret_cast<const uint4*>(stg + rl * 64 + ((c ^ ((rl >> 1) & 3)) << 4));
+        const int ro = quad * 32 + rl;
+        if (ro < a.R) *reinterpret_cast<uint4*>(a.out + out_row_index(a, b, h, ro) * D + col + c * 8) = x;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+            make_float4(val(4 * c), val(4 * c + 1), val(4 * c + 2), val(4 * c + 3));
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int rl = it * 4 + (lane >> 3);
+        const int c = lane & 7;
+        const float4 x = *reinterpret_cast<const float4*>(stg + rl * 128 + ((c ^ (rl & 7)) << 4));
+        const int ro = quad * 32 + rl;
+        if (ro < a.R) *reinterpret_cast<float4*>(a.part_o + (unit * a.R + ro) * D + col + c * 4) = x;
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
     split_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_q) {
   using C = TcCfg<D>;
   constexpr int T = C::T;
   constexpr int NSK = C::NSK;
   constexpr int NSV = C::NSV;
 
-  const int s = blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int L_raw = __ldg(&a.ctx_lens[b]);
-  const Geometry geo = make_geometry(L_raw, a.max_ctx_len, a.K, a.W, T, a.C);
-  if (threadIdx.x == 0 && s == 0 && h == 0 && (L_raw < 0 || L_raw > a.max_ctx_len))
-    flag_status(a.status, DFLASH_STATUS_BAD_CTX_LEN);
-  if (s >= geo.n_splits) return;  // empty unit, uniform over the CTA
-  const int tile0 = geo.t_begin + s * a.C;
-  int n = geo.n_tiles - s * a.C;
-  if (n > a.C) n = a.C;
-
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int warp_sums[C::kThreads / 32];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_u32);
+  int* PB = reinterpret_cast<int*>(gbase + C::kOffPB);
+  int* Lc = reinterpret_cast<int*>(gbase + C::kOffLc);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // The page-table rows are needed right after the prefix: every CTA pulls
+  // its share of the table into L2 while the lengths are being read.
+  {
+    const size_t lines = (static_cast<size_t>(a.B) * a.max_pages * 4 + 127) / 128;
+    const size_t per = (lines + gridDim.x - 1) / gridDim.x;
+    const size_t l0 = static_cast<size_t>(blockIdx.x) * per;
+    const size_t l1 = l0 + per < lines ? l0 + per : lines;
+    for (size_t l = l0 + threadIdx.x; l < l1; l += C::kThreads)
+      prefetch_l2(reinterpret_cast<const uint8_t*>(a.page_table) + l * 128);
+  }
+  // Tile prefix over the requests, computed by every CTA.
+  flat_tile_prefix<C::kThreads>(a, PB, Lc, warp_sums, blockIdx.x == 0);
+  const int total = a.Hkv * PB[a.B];
+  const int qn = flat_range_tiles(a, total);
+  const long long start_ll = static_cast<long long>(blockIdx.x) * qn;
+  if (start_ll >= total) return;  // no tiles for this CTA (uniform)
+  const int start = static_cast<int>(start_ll);
+  const int end = min(start + qn, total);
+  const int n = end - start;
+
   const uint32_t sQ = base + C::kOffQ;
   const uint32_t sK = base + C::kOffK;
   const uint32_t sV = base + C::kOffV;
@@ -110,17 +263,16 @@ __global__ void __launch_bounds__(352, 1)
   auto s_free = [&](int g) { return bars + 8u * (kB0 + 2 + g); };
   auto p_full = [&](int g) { return bars + 8u * (kB0 + 4 + g); };
   auto pv_done = [&](int g) { return bars + 8u * (kB0 + 6 + g); };
-  const uint32_t merge_bar = bars + 8u * (kB0 + 8);
+  const uint32_t q_full = bars + 8u * (kB0 + 8);
+  const uint32_t q_free = bars + 8u * (kB0 + 9);
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile uint32_t* tmem_slot = misc;          // TMEM base address from tcgen05.alloc
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile int* issued_k = reinterpret_cast<volatile int*>(misc + 2);
   volatile int* issued_v = reinterpret_cast<volatile int*>(misc + 3);
+  volatile int* issued_q = reinterpret_cast<volatile int*>(misc + 4);
+  volatile int* stop_word = reinterpret_cast<volatile int*>(misc + 5);  // softmax warps only
   float2* xchg = reinterpret_cast<float2*>(gbase + C::kOffXchg);
-  int* pg_smem = reinterpret_cast<int*>(gbase + C::kOffPages);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < NSK; ++st) {
@@ -137,82 +289,120 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(p_full(g), 4);
       mbar_init(pv_done(g), 1);
     }
-    mbar_init(merge_bar, 4);
+    mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
     *abort_flag = 0;
     *issued_k = 0;
     *issued_v = 0;
+    *issued_q = 0;
+    *stop_word = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_q);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), C::kTmemCols);
     tmem_relinquish();
   }
+  // Query rows R..127 stay zero (the TMA boxes cover rows 0..R-1 only), so
+  // their scores are zero and never disturb a warp's rescale decision.
+  {
+    constexpr int CPR = D / 8;
+    for (int idx = threadIdx.x; idx < (128 - a.R) * CPR; idx += C::kThreads) {
+      const int row = a.R + idx / CPR;
+      const int c = idx % CPR;
+      *reinterpret_cast<uint4*>(gbase + C::kOffQ + swz_offset(row, c, 128)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();  // barrier initialisation and the TMEM address are visible
   tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   // Every CTA of this grid is resident once the last one gets here: the
   // combine kernel may launch and start on its input-only work.
   pdl_launch_dependents();
 
-  const int pages_per_tile = T / a.P;
-  uint32_t tmem = 0;
   if (warp == 0 || warp == 10) {
-    // The producers start as soon as warp 0 has looked the unit's page ids
-    // up; they do not wait for the query tile.
-    if (warp == 0)
-      load_unit_pages(a, b, tile0 * pages_per_tile, n * pages_per_tile, geo.lo_min / a.P,
-                      (geo.hi_max + a.P - 1) / a.P, pg_smem, lane, 32);
-    named_barrier(2, 64);
-  } else {
-    // Warps 1..9: packed query tile, K-major with the 128-byte swizzle the
-    // MMA descriptor expects: rows r = i*G + g of kv head h; rows >= R zero.
-    constexpr int CPR = D / 8;
-    for (int idx = threadIdx.x - 32; idx < 128 * CPR; idx += 288) {
-      const int row = idx / CPR;
-      const int c = idx - row * CPR;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (row < a.R) {
-        const int i = row / a.G;
-        const int g = row - i * a.G;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + ((static_cast<size_t>(b) * a.K + i) * a.Hq + static_cast<size_t>(h) * a.G + g) * D);
-        v = __ldg(src + c);
+    // ------------------------------------------------------------ producers (whole warp)
+    const bool is_v = warp == 10;
+    const int ns = is_v ? NSV : NSK;
+    const uint32_t ring = is_v ? sV : sK;
+    const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+    volatile int* issued = is_v ? issued_v : issued_k;
+    const int ppt = T / a.P;  // pages per tile: 1, 2 or 4
+    const int tpc = 32 / ppt;  // tiles per page-id chunk
+    auto checked = [&](int raw) {
+      if (raw == kNoPage) return -1;  // zero fill
+      if (raw < 0 || raw >= a.num_pages) {
+        flag_status(a.status, DFLASH_STATUS_BAD_PAGE);
+        return -1;
       }
-      *reinterpret_cast<uint4*>(gbase + C::kOffQ + swz_offset(row, c, 128)) = v;
+      return raw;
+    };
+    int pg_cur = checked(chunk_page(a, PB, Lc, start, end, 0, lane, ppt));
+    int pg_nxt = chunk_page(a, PB, Lc, start, end, 1, lane, ppt);
+    int cur_k = 0;
+    Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
+    for (int j = 0; j < n; ++j) {
+      while (j >= sg.j1) seg_next(sg, PB, a.Hkv, start, end);
+      const int k = j / tpc;
+      if (k != cur_k) {
+        // The next chunk's table loads were issued a chunk ago.
+        pg_cur = checked(pg_nxt);
+        pg_nxt = chunk_page(a, PB, Lc, start, end, k + 1, lane, ppt);
+        cur_k = k;
+      }
+      const int lane0 = (j - k * tpc) * ppt;
+      int pages[4];
+#pragma unroll
+      for (int pj = 0; pj < 4; ++pj)
+        pages[pj] = __shfl_sync(0xffffffffu, pg_cur, lane0 + (pj < ppt ? pj : 0));
+      const int st = j % ns;
+      const uint32_t empty = is_v ? v_empty(st) : k_empty(st);
+      const uint32_t full = is_v ? v_full(st) : k_full(st);
+      if (j >= ns && !mbar_wait_warp(empty, ((j / ns) - 1) & 1)) {
+        if (lane == 0) flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        const uint32_t dst = ring + st * C::kTileBytes;
+#pragma unroll
+        for (int pj = 0; pj < 4; ++pj) {
+          if (pj >= ppt) break;
+#pragma unroll
+          for (int x = 0; x < D / 64; ++x)
+            tma_load_4d(dst + x * T * 128 + pj * a.P * 128, map, x * 64, 0, sg.h, pages[pj], full);
+        }
+        *issued = j + 1;
+      }
+      __syncwarp();
     }
-    fence_proxy_async_smem();
-    named_barrier(1, 288);
-    tmem = *tmem_slot;
-  }
-
-  if (warp == 0 || warp == 10) {
-    // ------------------------------------------------------------ producers
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ query loader
     if (lane == 0) {
-      const bool is_v = warp == 10;
-      const int ns = is_v ? NSV : NSK;
-      const uint32_t ring = is_v ? sV : sK;
-      const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-      volatile int* issued = is_v ? issued_v : issued_k;
-      for (int j = 0; j < n; ++j) {
-        const int st = j % ns;
-        const uint32_t empty = is_v ? v_empty(st) : k_empty(st);
-        const uint32_t full = is_v ? v_full(st) : k_full(st);
-        if (j >= ns && !mbar_wait(empty, ((j / ns) - 1) & 1)) {
+      Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
+      for (;;) {
+        if (sg.idx > 0 && !mbar_wait(q_free, (sg.idx - 1) & 1)) {
           flag_status(a.status, DFLASH_STATUS_TIMEOUT);
           *abort_flag = 1;
         }
         if (*abort_flag) break;
-        mbar_arrive_expect_tx(full, C::kTileBytes);
-        const uint32_t dst = ring + st * C::kTileBytes;
-        for (int pj = 0; pj < pages_per_tile; ++pj) {
-          const int page = pg_smem[j * pages_per_tile + pj];
+        // Box (64 columns, G heads, K tokens) lands as rows r = i*G + g with
+        // the 128-byte swizzle, one box per 64-column half.
+        mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(a.R * D * 2));
 #pragma unroll
-          for (int x = 0; x < D / 64; ++x)
-            tma_load_4d(dst + x * T * 128 + pj * a.P * 128, map, x * 64, 0, h, page, full);
-        }
-        *issued = j + 1;
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_3d(sQ + x * 128 * 128, &tm_q, x * 64, sg.h * a.G, sg.b * a.K, q_full);
+        *issued_q = sg.idx + 1;
+        if (sg.j1 >= n) break;
+        seg_next(sg, PB, a.Hkv, start, end);
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x) tma_prefetch_3d(&tm_q, x * 64, sg.h * a.G, sg.b * a.K);
       }
     }
   } else if (warp == 1) {
@@ -226,54 +416,80 @@ __global__ void __launch_bounds__(352, 1)
       const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
       const uint64_t dp = smem_desc_sw128(sP, 16, 1024);
       const uint64_t dv = smem_desc_sw128(sV, T * 128, 1024);
+      Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
+      int q_seg = -1;            // segment whose query tile has been waited for
+      int seg_prev = 0;          // segment of tile j-1
+      int pv_seg[2] = {-1, -1};  // segment of each group's latest PV
       int last_qk = -1, last_pv = -1;
+      // S_j = Q K_j^T into TMEM S buffer j%2.
+      auto issue_qk = [&](int j, int seg_j) -> bool {
+        const int st = j % NSK;
+        if (q_seg != seg_j) {
+          if (!mbar_wait(q_full, seg_j & 1)) return false;
+          q_seg = seg_j;
+        }
+        if (!mbar_wait(k_full(st), (j / NSK) & 1)) return false;
+        if (j >= 2 && !mbar_wait(s_free(j & 1), ((j >> 1) - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (j & 1) * T;
+        const uint32_t k_off = st * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t x = kk >> 2;
+          const uint32_t within = (kk & 3) * 32;
+          umma_bf16(d_tmem, dq + ((x * (128 * 128) + within) >> 4),
+                    dk + ((k_off + x * (T * 128) + within) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(k_empty(st));
+        umma_commit(s_full(j & 1));
+        // The query tile may be replaced once the segment's last QK^T is done.
+        if (j == sg.j1 - 1 && sg.j1 < n) umma_commit(q_free);
+        last_qk = j;
+        return true;
+      };
+      // O_g += P_j V_j, g = j%2, for tile jj of segment seg_prev.  The first
+      // PV of a group in a segment overwrites O_g: its P arrives only after
+      // every softmax thread has read the previous segment's accumulators.
+      auto issue_pv = [&](int jj) -> bool {
+        const int st = jj % NSV;
+        const int g = jj & 1;
+        const bool fresh = pv_seg[g] != seg_prev;
+        if (!mbar_wait(p_full(g), (jj >> 1) & 1)) return false;
+        if (!mbar_wait(v_full(st), (jj / NSV) & 1)) return false;
+        tc_fence_after();
+        pv_seg[g] = seg_prev;
+        const uint32_t v_off = st * C::kTileBytes;
+        const uint32_t o_col = g ? C::kColO1 : C::kColO0;
+#pragma unroll
+        for (int kk = 0; kk < T / 16; ++kk)
+          umma_bf16(tmem + o_col, dp + ((g * C::kPBytes + kk * 32) >> 4),
+                    dv + ((v_off + kk * 16 * 128) >> 4), idesc_pv, (!fresh || kk > 0) ? 1u : 0u);
+        umma_commit(v_empty(st));
+        umma_commit(pv_done(g));
+        last_pv = jj;
+        return true;
+      };
       for (int j = 0; j <= n; ++j) {
         if (*abort_flag) break;
+        int seg_j = seg_prev;
         if (j < n) {
-          const int st = j % NSK;
-          bool ok = mbar_wait(k_full(st), (j / NSK) & 1);
-          if (ok && j >= 2) ok = mbar_wait(s_free(j & 1), ((j >> 1) - 1) & 1);
-          if (!ok) {
-            flag_status(a.status, DFLASH_STATUS_TIMEOUT);
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem + (j & 1) * T;
-          const uint32_t k_off = st * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t x = kk >> 2;
-            const uint32_t within = (kk & 3) * 32;
-            umma_bf16(d_tmem, dq + ((x * (128 * 128) + within) >> 4),
-                      dk + ((k_off + x * (T * 128) + within) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(k_empty(st));
-          umma_commit(s_full(j & 1));
-          last_qk = j;
+          while (j >= sg.j1) seg_next(sg, PB, a.Hkv, start, end);
+          seg_j = sg.idx;
         }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int st = jj % NSV;
-          const int g = jj & 1;
-          bool ok = mbar_wait(p_full(g), (jj >> 1) & 1);
-          if (ok) ok = mbar_wait(v_full(st), (jj / NSV) & 1);
-          if (!ok) {
-            flag_status(a.status, DFLASH_STATUS_TIMEOUT);
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t v_off = st * C::kTileBytes;
-          const uint32_t o_col = g ? C::kColO1 : C::kColO0;
-#pragma unroll
-          for (int kk = 0; kk < T / 16; ++kk)
-            umma_bf16(tmem + o_col, dp + ((g * C::kPBytes + kk * 32) >> 4),
-                      dv + ((v_off + kk * 16 * 128) >> 4), idesc_pv, (jj >= 2 || kk > 0) ? 1u : 0u);
-          umma_commit(v_empty(st));
-          umma_commit(pv_done(g));
-          last_pv = jj;
+        // QK^T runs one tile ahead of PV, except across a segment boundary:
+        // there the previous segment's last PV goes first, so that segment's
+        // output does not wait for the next query tile.
+        const bool boundary = j < n && j > 0 && seg_j != seg_prev;
+        bool ok = true;
+        if (boundary) ok = issue_pv(j - 1);
+        if (ok && j < n) ok = issue_qk(j, seg_j);
+        if (ok && !boundary && j >= 1) ok = issue_pv(j - 1);
+        if (!ok) {
+          flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+          *abort_flag = 1;
+          break;
         }
+        seg_prev = seg_j;
       }
       // Let the last commits land before the CTA winds down.
       for (int jj = last_qk - NSK + 1; jj <= last_qk; ++jj)
@@ -290,188 +506,163 @@ __global__ void __launch_bounds__(352, 1)
     const int gthread = (sw & 3) * 32 + lane;  // 0..127 within the group
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t o_col = grp ? C::kColO1 : C::kColO0;
-    const int L = geo.L;
-    int lo_r = 0x7fffffff, hi_r = -0x7fffffff;
-    if (row < a.R) {
-      const int i = row / a.G;
-      lo_r = 0;
-      if (a.W > 0) {
-        lo_r = L + i - a.W + 1;
-        if (lo_r < 0) lo_r = 0;
-      }
-      hi_r = a.future_keys ? L + a.K : L + i + 1;
-    }
-    int lo_rows_max = 0;
-    if (a.W > 0) {
-      lo_rows_max = L + a.K - a.W;
-      if (lo_rows_max < 0) lo_rows_max = 0;
-    }
-    const int hi_rows_min = a.future_keys ? L + a.K : L + 1;
-
-    float m_ref = ninf();
-    float l_run = 0.f;
+    const int i_row = row < a.R ? row / a.G : 0;
     bool ok = true;
-    for (int j = grp; j < n; j += 2) {
-      if (!mbar_wait_warp(s_full(grp), (j >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld64_wait(lane_addr + grp * T, sr);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(grp));
-
-      const int p0 = (tile0 + j) * T;
-      const bool need_mask = (p0 < lo_rows_max) || (p0 + T > hi_rows_min);
-      // Row max of the raw scores (the scale is positive), four independent
-      // chains; masked keys become -inf by select.  Boundary tiles only.
-      float mx[4] = {ninf(), ninf(), ninf(), ninf()};
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int pos = p0 + c;
-          const float v = (pos >= lo_r && pos < hi_r) ? __uint_as_float(sr[c]) : ninf();
-          sr[c] = __float_as_uint(v);
-          mx[c & 3] = fmaxf(mx[c & 3], v);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c]));
-      }
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
-      // The reference max moves only when this tile's max passes it by more
-      // than 8 (p stays <= 2^8); O_g and l are rescaled then, which is exact.
-      const bool resc = mt > m_ref + 8.f;
-      float corr = 1.f;
-      if (resc) {
-        corr = (m_ref == ninf()) ? 0.f : fast_exp2(m_ref - mt);
-        l_run *= corr;
-        m_ref = mt;
-      }
-      const float neg_m = (m_ref == ninf()) ? 0.f : -m_ref;
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float pa = fast_exp2(fmaf(__uint_as_float(sr[2 * c]), a.scale_log2, neg_m));
-        const float pb = fast_exp2(fmaf(__uint_as_float(sr[2 * c + 1]), a.scale_log2, neg_m));
-        sm[c & 3] += pa + pb;
-        pk[c] = pack_bf16x2(pa, pb);
-      }
-      l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
-
-      // This group's P buffer and O_g are free once its previous PV (tile
-      // j-2) has completed.  The TMEM load/store of the rescale are
-      // warp-collective: the whole warp runs them when any of its rows moved
-      // its reference max (factor 1 for the other rows).
-      const bool warp_resc = __any_sync(0xffffffffu, resc);
-      if (j >= 2) {
-        if (!mbar_wait_warp(pv_done(grp), ((j >> 1) - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        if (warp_resc) {
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32_wait(lane_addr + o_col + cc * 32, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-            tmem_st32(lane_addr + o_col + cc * 32, o);
-          }
-          tmem_wait_st();
-        }
-      }
-      // Value rows outside [lo_min, L+K) may hold anything: zero them in the
-      // stage before the PV MMA reads it (boundary tiles only).
-      if (p0 < geo.lo_min || p0 + T > geo.hi_max) {
-        const int st = j % NSV;
-        if (!mbar_wait_warp(v_full(st), (j / NSV) & 1)) { ok = false; break; }
-        if (gthread < T) {
-          const int pos = p0 + gthread;
-          if (pos < geo.lo_min || pos >= geo.hi_max) {
-            uint8_t* vrow = gbase + C::kOffV + st * C::kTileBytes + gthread * 128;
-#pragma unroll
-            for (int x2 = 0; x2 < D / 64; ++x2)
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(vrow + x2 * T * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-      }
-      // P row -> this group's shared buffer, K-major, 128-byte swizzle.
+    Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
+    for (;;) {
+      const Geometry geo = make_geometry(Lc[sg.b], a.max_ctx_len, a.K, a.W, T, 1);
+      const int L = geo.L;
+      int lo_r = 0x7fffffff, hi_r = -0x7fffffff;
       if (row < a.R) {
-        uint8_t* prow = gbase + C::kOffP + grp * C::kPBytes + row * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        lo_r = 0;
+        if (a.W > 0) {
+          lo_r = L + i_row - a.W + 1;
+          if (lo_r < 0) lo_r = 0;
+        }
+        hi_r = a.future_keys ? L + a.K : L + i_row + 1;
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(grp));
-    }
+      int lo_rows_max = 0;
+      if (a.W > 0) {
+        lo_rows_max = L + a.K - a.W;
+        if (lo_rows_max < 0) lo_rows_max = 0;
+      }
+      const int hi_rows_min = a.future_keys ? L + a.K : L + 1;
+      const int pos_base = (geo.t_begin - (sg.g0 - start)) * T;  // position of CTA tile 0, this pair
 
-    // Group 1 hands its row state to group 0 once its last PV is done.
-    const int last0 = (n - 1) & ~1;            // last even tile (n >= 1)
-    const int last1 = (n >= 2) ? ((n - 2) | 1) : -1;
-    if (grp == 1) {
-      if (ok && last1 >= 0 && !mbar_wait_warp(pv_done(1), (last1 >> 1) & 1)) ok = false;
-      xchg[row] = make_float2(m_ref, l_run);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(merge_bar);
-      if (!ok) {
-        flag_status(a.status, DFLASH_STATUS_TIMEOUT);
-        *abort_flag = 1;
-      }
-    } else {
-      if (ok && !mbar_wait_warp(pv_done(0), (last0 >> 1) & 1)) ok = false;
-      if (ok && last1 >= 0 && !mbar_wait_warp(pv_done(1), (last1 >> 1) & 1)) ok = false;
-      if (ok && !mbar_wait_warp(merge_bar, 0)) ok = false;
-      if (!ok) {
-        flag_status(a.status, DFLASH_STATUS_TIMEOUT);
-        *abort_flag = 1;
-      } else {
+      float m_ref = ninf();
+      float l_run = 0.f;
+      int last_j = -1;  // this group's latest tile in the segment
+      const int jfirst = sg.j0 + (((sg.j0 & 1) != grp) ? 1 : 0);
+      for (int j = jfirst; ok && j < sg.j1; j += 2) {
+        if (!mbar_wait_warp(s_full(grp), (j >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const float2 other = xchg[row];
-        const float M = fmaxf(m_ref, other.x);
-        const float w0 = (m_ref == ninf()) ? 0.f : fast_exp2(m_ref - M);
-        const float w1 = (other.x == ninf() || other.y == 0.f) ? 0.f : fast_exp2(other.x - M);
-        const float l = w0 * l_run + w1 * other.y;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t unit = (static_cast<size_t>(b) * a.Hkv + h) * a.S + s;
-        const bool direct = a.S == 1;  // one unit per (request, kv head): final output
-        const size_t orow = row < a.R ? out_row_index(a, b, h, row) : 0;
+        uint32_t sr[64];
+        tmem_ld64_wait(lane_addr + grp * T, sr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free(grp));
+
+        const int p0 = pos_base + j * T;
+        const bool need_mask = (p0 < lo_rows_max) || (p0 + T > hi_rows_min);
+        // Row max of the raw scores (the scale is positive), four independent
+        // chains; masked keys become -inf by select.  Boundary tiles only.
+        float mx[4] = {ninf(), ninf(), ninf(), ninf()};
+        if (need_mask) {
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o0[32], o1[32];
-          tmem_ld32_wait(lane_addr + C::kColO0 + cc * 32, o0);
-          tmem_ld32_wait(lane_addr + C::kColO1 + cc * 32, o1);
-          if (row < a.R) {
-            float v[32];
+          for (int c = 0; c < 64; ++c) {
+            const int pos = p0 + c;
+            const float v = (pos >= lo_r && pos < hi_r) ? __uint_as_float(sr[c]) : ninf();
+            sr[c] = __float_as_uint(v);
+            mx[c & 3] = fmaxf(mx[c & 3], v);
+          }
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              // A group that saw no key never wrote its accumulator: select,
-              // so its uninitialised columns cannot leak in.
-              const float a0 = w0 > 0.f ? w0 * __uint_as_float(o0[e]) : 0.f;
-              const float a1 = w1 > 0.f ? w1 * __uint_as_float(o1[e]) : 0.f;
-              v[e] = (a0 + a1) * inv;
+          for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c]));
+        }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+        // The reference max moves only when this tile's max passes it by more
+        // than 8 (p stays <= 2^8); O_g and l are rescaled then, which is exact.
+        const bool resc = mt > m_ref + 8.f;
+        float corr = 1.f;
+        if (resc) {
+          corr = (m_ref == ninf()) ? 0.f : fast_exp2(m_ref - mt);
+          l_run *= corr;
+          m_ref = mt;
+        }
+        const float neg_m = (m_ref == ninf()) ? 0.f : -m_ref;
+        float sm[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float pa = fast_exp2(fmaf(__uint_as_float(sr[2 * c]), a.scale_log2, neg_m));
+          const float pb = fast_exp2(fmaf(__uint_as_float(sr[2 * c + 1]), a.scale_log2, neg_m));
+          sm[c & 3] += pa + pb;
+          pk[c] = pack_bf16x2(pa, pb);
+        }
+        l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+
+        // This group's P buffer and O_g are free once its previous PV (tile
+        // j-2, possibly of the previous segment) has completed.  O_g holds
+        // this segment's sum only after the group's first tile in it.  The
+        // rescale's TMEM load/store are warp-collective: the whole warp runs
+        // them when any of its rows moved its reference max (factor 1 for
+        // the other rows).
+        const bool warp_resc = __any_sync(0xffffffffu, resc);
+        if (j >= 2) {
+          if (!mbar_wait_warp(pv_done(grp), ((j >> 1) - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          if (warp_resc && last_j >= 0) {
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32_wait(lane_addr + o_col + cc * 32, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+              tmem_st32(lane_addr + o_col + cc * 32, o);
             }
-            if (direct) {
-              uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + cc * 32);
+            tmem_wait_st();
+          }
+        }
+        // Value rows outside [lo_min, L+K) may hold anything: zero them in the
+        // stage before the PV MMA reads it (boundary tiles only).
+        if (p0 < geo.lo_min || p0 + T > geo.hi_max) {
+          const int st = j % NSV;
+          if (!mbar_wait_warp(v_full(st), (j / NSV) & 1)) { ok = false; break; }
+          if (gthread < T) {
+            const int pos = p0 + gthread;
+            if (pos < geo.lo_min || pos >= geo.hi_max) {
+              uint8_t* vrow = gbase + C::kOffV + st * C::kTileBytes + gthread * 128;
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                dst[e] = make_uint4(pack_bf16x2(v[8 * e], v[8 * e + 1]),
-                                    pack_bf16x2(v[8 * e + 2], v[8 * e + 3]),
-                                    pack_bf16x2(v[8 * e + 4], v[8 * e + 5]),
-                                    pack_bf16x2(v[8 * e + 6], v[8 * e + 7]));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(a.part_o + (unit * a.R + row) * D + cc * 32);
+              for (int x2 = 0; x2 < D / 64; ++x2)
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                for (int c = 0; c < 8; ++c)
+                  *reinterpret_cast<uint4*>(vrow + x2 * T * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
           }
         }
+        // P row -> this group's shared buffer, K-major, 128-byte swizzle.
         if (row < a.R) {
+          uint8_t* prow = gbase + C::kOffP + grp * C::kPBytes + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(grp));
+        last_j = j;
+      }
+
+      // ---- end of segment.  Each group publishes its row state once its last
+      // PV of the segment is done; then both merge the two states, group g
+      // for output columns [g*D/2, (g+1)*D/2).  Named barrier 3 joins the
+      // eight softmax warps; the stop decision is read between two barriers
+      // so that every softmax thread takes it alike.
+      if (ok && last_j >= 0 && !mbar_wait_warp(pv_done(grp), (last_j >> 1) & 1)) ok = false;
+      xchg[grp * 128 + row] = make_float2(m_ref, l_run);
+      if (!ok) *stop_word = 1;
+      tc_fence_before();
+      named_barrier(3, 256);
+      const bool stop = *stop_word != 0;
+      const bool direct = sg.g0 >= start && sg.g0 + sg.nb <= end;
+      const size_t orow = row < a.R ? out_row_index(a, sg.b, sg.h, row) : 0;
+      // A cut pair's partial goes to slot 0 (the range's first segment) or
+      // slot 1 (its last), for the combine kernel.
+      const size_t unit = static_cast<size_t>(blockIdx.x) * 2 + (sg.idx == 0 ? 0 : 1);
+      if (!stop) {
+        tc_fence_after();
+        const float2 s0 = xchg[row];
+        const float2 s1 = xchg[128 + row];
+        const float M = fmaxf(s0.x, s1.x);
+        const float w0 = (s0.x == ninf() || s0.y == 0.f) ? 0.f : fast_exp2(s0.x - M);
+        const float w1 = (s1.x == ninf() || s1.y == 0.f) ? 0.f : fast_exp2(s1.x - M);
+        const float l = w0 * s0.y + w1 * s1.y;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        store_segment_rows<D>(a, gbase + C::kOffP + sw * 4096, lane_addr, grp, quad, lane, w0, w1, inv,
+                              direct, sg.b, sg.h, unit);
+        if (row < a.R && grp == 0) {
           const float lse = l > 0.f ? M + log2f(l) : ninf();
           if (direct)
             a.lse2[orow] = lse;
@@ -479,15 +670,28 @@ __global__ void __launch_bounds__(352, 1)
             a.part_lse[unit * a.R + row] = lse;
         }
       }
+      // Every softmax thread has read stop_word, the states and both
+      // accumulators before any goes on (the next segment's first P, which
+      // lets the MMA overwrite an accumulator, comes after this barrier).
+      tc_fence_before();
+      named_barrier(3, 256);
+      if (stop) {
+        if (lane == 0) flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      if (sg.j1 >= n) break;
+      seg_next(sg, PB, a.Hkv, start, end);
     }
     tc_fence_before();
   }
 
   __syncthreads();
   if (*abort_flag && threadIdx.x == 0) {
-    const int ik = *issued_k, iv = *issued_v;
+    const int ik = *issued_k, iv = *issued_v, iq = *issued_q;
     for (int j = ik > NSK ? ik - NSK : 0; j < ik; ++j) (void)mbar_wait(k_full(j % NSK), (j / NSK) & 1);
     for (int j = iv > NSV ? iv - NSV : 0; j < iv; ++j) (void)mbar_wait(v_full(j % NSV), (j / NSV) & 1);
+    if (iq > 0) (void)mbar_wait(q_full, (iq - 1) & 1);
   }
   __syncthreads();
   if (warp == 1) {
@@ -498,13 +702,13 @@ __global__ void __launch_bounds__(352, 1)
 
 template <int D>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
-             const CUtensorMap& tm_v, cudaStream_t stream) {
+             const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream) {
   auto kern = split_tc_kernel<D>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
   if (err != cudaSuccess) return err;
-  dim3 grid(plan.S, a.Hkv, a.B);
-  kern<<<grid, TcCfg<D>::kThreads, TcCfg<D>::kSmem, stream>>>(a, tm_k, tm_v);
+  kern<<<static_cast<unsigned>(plan.units), TcCfg<D>::kThreads, TcCfg<D>::kSmem, stream>>>(
+      a, tm_k, tm_v, tm_q);
   return cudaGetLastError();
 }
 
@@ -516,9 +720,9 @@ int split_tc_threads() { return TcCfg<128>::kThreads; }
 int split_tc_smem_bytes(int D) { return D == 64 ? TcCfg<64>::kSmem : TcCfg<128>::kSmem; }
 
 int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
-                    const CUtensorMap& tm_v, cudaStream_t stream) {
-  if (a.D == 64) return launch_t<64>(a, plan, tm_k, tm_v, stream);
-  if (a.D == 128) return launch_t<128>(a, plan, tm_k, tm_v, stream);
+                    const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream) {
+  if (a.D == 64) return launch_t<64>(a, plan, tm_k, tm_v, tm_q, stream);
+  if (a.D == 128) return launch_t<128>(a, plan, tm_k, tm_v, tm_q, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -136,6 +136,9 @@ def touched_tiles(L, K, W, T):
     dict(window=100, max_ctx_len=1000), dict(batch=1, max_ctx_len=32768, max_pages_per_req=1030),
     dict(force_split_tiles=1), dict(force_split_tiles=3, window=50),
     dict(num_q_heads=64, num_kv_heads=16, batch=256, max_ctx_len=131072, max_pages_per_req=4100),
+    dict(num_q_heads=64, num_kv_heads=4, batch=96, max_ctx_len=8192, max_pages_per_req=260),
+    dict(num_q_heads=16, num_kv_heads=1, force_path=2, force_split_tiles=3, window=50),
+    dict(num_q_heads=16, num_kv_heads=1, batch=900, max_ctx_len=100, max_pages_per_req=4),
 ])
 def test_planner_covers_every_length(dflash_lib, kw):
     """For every context length up to max_ctx_len the units cover all tiles,
@@ -144,14 +147,23 @@ def test_planner_covers_every_length(dflash_lib, kw):
     p = base_params(**kw)
     pl = d.plan(p)
     T, C, S = pl["tile_keys"], pl["split_tiles"], pl["max_splits"]
-    assert pl["units"] == p.batch * p.num_kv_heads * S
     worst = max(touched_tiles(L, p.block_size, p.window, T) for L in range(0, p.max_ctx_len + 1))
-    assert S * C >= worst
-    assert (S - 1) * C < worst + C
     R = p.num_q_heads // p.num_kv_heads * p.block_size
     assert pl["rows"] == R and pl["rows_padded"] >= R
     ws = d.workspace_size(p)
-    assert ws >= 256 + pl["units"] * R * (p.head_dim + 1) * 4
+    if pl["path"] == d.PATH_TCGEN05:
+        # Flat split: `units` CTAs of C tiles cover every pair at max_ctx_len,
+        # two partial slots per CTA, at most one CTA per SM unless forced.
+        assert S == 2
+        assert pl["units"] * C >= p.batch * p.num_kv_heads * worst
+        if not kw.get("force_split_tiles"):
+            assert pl["units"] <= pl["num_sms"]
+        assert ws >= 256 + 2 * pl["units"] * R * (p.head_dim + 1) * 4
+    else:
+        assert pl["units"] == p.batch * p.num_kv_heads * S
+        assert S * C >= worst
+        assert (S - 1) * C < worst + C
+        assert ws >= 256 + pl["units"] * R * (p.head_dim + 1) * 4
     if kw.get("force_split_tiles"):
         assert C == kw["force_split_tiles"]
 
