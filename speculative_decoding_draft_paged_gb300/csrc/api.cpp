@@ -243,9 +243,9 @@ bool encode_pool(CUtensorMap* map, const void* pool, const dflash_params* p) {
   return r == CUDA_SUCCESS;
 }
 
-// 3-D view [B*K][Hq][D] of the queries, box = (64 columns, G heads, K
-// tokens): one box is the packed tile of one (request, kv head) pair, rows
-// r = i*G + g, for one 64-column half; 128-byte swizzle.
+// 3-D view [B*K][Hq][D] of the queries (or of the output), box = (64
+// columns, G heads, K tokens): one box is the packed tile of one (request,
+// kv head) pair, rows r = i*G + g, for one 64-column half; 128-byte swizzle.
 bool encode_queries(CUtensorMap* map, const void* q, const dflash_params* p) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
@@ -259,6 +259,23 @@ bool encode_queries(CUtensorMap* map, const void* q, const dflash_params* p) {
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D view [slots][R][D] of the fp32 partial outputs, box = (32 columns,
+// R rows, one slot); 128-byte swizzle.
+bool encode_partials(CUtensorMap* map, void* part_o, const dflash_params* p, int R, int64_t slots) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->head_dim), static_cast<cuuint64_t>(R),
+                              static_cast<cuuint64_t>(slots)};
+  const cuuint64_t row = static_cast<cuuint64_t>(p->head_dim) * 4;
+  const cuuint64_t strides[2] = {row, row * R};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(R), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, part_o, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -323,9 +340,8 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   if (workspace_bytes < workspace_bytes_for(p, k)) return DFLASH_ERR_WORKSPACE;
 
   const bool tc = k.path == DFLASH_PATH_TCGEN05;
-  CUtensorMap tm_k, tm_v, tm_q;
+  CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_part;
   if (!encode_pool(&tm_k, k_pages, p) || !encode_pool(&tm_v, v_pages, p)) return DFLASH_ERR_LAUNCH;
-  if (tc && !encode_queries(&tm_q, q, p)) return DFLASH_ERR_LAUNCH;
 
   AttnArgs a{};
   a.q = static_cast<const uint16_t*>(q);
@@ -340,6 +356,9 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   const size_t off_lse = kHeaderBytes;
   a.part_lse = reinterpret_cast<float*>(ws + off_lse);
   a.part_o = reinterpret_cast<float*>(ws + off_lse + align_up(partial_rows_for(k) * sizeof(float), 256));
+  if (tc && (!encode_queries(&tm_q, q, p) || !encode_queries(&tm_out, out, p) ||
+             !encode_partials(&tm_part, a.part_o, p, k.R, k.units * k.S)))
+    return DFLASH_ERR_LAUNCH;
   a.B = p->batch;
   a.Hq = p->num_q_heads;
   a.Hkv = p->num_kv_heads;
@@ -366,7 +385,8 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   if (split_start != nullptr &&
       cudaEventRecord(static_cast<cudaEvent_t>(split_start), s) != cudaSuccess)
     return DFLASH_ERR_LAUNCH;
-  int err = tc ? launch_split_tc(a, k, tm_k, tm_v, tm_q, s) : launch_split_mma(a, k, tm_k, tm_v, s);
+  int err = tc ? launch_split_tc(a, k, tm_k, tm_v, tm_q, tm_out, tm_part, s)
+               : launch_split_mma(a, k, tm_k, tm_v, s);
   if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
   if (split_done != nullptr &&
       cudaEventRecord(static_cast<cudaEvent_t>(split_done), s) != cudaSuccess)

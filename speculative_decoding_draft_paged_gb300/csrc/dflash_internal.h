@@ -107,7 +107,8 @@ struct KernelPlan {
 int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
                      const CUtensorMap& tm_v, cudaStream_t stream);
 int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
-                    const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream);
+                    const CUtensorMap& tm_v, const CUtensorMap& tm_q, const CUtensorMap& tm_out,
+                    const CUtensorMap& tm_part, cudaStream_t stream);
 int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat);
 
 // Shared-memory bytes of each split kernel for a plan (used by the planner).

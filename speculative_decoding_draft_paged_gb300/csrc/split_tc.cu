@@ -148,27 +148,30 @@ __device__ __forceinline__ int chunk_page(const AttnArgs& a, const int* PB, cons
   return __ldg(&a.page_table[static_cast<size_t>(b) * a.max_pages + slot]);
 }
 
-// End-of-segment output of one softmax warp: its 32 rows (TMEM lanes of
-// its quadrant) x its group's half of the columns, w0 * O0 + w1 * O1 scaled
-// by inv, written as bf16 rows of the output (direct) or fp32 rows of the
-// CTA's partial slot `unit`.  The rows go through the warp's own 4 KB of the
-// idle P buffers, transposed so that a store instruction covers whole row
-// pieces instead of one 16-byte piece per row.  Row pieces in the slot:
-// bf16, 64 bytes = 4 chunks of 16 stored at c ^ ((lane >> 1) & 3); fp32,
-// 128 bytes = 8 chunks stored at c ^ (lane & 7) (conflict-free both ways).
-// Kept out of line: it runs once per segment, and inlined it would crowd
-// the tile loop's registers.
+// End-of-segment output of one softmax group for output columns
+// [col0, col0 + 64): w0 * O0 + w1 * O1 scaled by inv, as bf16 rows of the
+// output (direct) or fp32 rows of the CTA's partial slot `unit`.  Each thread
+// puts its row into the group's (now idle) 16 KB P buffer with the 128-byte
+// swizzle, and one thread hands the box to the TMA engine, which writes it
+// asynchronously: bf16 as one box (64 columns, G heads, K tokens) of the
+// output, fp32 as two boxes (32 columns, R rows) of the partial slot.  The
+// threads only wait until the box has been read out of shared memory.  Kept
+// out of line: it runs once per segment, and inlined it would crowd the tile
+// loop's registers.
 template <int D>
-__device__ __noinline__ void store_segment_rows(const AttnArgs& a, uint8_t* stg, uint32_t lane_addr,
-                                                int grp, int quad, int lane, float w0, float w1,
-                                                float inv, bool direct, int b, int h, size_t unit) {
+__device__ __noinline__ void store_segment_rows(const AttnArgs& a, const CUtensorMap* tm_out,
+                                                const CUtensorMap* tm_part, uint8_t* stg,
+                                                uint32_t stg_u32, uint32_t lane_addr, int col0, int grp,
+                                                int row, bool leader, float w0, float w1, float inv,
+                                                bool direct, int b, int h, int unit) {
   constexpr int kColO0 = 128, kColO1 = 256;
+  const int bar_id = 4 + grp;
+  uint8_t* srow = stg + row * 128;
+  const int sw = row & 7;
 #pragma unroll 1
-  for (int cc = 0; cc < D / 64; ++cc) {
-    const int col = grp * (D / 2) + cc * 32;
-    __syncwarp();  // the previous chunk's reads of the staging slot are done
+  for (int cc = 0; cc < 2; ++cc) {
     uint32_t o0[32], o1[32];
-    tmem_ld32x2_wait(lane_addr + kColO0 + col, lane_addr + kColO1 + col, o0, o1);
+    tmem_ld32x2_wait(lane_addr + kColO0 + col0 + cc * 32, lane_addr + kColO1 + col0 + cc * 32, o0, o1);
     // A group that saw no key of this segment holds a stale or
     // uninitialised accumulator: select, so it cannot leak in.
     auto val = [&](int e) {
@@ -178,33 +181,28 @@ __device__ __noinline__ void store_segment_rows(const AttnArgs& a, uint8_t* stg,
     };
     if (direct) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
-            make_uint4(pack_bf16x2(val(8 * c), val(8 * c + 1)), pack_bf16x2(val(8 * c + 2), val(8 * c + 3)),
-                       pack_bf16x2(val(8 * c + 4), val(8 * c + 5)), pack_bf16x2(val(8 * c + 6), val(8 * c + 7)));
-      __syncwarp();
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int rl = it * 8 + (lane >> 2);
-        const int c = lane & 3;
-        const uint4 x = *reinterpret_cast<const uint4*>(stg + rl * 64 + ((c ^ ((rl >> 1) & 3)) << 4));
-        const int ro = quad * 32 + rl;
-        if (ro < a.R) *reinterpret_cast<uint4*>(a.out + out_row_index(a, b, h, ro) * D + col + c * 8) = x;
-      }
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(srow + (((cc * 4 + q) ^ sw) << 4)) =
+            make_uint4(pack_bf16x2(val(8 * q), val(8 * q + 1)), pack_bf16x2(val(8 * q + 2), val(8 * q + 3)),
+                       pack_bf16x2(val(8 * q + 4), val(8 * q + 5)), pack_bf16x2(val(8 * q + 6), val(8 * q + 7)));
     } else {
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-            make_float4(val(4 * c), val(4 * c + 1), val(4 * c + 2), val(4 * c + 3));
-      __syncwarp();
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int rl = it * 4 + (lane >> 3);
-        const int c = lane & 7;
-        const float4 x = *reinterpret_cast<const float4*>(stg + rl * 128 + ((c ^ (rl & 7)) << 4));
-        const int ro = quad * 32 + rl;
-        if (ro < a.R) *reinterpret_cast<float4*>(a.part_o + (unit * a.R + ro) * D + col + c * 4) = x;
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(srow + ((q ^ sw) << 4)) =
+            make_float4(val(4 * q), val(4 * q + 1), val(4 * q + 2), val(4 * q + 3));
+    }
+    if (!direct || cc == 1) {
+      fence_proxy_async_smem();
+      named_barrier(bar_id, 128);
+      if (leader) {
+        if (direct)
+          tma_store_3d(tm_out, stg_u32, col0, h * a.G, b * a.K);
+        else
+          tma_store_3d(tm_part, stg_u32, col0 + cc * 32, 0, unit);
+        bulk_commit();
+        bulk_wait_read_all();
       }
+      named_barrier(bar_id, 128);  // the staging rows may be written again
     }
   }
 }
@@ -212,8 +210,9 @@ __device__ __noinline__ void store_segment_rows(const AttnArgs& a, uint8_t* stg,
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     split_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_q) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_out,
+                    const __grid_constant__ CUtensorMap tm_part) {
   using C = TcCfg<D>;
   constexpr int T = C::T;
   constexpr int NSK = C::NSK;
@@ -300,6 +299,8 @@ __global__ void __launch_bounds__(384, 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_out);
+    prefetch_tensormap(&tm_part);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), C::kTmemCols);
@@ -660,8 +661,11 @@ __global__ void __launch_bounds__(384, 1)
         const float w1 = (s1.x == ninf() || s1.y == 0.f) ? 0.f : fast_exp2(s1.x - M);
         const float l = w0 * s0.y + w1 * s1.y;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        store_segment_rows<D>(a, gbase + C::kOffP + sw * 4096, lane_addr, grp, quad, lane, w0, w1, inv,
-                              direct, sg.b, sg.h, unit);
+        // D = 128: group g writes columns [64g, 64g + 64); D = 64: group 0 all.
+        if (grp * 64 < D)
+          store_segment_rows<D>(a, &tm_out, &tm_part, gbase + C::kOffP + grp * C::kPBytes,
+                                sP + grp * C::kPBytes, lane_addr, grp * 64, grp, row, gthread == 0, w0, w1,
+                                inv, direct, sg.b, sg.h, static_cast<int>(unit));
         if (row < a.R && grp == 0) {
           const float lse = l > 0.f ? M + log2f(l) : ninf();
           if (direct)
@@ -683,6 +687,7 @@ __global__ void __launch_bounds__(384, 1)
       if (sg.j1 >= n) break;
       seg_next(sg, PB, a.Hkv, start, end);
     }
+    if (gthread == 0) bulk_wait_all();  // this group's output boxes are written
     tc_fence_before();
   }
 
@@ -702,13 +707,14 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
-             const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream) {
+             const CUtensorMap& tm_v, const CUtensorMap& tm_q, const CUtensorMap& tm_out,
+             const CUtensorMap& tm_part, cudaStream_t stream) {
   auto kern = split_tc_kernel<D>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
   if (err != cudaSuccess) return err;
   kern<<<static_cast<unsigned>(plan.units), TcCfg<D>::kThreads, TcCfg<D>::kSmem, stream>>>(
-      a, tm_k, tm_v, tm_q);
+      a, tm_k, tm_v, tm_q, tm_out, tm_part);
   return cudaGetLastError();
 }
 
@@ -720,9 +726,10 @@ int split_tc_threads() { return TcCfg<128>::kThreads; }
 int split_tc_smem_bytes(int D) { return D == 64 ? TcCfg<64>::kSmem : TcCfg<128>::kSmem; }
 
 int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
-                    const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream) {
-  if (a.D == 64) return launch_t<64>(a, plan, tm_k, tm_v, tm_q, stream);
-  if (a.D == 128) return launch_t<128>(a, plan, tm_k, tm_v, tm_q, stream);
+                    const CUtensorMap& tm_v, const CUtensorMap& tm_q, const CUtensorMap& tm_out,
+                    const CUtensorMap& tm_part, cudaStream_t stream) {
+  if (a.D == 64) return launch_t<64>(a, plan, tm_k, tm_v, tm_q, tm_out, tm_part, stream);
+  if (a.D == 128) return launch_t<128>(a, plan, tm_k, tm_v, tm_q, tm_out, tm_part, stream);
   return cudaErrorInvalidValue;
 }
 
