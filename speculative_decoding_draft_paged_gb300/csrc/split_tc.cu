@@ -30,7 +30,7 @@
 //                    segment's tile is prefetched into L2 meanwhile;
 //   warp 1           allocates 512 TMEM columns; lane 0 issues the MMAs:
 //                    S_j = Q K_j^T (M=128, N=64, K=D) into TMEM S buffer j%2,
-//                    then O_{j%2} += P_j V_j (M=128, N=D, K=64);
+//                    then O_{j%2} += P_j V_j (M=128, N=D, K=64; P from TMEM);
 //   warps 2..9       softmax, two groups of four warps: group g takes the
 //                    range's tiles j = g, g+2, ... with its own running state
 //                    and TMEM accumulator O_g.  A thread owns one query row
@@ -38,8 +38,8 @@
 //                    S_j, masks by select, keeps a base-2 reference max that
 //                    moves only when a tile's max exceeds it by more than 8
 //                    (then O_g and the row sum are rescaled, exactly), and
-//                    writes P_j = 2^(s - m) in bf16 to its group's shared P
-//                    buffer, the A operand of the PV MMA.  At the end of each
+//                    writes P_j = 2^(s - m) in bf16 to its group's TMEM P
+//                    columns, the A operand of the PV MMA.  At the end of each
 //                    segment both groups merge the two states, each for half
 //                    of the output columns, and write them.
 // Every mbarrier wait is bounded (DFLASH_STATUS_TIMEOUT, then drain).
@@ -56,15 +56,15 @@ template <int D>
 struct TcCfg {
   static constexpr int T = 64;               // keys per tile
   static constexpr int NSK = 4;              // K ring stages
-  static constexpr int NSV = 4;              // V ring stages
+  static constexpr int NSV = 5;              // V ring stages (V slots are held longer)
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kTileBytes = T * D * 2;  // one K or V tile
-  static constexpr int kPBytes = 128 * T * 2;   // one group's P buffer
+  static constexpr int kStageBytes = 128 * T * 2;   // one group's output staging buffer
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + NSK * kTileBytes;
-  static constexpr int kOffP = kOffV + NSV * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffStage = kOffV + NSV * kTileBytes;
+  static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
   // k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
   // s_free[2], p_full[2], pv_done[2], q_full, q_free
   static constexpr int kNumBars = 2 * NSK + 2 * NSV + 10;
@@ -73,9 +73,12 @@ struct TcCfg {
   static constexpr int kOffPB = kOffXchg + 2 * 128 * 8;          // tile prefix per request
   static constexpr int kOffLc = kOffPB + 4 * (kTcMaxBatch + 1);  // clamped context lengths
   static constexpr int kSmem = kOffLc + 4 * kTcMaxBatch + 1024;
-  static constexpr int kTmemCols = 512;   // S0 [0,64) S1 [64,128) O0 [128,128+D) O1 [256,256+D)
+  // TMEM columns: S0 [0,64) S1 [64,128) O0 [128,128+D) O1 [256,256+D)
+  // P0 [384,416) P1 [416,448) (bf16 pairs).
+  static constexpr int kTmemCols = 512;
   static constexpr int kColO0 = 128;
   static constexpr int kColO1 = 256;
+  static constexpr int kColP = 384;
   static constexpr int kThreads = 384;
 };
 
@@ -151,7 +154,7 @@ __device__ __forceinline__ int chunk_page(const AttnArgs& a, const int* PB, cons
 // End-of-segment output of one softmax group for output columns
 // [col0, col0 + 64): w0 * O0 + w1 * O1 scaled by inv, as bf16 rows of the
 // output (direct) or fp32 rows of the CTA's partial slot `unit`.  Each thread
-// puts its row into the group's (now idle) 16 KB P buffer with the 128-byte
+// puts its row into the group's 16 KB staging buffer with the 128-byte
 // swizzle, and one thread hands the box to the TMA engine, which writes it
 // asynchronously: bf16 as one box (64 columns, G heads, K tokens) of the
 // output, fp32 as two boxes (32 columns, R rows) of the partial slot.  The
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sQ = base + C::kOffQ;
   const uint32_t sK = base + C::kOffK;
   const uint32_t sV = base + C::kOffV;
-  const uint32_t sP = base + C::kOffP;
+  const uint32_t sStage = base + C::kOffStage;
   const uint32_t bars = base + C::kOffBar;
   auto k_full = [&](int st) { return bars + 8u * st; };
   auto k_empty = [&](int st) { return bars + 8u * (NSK + st); };
@@ -415,7 +418,6 @@ __global__ void __launch_bounds__(384, 1)
       // address >> 4): build each base once and add offsets >> 4.
       const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t dp = smem_desc_sw128(sP, 16, 1024);
       const uint64_t dv = smem_desc_sw128(sV, T * 128, 1024);
       Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
       int q_seg = -1;            // segment whose query tile has been waited for
@@ -463,8 +465,8 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t o_col = g ? C::kColO1 : C::kColO0;
 #pragma unroll
         for (int kk = 0; kk < T / 16; ++kk)
-          umma_bf16(tmem + o_col, dp + ((g * C::kPBytes + kk * 32) >> 4),
-                    dv + ((v_off + kk * 16 * 128) >> 4), idesc_pv, (!fresh || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + o_col, tmem + C::kColP + g * (T / 2) + kk * 8,
+                       dv + ((v_off + kk * 16 * 128) >> 4), idesc_pv, (!fresh || kk > 0) ? 1u : 0u);
         umma_commit(v_empty(st));
         umma_commit(pv_done(g));
         last_pv = jj;
@@ -582,7 +584,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
 
-        // This group's P buffer and O_g are free once its previous PV (tile
+        // This group's P columns and O_g are free once its previous PV (tile
         // j-2, possibly of the previous segment) has completed.  O_g holds
         // this segment's sum only after the group's first tile in it.  The
         // rescale's TMEM load/store are warp-collective: the whole warp runs
@@ -621,15 +623,10 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
         }
-        // P row -> this group's shared buffer, K-major, 128-byte swizzle.
-        if (row < a.R) {
-          uint8_t* prow = gbase + C::kOffP + grp * C::kPBytes + row * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        }
-        fence_proxy_async_smem();
+        // P row -> this group's TMEM P columns (key pairs per column).
+        tmem_st32(lane_addr + C::kColP + grp * (T / 2), pk);
+        tmem_wait_st();
+        fence_proxy_async_smem();  // the zeroed V rows, for the MMA
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full(grp));
@@ -663,8 +660,8 @@ __global__ void __launch_bounds__(384, 1)
         const float inv = l > 0.f ? 1.f / l : 0.f;
         // D = 128: group g writes columns [64g, 64g + 64); D = 64: group 0 all.
         if (grp * 64 < D)
-          store_segment_rows<D>(a, &tm_out, &tm_part, gbase + C::kOffP + grp * C::kPBytes,
-                                sP + grp * C::kPBytes, lane_addr, grp * 64, grp, row, gthread == 0, w0, w1,
+          store_segment_rows<D>(a, &tm_out, &tm_part, gbase + C::kOffStage + grp * C::kStageBytes,
+                                sStage + grp * C::kStageBytes, lane_addr, grp * 64, grp, row, gthread == 0, w0, w1,
                                 inv, direct, sg.b, sg.h, static_cast<int>(unit));
         if (row < a.R && grp == 0) {
           const float lse = l > 0.f ? M + log2f(l) : ninf();
