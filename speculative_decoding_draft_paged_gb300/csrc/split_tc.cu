@@ -18,7 +18,7 @@
 // of QK^T.
 //
 // Warp roles (384 threads):
-//   warp 0 / warp 10 K / V producer: the warp keeps the page ids of the next
+//   warp 10 / warp 0 K / V producer: the warp keeps the page ids of the next
 //                    32 page-table slots in registers (one chunk ahead); lane
 //                    0 issues one 128-byte-swizzled TMA box per (page,
 //                    64-column half) into separate K and V rings.  A K slot is
@@ -331,7 +331,10 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0 || warp == 10) {
     // ------------------------------------------------------------ producers (whole warp)
-    const bool is_v = warp == 10;
+    // Warp 0 reaches its first page-table shuffle about 2 us later than the
+    // other warps (measured); the V tiles are needed a softmax later than the
+    // K tiles, so warp 0 takes the V ring.
+    const bool is_v = warp == 0;
     const int ns = is_v ? NSV : NSK;
     const uint32_t ring = is_v ? sV : sK;
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
