@@ -138,12 +138,17 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
     // every pair at max_ctx_len.  Two partial slots per CTA.
     if (p->force_split_tiles > 0) {
       k.C = p->force_split_tiles;
+      k.seg_cost = 0;
       k.units = (tc_tiles + k.C - 1) / k.C;
     } else {
-      int64_t ctas = (tc_tiles + kTcMinTiles - 1) / kTcMinTiles;
+      // A segment's end (merge, output staging, query reload) costs about as
+      // much time as this many key tiles (measured on the headline shape).
+      k.seg_cost = D == 128 ? 4 : 8;
+      const int64_t cost = tc_tiles + static_cast<int64_t>(k.seg_cost) * p->batch * p->num_kv_heads;
+      int64_t ctas = (cost + kTcMinTiles - 1) / kTcMinTiles;
       if (ctas > num_sms) ctas = num_sms;
       k.units = ctas;
-      k.C = static_cast<int>((tc_tiles + ctas - 1) / ctas);
+      k.C = static_cast<int>((cost + ctas - 1) / ctas);
       if (k.C < kTcMinTiles) k.C = kTcMinTiles;
     }
     k.S = 2;
@@ -380,6 +385,7 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   a.ncta = tc ? static_cast<int>(k.units) : 0;
   a.qn_force = tc ? p->force_split_tiles : 0;
   a.qn_min = kTcMinTiles;
+  a.seg_cost = tc ? k.seg_cost : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (split_start != nullptr &&

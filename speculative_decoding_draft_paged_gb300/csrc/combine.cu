@@ -11,7 +11,7 @@
 //   mma.sync split kernel: the row's partials are the units s of its
 //   (request, kv head) pair, when a request has more than one unit.
 //   tcgen05 flat split: the pair's tiles [g0, g0 + nb) lie in the ranges of
-//   CTAs c0..c1 (range length qn, the same tile prefix as the split kernel);
+//   CTAs c0..c1 (the same tile prefix and range map as the split kernel);
 //   partial s is CTA c0 + s, slot 1 of c0 when the pair starts inside c0's
 //   range (its last segment there), else slot 0 (the first segment of the
 //   range).  A pair inside one range was written by the split kernel itself.
@@ -175,13 +175,15 @@ __global__ void __launch_bounds__(kThreads, 6) combine_flat_kernel(const AttnArg
   row_coords(a, row_id, b, i, hq);
   const int h = hq / a.G;
   const int r = i * a.G + (hq - h * a.G);
-  const int qn = flat_range_tiles(a, a.Hkv * PB[a.B]);
+  const FlatMap fmap = flat_map(a, PB);
   const int nb = PB[b + 1] - PB[b];
   const int g0 = a.Hkv * PB[b] + h * nb;
-  const int c0 = g0 / qn;
-  const int c1 = (g0 + nb - 1) / qn;
+  const long long cp = flat_pair_cost(a, PB, fmap, b, h);
+  const int c0 = static_cast<int>(cp / fmap.q);
+  const int c1 = static_cast<int>((cp + nb - 1) / fmap.q);
   if (c0 == c1) return;  // the split kernel wrote this row
-  const int slot0 = g0 > c0 * qn ? 1 : 0;
+  // Slot 1 of c0 when c0's range starts before this pair.
+  const int slot0 = flat_tile_at(a, PB, fmap, static_cast<long long>(c0) * fmap.q) < g0 ? 1 : 0;
 
   pdl_wait_primary();
   float acc[D / 32], M, den;

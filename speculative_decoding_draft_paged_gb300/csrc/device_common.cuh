@@ -274,12 +274,65 @@ __device__ __forceinline__ void flat_tile_prefix(const AttnArgs& a, int* PB, int
   __syncthreads();
 }
 
-// Tiles per CTA range: forced, or an equal share of `total` over the grid
-// (at least qn_min).
-__device__ __forceinline__ int flat_range_tiles(const AttnArgs& a, int total) {
-  if (a.qn_force > 0) return a.qn_force;
-  const int q = (total + a.ncta - 1) / a.ncta;
-  return q < a.qn_min ? a.qn_min : q;
+// CTA ranges of the flat split.  Pair p = b*Hkv + h has nb = PB[b+1] - PB[b]
+// tiles; in "cost" units its tiles sit at C_p .. C_p + nb - 1 with
+// C_p = Hkv*PB[b] + h*nb + w*p, followed by w units standing for the epilogue
+// that ends the pair's segment.  CTA c takes the tiles whose cost position
+// lies in [c*q, (c+1)*q), so a range that holds more pair ends holds fewer
+// tiles.  w = 0 and q = a forced length when force_split_tiles is set.
+struct FlatMap {
+  int q;      // cost units per CTA range
+  int w;      // cost units per pair end
+  int total;  // tiles of all pairs
+};
+
+__device__ __forceinline__ FlatMap flat_map(const AttnArgs& a, const int* PB) {
+  FlatMap m;
+  m.total = a.Hkv * PB[a.B];
+  if (a.qn_force > 0) {
+    m.q = a.qn_force;
+    m.w = 0;
+    return m;
+  }
+  m.w = a.seg_cost;
+  const long long cost = static_cast<long long>(m.total) + static_cast<long long>(m.w) * a.B * a.Hkv;
+  long long q = (cost + a.ncta - 1) / a.ncta;
+  if (q < a.qn_min) q = a.qn_min;
+  m.q = static_cast<int>(q);
+  return m;
+}
+
+// Cost position of the first tile of pair (b, h).
+__device__ __forceinline__ long long flat_pair_cost(const AttnArgs& a, const int* PB, const FlatMap& m,
+                                                    int b, int h) {
+  const int nb = PB[b + 1] - PB[b];
+  return static_cast<long long>(a.Hkv) * PB[b] + static_cast<long long>(h) * nb +
+         static_cast<long long>(m.w) * (static_cast<long long>(b) * a.Hkv + h);
+}
+
+// First tile whose cost position is >= x (m.total past the last one).
+__device__ __forceinline__ int flat_tile_at(const AttnArgs& a, const int* PB, const FlatMap& m, long long x) {
+  if (x <= 0) return 0;
+  int lo = 0, hi = a.B - 1;  // last request whose first pair's cost is <= x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (flat_pair_cost(a, PB, m, mid, 0) <= x) lo = mid; else hi = mid - 1;
+  }
+  const int nb = PB[lo + 1] - PB[lo];
+  const long long rel = x - flat_pair_cost(a, PB, m, lo, 0);
+  const long long per = static_cast<long long>(nb) + m.w;
+  long long h = rel / per;
+  if (h >= a.Hkv) return a.Hkv * PB[lo + 1];
+  long long t = rel - h * per;
+  if (t > nb) t = nb;
+  return a.Hkv * PB[lo] + static_cast<int>(h) * nb + static_cast<int>(t);
+}
+
+// Tile range [start, end) of CTA c.
+__device__ __forceinline__ void flat_range(const AttnArgs& a, const int* PB, const FlatMap& m, int c,
+                                           int& start, int& end) {
+  start = flat_tile_at(a, PB, m, static_cast<long long>(c) * m.q);
+  end = flat_tile_at(a, PB, m, static_cast<long long>(c + 1) * m.q);
 }
 
 // Programmatic dependent launch controls.

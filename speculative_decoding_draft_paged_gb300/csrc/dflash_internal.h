@@ -51,7 +51,8 @@ struct AttnArgs {
   // part_o/part_lse hold two slots per CTA.
   int ncta;                   // CTAs of the tcgen05 split kernel
   int qn_force;               // tiles per CTA range if > 0, else from the lengths
-  int qn_min;                 // fewest tiles per CTA range (lengths-derived case)
+  int qn_min;                 // fewest cost units per CTA range (lengths-derived case)
+  int seg_cost;               // cost units (tile times) of a segment's end, per pair
 };
 
 // Per-(request, kv head) key-range geometry of the split kernel, which covers
@@ -100,6 +101,7 @@ struct KernelPlan {
   int64_t units;    // mma: split units; tcgen05: CTAs
   int threads, smem_bytes;
   int kpw;          // mma path: keys per warp per tile
+  int seg_cost;     // tcgen05 path: cost units of a segment's end
   int num_sms;
 };
 

@@ -243,12 +243,10 @@ __global__ void __launch_bounds__(384, 1)
   }
   // Tile prefix over the requests, computed by every CTA.
   flat_tile_prefix<C::kThreads>(a, PB, Lc, warp_sums, blockIdx.x == 0);
-  const int total = a.Hkv * PB[a.B];
-  const int qn = flat_range_tiles(a, total);
-  const long long start_ll = static_cast<long long>(blockIdx.x) * qn;
-  if (start_ll >= total) return;  // no tiles for this CTA (uniform)
-  const int start = static_cast<int>(start_ll);
-  const int end = min(start + qn, total);
+  const FlatMap fmap = flat_map(a, PB);
+  int start, end;
+  flat_range(a, PB, fmap, blockIdx.x, start, end);
+  if (end <= start) return;  // no tiles for this CTA (uniform)
   const int n = end - start;
 
   const uint32_t sQ = base + C::kOffQ;
