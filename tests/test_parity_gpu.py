@@ -86,6 +86,26 @@ def test_tcgen05_unit_tile_counts(cuda_device, n_tiles):
     check_case(spec, cuda_device, force_path=dflash.PATH_TCGEN05, force_split_tiles=n_tiles)
 
 
+@pytest.mark.parametrize("kind", ["many_short", "one_long", "max_batch"])
+def test_tcgen05_flat_split_batches(cuda_device, kind):
+    """The flat split over many pairs: ranges holding many whole pairs
+    (direct outputs), one long pair cut over many CTAs among short ones, and
+    the largest batch the tcgen05 kernel takes."""
+    rng = np.random.default_rng({"many_short": 21, "one_long": 22, "max_batch": 23}[kind])
+    if kind == "many_short":
+        lens = [int(x) for x in rng.integers(0, 300, size=200)]
+        window = 0
+    elif kind == "one_long":
+        lens = [12000] + [int(x) for x in rng.integers(0, 200, size=39)]
+        window = 4096
+    else:
+        lens = [int(x) for x in rng.integers(0, 64, size=768)]
+        window = 0
+    spec = W.CaseSpec(f"tc_flat_{kind}", B=len(lens), Hq=16, Hkv=1, D=128, K=7, P=64, window=window,
+                      future_keys=1, ctx_lens=lens, seed=31, poison=True)
+    check_case(spec, cuda_device, force_path=dflash.PATH_TCGEN05)
+
+
 @pytest.mark.parametrize("G,K", [(1, 1), (4, 3), (16, 1), (3, 5), (4, 7), (6, 7), (16, 3), (5, 13),
                                  (16, 7), (8, 16)])
 @pytest.mark.parametrize("D", [64, 128])
