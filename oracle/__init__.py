@@ -60,7 +60,7 @@ def load_library(path: str):
     f = lib.oracle_block_attn
     f.restype = ctypes.c_int
     i32, vp = ctypes.c_int, ctypes.c_void_p
-    f.argtypes = [i32] * 10 + [ctypes.c_double] + [vp] * 6 + [i32] + [vp, vp, i32]
+    f.argtypes = [i32] * 11 + [ctypes.c_double] + [vp] * 6 + [i32] + [vp, vp, i32]
     return lib
 
 
@@ -77,7 +77,7 @@ def _ptr(a):
 
 
 def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window, future_keys,
-               scale, req_ids=None, nthreads=0, lib=None):
+               scale, right_window=0, req_ids=None, nthreads=0, lib=None):
     """Return ``(out, lse2)`` in float64 for requests ``req_ids`` (all when None).
 
     ``q``: uint16 bf16 bits ``[B, K, Hq, D]``; ``k_pages``/``v_pages``: uint16
@@ -105,7 +105,7 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window,
     lse2 = np.zeros((n, K, Hq), dtype=np.float64)
     rc = (lib or _load()).oracle_block_attn(
         B, Hq, Hkv, D, P, page_table.shape[1], num_pages, K, int(window), int(future_keys),
-        float(scale), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(ctx_lens),
+        int(right_window), float(scale), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(ctx_lens),
         _ptr(req_ids), n, _ptr(out), _ptr(lse2), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_block_attn failed with status {rc}")

@@ -12,10 +12,12 @@
 // the same pages at logical positions L .. L+K-1, query token i of the block
 // (position L+i) of query head hq, which reads kv head hq / G (G = Hq / Hkv),
 // sees
-//   * context positions p in [lo_i, L), lo_i = max(0, L+i-W+1) when a window
-//     W > 0 is given (the causal window (L+i-W, L+i]), else lo_i = 0;
-//   * block positions L+j for every j in [0, K) in the non-causal form
-//     (future_keys = 1), or for j in [0, i] in the causal form.
+//   * the causal window (L+i-W, L+i] when a window W > 0 is given, else every
+//     position up to L+i (context and block keys alike);
+//   * the later block keys L+j, i < j <= i + r, where r = K-1 in the
+//     non-causal form (future_keys = 1: every later block key) and r is the
+//     given right window otherwise (0: the causal form) -- PR #21130 "Why":
+//     the causal window plus the later keys of the block.
 // Every key row is read through the page table: the row of logical position p
 // is pages[page_table[b][p / P]][h][p % P][:] (HND page layout, PR #20374
 // kernel sweep: "page 32, HND").  Then, in double precision,
@@ -44,7 +46,7 @@ double bf16_to_double(uint16_t bits) {
 }
 
 struct Problem {
-  int B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys;
+  int B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys, right_window;
   double scale;
   const uint16_t* q;
   const uint16_t* k_pages;
@@ -70,12 +72,14 @@ int attend_row(const Problem& pr, int b, int i, int hq, double* out_row, double*
   const int64_t L = pr.ctx_lens[b];
   if (L < 0) return -2;
 
-  // Visible logical positions, in increasing order.
+  // Visible logical positions, in increasing order: the causal window, then
+  // the later block keys within the right window.
   std::vector<int64_t> pos;
   const int64_t lo = (pr.W > 0) ? std::max<int64_t>(0, L + i - pr.W + 1) : 0;
-  for (int64_t p = lo; p < L; ++p) pos.push_back(p);
-  const int j_end = pr.future_keys ? pr.K : i + 1;
-  for (int j = 0; j < j_end; ++j) pos.push_back(L + j);
+  for (int64_t p = lo; p <= L + i; ++p) pos.push_back(p);
+  const int r = pr.future_keys ? pr.K - 1 : pr.right_window;
+  const int j_last = std::min(pr.K - 1, i + r);
+  for (int j = i + 1; j <= j_last; ++j) pos.push_back(L + j);
 
   const uint16_t* qrow = pr.q + ((static_cast<int64_t>(b) * pr.K + i) * pr.Hq + hq) * pr.D;
   std::vector<double> qd(pr.D);
@@ -116,15 +120,15 @@ extern "C" {
 // negative context length, -3 for a visible position whose page-table entry is
 // out of range.
 int oracle_block_attn(int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
-                      int K, int W, int future_keys, double scale,
+                      int K, int W, int future_keys, int right_window, double scale,
                       const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
                       const int32_t* page_table, const int32_t* ctx_lens,
                       const int32_t* req_ids, int n_req,
                       double* out, double* lse2, int nthreads) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0 || K <= 0 ||
-      W < 0 || max_pages <= 0 || num_pages <= 0)
+      W < 0 || max_pages <= 0 || num_pages <= 0 || right_window < 0)
     return -1;
-  Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, scale,
+  Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, right_window, scale,
              q, k_pages, v_pages, page_table, ctx_lens};
   if (req_ids == nullptr) n_req = B;
   const int G = Hq / Hkv;

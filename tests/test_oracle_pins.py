@@ -28,20 +28,21 @@ LN2 = math.log(2.0)
 # Dense library references (torch float64 on CPU, contiguous keys, no paging)
 # ----------------------------------------------------------------------------
 
-def visible_mask(L, K, W, future_keys):
+def visible_mask(L, K, W, future_keys, right_window=0):
     """Boolean [K, L+K] mask of the pages' visible set, by position.
 
     Query i sits at position L+i.  Causal window: (L+i-W, L+i] (all of
-    [0, L+i] when W = 0).  Non-causal form: every block key L..L+K-1 too.
+    [0, L+i] when W = 0).  Later block keys: positions in (L+i, L+i+r], r =
+    K-1 in the non-causal form (every later block key) else the right window.
     """
-    pos = np.arange(L + K)
+    pos = np.arange(L + K)[None, :]
     qpos = L + np.arange(K)[:, None]
-    causal = pos[None, :] <= qpos
+    causal = pos <= qpos
     if W > 0:
-        causal &= pos[None, :] > qpos - W
-    if future_keys:
-        return causal | (pos[None, :] >= L)
-    return causal
+        causal &= pos > qpos - W
+    r = K - 1 if future_keys else right_window
+    later = (pos > qpos) & (pos <= qpos + r)
+    return causal | later
 
 
 def dense_attention(q_bits, k_bits, v_bits, scale, mask):
@@ -98,13 +99,7 @@ def test_unwindowed_equals_dense_full_attention(oracle_mod, shape, K):
 @pytest.mark.parametrize("W", [0, 1, 3, 6, 50])
 @pytest.mark.parametrize("K", [1, 3, 4])
 def test_causal_block_equals_windowed_decode(oracle_mod, W, K):
-    """future_keys=0 (and K=1 in any form) is causal windowed decode, by position mask.
-
-    Only for W = 0 or W >= K: below that the causal window would drop block
-    keys the pages' non-causal definition keeps, and the library rejects it.
-    """
-    if 0 < W < K:
-        pytest.skip("0 < W < K is outside the defined range")
+    """future_keys=0 (and K=1 in any form) is causal windowed decode, by position mask."""
     rng = np.random.default_rng(200 + W * 5 + K)
     Hq, Hkv, D, P = 4, 2, 8, 4
     lens = [0, 2, 7, 23, 31]
@@ -133,6 +128,50 @@ def test_noncausal_window_equals_masked_dense(oracle_mod, W, K):
         ro, rl = dense_attention(q[b], dk[b], dv[b], 0.41, visible_mask(L, K, W, 1))
         np.testing.assert_allclose(out[b], ro, rtol=1e-11, atol=1e-12)
         np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("W", [0, 1, 2, 3, 9])
+@pytest.mark.parametrize("r", [0, 1, 2, 3])
+def test_right_window_equals_masked_dense(oracle_mod, W, r):
+    """A right window r: the causal window (L+i-W, L+i] plus block keys
+    L+i+1 .. L+i+r; with 0 < W < K the window also drops block keys."""
+    K = 4
+    rng = np.random.default_rng(310 + 10 * W + r)
+    Hq, Hkv, D, P = 4, 2, 8, 3
+    lens = [0, 1, 4, 13, 26]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    out, lse2 = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W, future_keys=0,
+                                      right_window=r, scale=0.53)
+    for b, L in enumerate(lens):
+        ro, rl = dense_attention(q[b], dk[b], dv[b], 0.53, visible_mask(L, K, W, 0, r))
+        np.testing.assert_allclose(out[b], ro, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
+    if r == K - 1:
+        full = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W, future_keys=1,
+                                     scale=0.53)
+        np.testing.assert_array_equal(full[0], out)
+        np.testing.assert_array_equal(full[1], lse2)
+
+
+def test_window_one_right_zero_is_own_key(oracle_mod):
+    """W = 1, r = 0: every row sees its own key only: out = v, lse2 = s/ln 2."""
+    import oracle
+
+    rng = np.random.default_rng(330)
+    K, Hq, Hkv, D, P = 3, 2, 1, 4, 2
+    lens = [0, 3, 8]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    out, lse2 = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=1, future_keys=0,
+                                      right_window=0, scale=0.25)
+    for b, L in enumerate(lens):
+        qf = oracle.bf16_bits_to_float(q[b]).astype(np.float64)
+        kf = oracle.bf16_bits_to_float(dk[b]).astype(np.float64)
+        vf = oracle.bf16_bits_to_float(dv[b]).astype(np.float64)
+        for i in range(K):
+            for hq in range(Hq):
+                np.testing.assert_array_equal(out[b, i, hq], vf[L + i, 0])
+                s = 0.25 * float(np.dot(qf[i, hq], kf[L + i, 0]))
+                assert abs(lse2[b, i, hq] - s / LN2) < 1e-12
 
 
 @pytest.mark.parametrize("W", [0, 5, 12])
@@ -323,7 +362,11 @@ def test_errors(oracle_mod):
 
 MUTANTS = [
     ("window off by one", "L + i - pr.W + 1", "L + i - pr.W"),
-    ("future keys include only j < i", "pr.future_keys ? pr.K : i + 1", "pr.future_keys ? pr.K : i"),
+    ("later keys skip the first", "for (int j = i + 1; j <= j_last; ++j)", "for (int j = i + 2; j <= j_last; ++j)"),
+    ("right window ignored", "const int r = pr.future_keys ? pr.K - 1 : pr.right_window;",
+     "const int r = pr.future_keys ? pr.K - 1 : 0;"),
+    ("causal window stops before the query", "for (int64_t p = lo; p <= L + i; ++p)",
+     "for (int64_t p = lo; p < L + i; ++p)"),
     ("wrong GQA head map", "const int h = hq / G;", "const int h = hq % pr.Hkv;"),
     ("page slot / offset swapped", "(p % pr.P)) * pr.D", "(p / pr.P) % pr.P) * pr.D"),
     ("scale dropped", "s[t] = pr.scale * acc;", "s[t] = acc;"),
@@ -339,16 +382,17 @@ def _pins_pass(lib) -> bool:
 
     rng = np.random.default_rng(1234)
     try:
-        for (Hq, Hkv, D, P, K, W, fk, lens) in [
-            (4, 2, 8, 4, 3, 0, 1, [0, 5, 14]),
-            (4, 2, 8, 4, 3, 5, 0, [2, 9, 20]),
-            (6, 3, 8, 3, 4, 6, 1, [1, 7, 25]),
+        for (Hq, Hkv, D, P, K, W, fk, rw, lens) in [
+            (4, 2, 8, 4, 3, 0, 1, 0, [0, 5, 14]),
+            (4, 2, 8, 4, 3, 5, 0, 0, [2, 9, 20]),
+            (6, 3, 8, 3, 4, 6, 1, 0, [1, 7, 25]),
+            (4, 2, 8, 4, 4, 2, 0, 2, [0, 6, 11]),
         ]:
             q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
             out, lse2 = oracle.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W,
-                                          future_keys=fk, scale=0.45, lib=lib)
+                                          future_keys=fk, right_window=rw, scale=0.45, lib=lib)
             for b, L in enumerate(lens):
-                ro, rl = dense_attention(q[b], dk[b], dv[b], 0.45, visible_mask(L, K, W, fk))
+                ro, rl = dense_attention(q[b], dk[b], dv[b], 0.45, visible_mask(L, K, W, fk, rw))
                 if not (np.allclose(out[b], ro, rtol=1e-10, atol=1e-11) and
                         np.allclose(lse2[b], rl, rtol=1e-10, atol=1e-11)):
                     return False
