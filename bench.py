@@ -13,8 +13,10 @@ call, outside its CUDA-event pair.
 Workloads (``--workload``): ``tiny``, ``minimax_B{B}_K{K}_L{L}`` (16/1 heads,
 D=128, W=4096, page 64), ``adp_B{B}_K{K}_L{L}`` (64/4 heads, 1 % key outliers),
 ``longctx_{8|12}x2_B{B}_L{L}`` (D=64, page 32, unwindowed),
-``ragged_B{B}`` (64/16 heads, contexts uniform in [1K, 128K]).  The default is
-the MiniMax-style windowed TP rank at its largest point: B=64, K=7, L=16384.
+``ragged_B{B}`` (64/16 heads, contexts uniform in [1K, 128K]); a suffix
+``_r{R}`` turns any of them into the causal block with a right window of R
+block keys.  The default is the MiniMax-style windowed TP rank at its largest
+point: B=64, K=7, L=16384.
 
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
 workload on the host cores (the slow baseline arm).
@@ -44,6 +46,12 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 def workload_spec(name: str, seed_offset: int = 0):
+    import dataclasses
+
+    m = re.fullmatch(r"(.+)_r(\d+)", name)
+    if m:
+        base = workload_spec(m[1], seed_offset)
+        return dataclasses.replace(base, name=name, future_keys=0, right_window=int(m[2]))
     from speculative_decoding_draft_paged_gb300 import workloads as W
 
     if name == "tiny":
@@ -198,6 +206,7 @@ def time_oracle_sample(spec, budget_s: float = 15.0, device_inputs=None):
         cost += per_req[b] / rate
     sub = W.CaseSpec(spec.name + "_sample", B=len(ids), Hq=spec.Hq, Hkv=spec.Hkv, D=spec.D, K=spec.K,
                      P=spec.P, window=spec.window, future_keys=spec.future_keys,
+                     right_window=spec.right_window,
                      ctx_lens=[spec.ctx_lens[b] for b in ids], sigma=spec.sigma,
                      outlier_frac=spec.outlier_frac, seed=spec.seed)
     inp = W.make_inputs(sub, "cpu")
@@ -209,7 +218,7 @@ def time_oracle_sample(spec, budget_s: float = 15.0, device_inputs=None):
             inp["ctx_lens"].numpy())
     t0 = time.perf_counter()
     oracle.block_attn(*args, block_size=sub.K, window=sub.window, future_keys=sub.future_keys,
-                      scale=sub.softmax_scale, nthreads=threads)
+                      right_window=sub.right_window, scale=sub.softmax_scale, nthreads=threads)
     dt = time.perf_counter() - t0
     desc = f"{len(ids)} of {spec.B} requests (same shapes and lengths), fp64, {threads} threads"
     return sub.kv_bytes() / dt, dt, len(ids), threads, desc
@@ -280,7 +289,8 @@ def main():
     inp = W.make_inputs(spec, dev)
     p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K,
                           window=spec.window, future_keys=spec.future_keys,
-                          scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len)
+                          scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len,
+                          right_window=spec.right_window)
     plan = dflash.plan(p)
     ws_bytes = dflash.workspace_size(p)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)

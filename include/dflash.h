@@ -16,7 +16,10 @@
  *     the block keys after i are folded in by a base-2 log-sum-exp merge,
  *     which is skipped exactly when no later key exists (K = 1, or the causal
  *     form);
- *   - the causal block (future_keys = 0): the causal (windowed) decode alone.
+ *   - the causal block (future_keys = 0): the causal (windowed) decode alone,
+ *     or with a right window r (right_window = r): the causal window plus the
+ *     next r block keys, which generalises both forms (r = K-1 is the
+ *     non-causal block); a window W < K bounds the block keys as well.
  * The softmax statistics are returned as base-2 LSE (PR #21130 change 1) and
  * the caller sizes a workspace that includes the partial softmax statistics
  * (PR #21130 change 3); sequence lengths stay on the device so one captured
@@ -72,14 +75,18 @@ typedef struct dflash_params {
   int32_t max_pages_per_req; /* row stride of page_table */
   int32_t num_pages;         /* pages in the K pool (and in the V pool) */
   int32_t block_size;        /* K draft tokens per request, 1..16; G*K <= 128 */
-  int32_t window;            /* W: 0 = unwindowed; W >= K = causal window (L+i-W, L+i] */
-  int32_t future_keys;       /* 1: non-causal block (all K block keys); 0: causal block */
+  int32_t window;            /* W: 0 = unwindowed; W > 0 = causal window (L+i-W, L+i],
+                                which also bounds the block keys when W < K */
+  int32_t future_keys;       /* 1: non-causal block (every later block key);
+                                0: causal block plus right_window later keys */
   float   scale;             /* softmax scale > 0, applied to q.k in fp32 */
   int32_t max_ctx_len;       /* host bound on every ctx_lens[b]; sizes the plan */
   int32_t force_path;        /* DFLASH_PATH_*; 0 picks by the packed row count */
   int32_t force_split_tiles; /* 1..64: key tiles per split unit, or per CTA range on
                                 the tcgen05 path (tests); 0 = planner */
-  int32_t reserved[4];       /* must be zero */
+  int32_t right_window;      /* with future_keys = 0: row i also sees block keys
+                                i+1 .. i+right_window (0 .. K-1); 0 when future_keys = 1 */
+  int32_t reserved[3];       /* must be zero */
 } dflash_params;
 
 /*

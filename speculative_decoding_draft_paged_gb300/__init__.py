@@ -37,7 +37,7 @@ class DflashError(RuntimeError):
 
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_req,
                 num_pages, block_size, window, future_keys, scale, max_ctx_len, force_path=0,
-                force_split_tiles=0) -> Params:
+                force_split_tiles=0, right_window=0) -> Params:
     p = Params()
     p.batch = batch
     p.num_q_heads = num_q_heads
@@ -53,11 +53,12 @@ def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pa
     p.max_ctx_len = max_ctx_len
     p.force_path = force_path
     p.force_split_tiles = force_split_tiles
+    p.right_window = right_window
     return p
 
 
 def params_for(q, k_pages, page_table, *, block_size, window, future_keys, scale, max_ctx_len,
-               force_path=0, force_split_tiles=0) -> Params:
+               force_path=0, force_split_tiles=0, right_window=0) -> Params:
     B, K, Hq, D = q.shape
     num_pages, Hkv, P, _ = k_pages.shape
     if K != block_size:
@@ -66,7 +67,7 @@ def params_for(q, k_pages, page_table, *, block_size, window, future_keys, scale
                        max_pages_per_req=page_table.shape[1], num_pages=num_pages,
                        block_size=block_size, window=window, future_keys=future_keys, scale=scale,
                        max_ctx_len=max_ctx_len, force_path=force_path,
-                       force_split_tiles=force_split_tiles)
+                       force_split_tiles=force_split_tiles, right_window=right_window)
 
 
 def workspace_size(p: Params) -> int:
@@ -111,7 +112,8 @@ def block_attn_timed_raw(p: Params, q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, ou
 
 def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size: int, window: int,
                future_keys: int, scale: float, max_ctx_len: int, out=None, lse2=None,
-               workspace=None, stream=None, force_path: int = 0, force_split_tiles: int = 0):
+               workspace=None, stream=None, force_path: int = 0, force_split_tiles: int = 0,
+               right_window: int = 0):
     """Draft-block attention over a paged bf16 KV cache.  Returns ``(out, lse2)``.
 
     ``q [B,K,Hq,D]`` bf16, ``k_pages``/``v_pages [num_pages,Hkv,P,D]`` bf16,
@@ -124,7 +126,8 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size: int, wi
 
     p = params_for(q, k_pages, page_table, block_size=block_size, window=window,
                    future_keys=future_keys, scale=scale, max_ctx_len=max_ctx_len,
-                   force_path=force_path, force_split_tiles=force_split_tiles)
+                   force_path=force_path, force_split_tiles=force_split_tiles,
+                   right_window=right_window)
     for name, t, dt in (("q", q, torch.bfloat16), ("k_pages", k_pages, torch.bfloat16),
                         ("v_pages", v_pages, torch.bfloat16), ("page_table", page_table, torch.int32),
                         ("ctx_lens", ctx_lens, torch.int32)):

@@ -56,7 +56,8 @@ class Params(ctypes.Structure):
         ("max_ctx_len", ctypes.c_int32),
         ("force_path", ctypes.c_int32),
         ("force_split_tiles", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("right_window", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 

@@ -76,8 +76,10 @@ bool params_valid(const dflash_params* p) {
   if (p->block_size < 1 || p->block_size > kMaxBlock) return false;
   const int64_t G = p->num_q_heads / p->num_kv_heads;
   if (G * p->block_size > kMaxRows) return false;
-  if (p->window < 0 || (p->window > 0 && p->window < p->block_size)) return false;
+  if (p->window < 0) return false;
   if (p->future_keys != 0 && p->future_keys != 1) return false;
+  if (p->right_window < 0 || p->right_window >= p->block_size) return false;
+  if (p->future_keys == 1 && p->right_window != 0) return false;
   if (!std::isfinite(p->scale) || !(p->scale > 0.f)) return false;
   // Positions are 32-bit on the device: keep L + K + a tile well inside int32.
   if (p->max_ctx_len < 0 || p->max_ctx_len > (1 << 30)) return false;
@@ -374,7 +376,7 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   a.num_pages = p->num_pages;
   a.K = p->block_size;
   a.W = p->window;
-  a.future_keys = p->future_keys;
+  a.rw = p->future_keys ? p->block_size - 1 : p->right_window;
   a.max_ctx_len = p->max_ctx_len;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.R = k.R;

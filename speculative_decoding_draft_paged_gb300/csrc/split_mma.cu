@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(MAXT, 1)
           if (lo < 0) lo = 0;
         }
         lo_r[e] = lo;
-        hi_r[e] = a.future_keys ? L + a.K : L + i + 1;
+        hi_r[e] = L + min(a.K, i + 1 + a.rw);
       } else {
         lo_r[e] = 0x7fffffff;
         hi_r[e] = -0x7fffffff;
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(MAXT, 1)
       lo_rows_max = L + a.K - a.W;
       if (lo_rows_max < 0) lo_rows_max = 0;
     }
-    const int hi_rows_min = a.future_keys ? L + a.K : L + 1;  // smallest row upper bound
+    const int hi_rows_min = L + min(a.K, 1 + a.rw);  // smallest row upper bound (row 0)
 
     float m_run[2] = {neg_inf(), neg_inf()};
     float l_run[2] = {0.f, 0.f};

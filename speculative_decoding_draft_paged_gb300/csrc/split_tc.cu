@@ -523,14 +523,14 @@ __global__ void __launch_bounds__(384, 1)
           lo_r = L + i_row - a.W + 1;
           if (lo_r < 0) lo_r = 0;
         }
-        hi_r = a.future_keys ? L + a.K : L + i_row + 1;
+        hi_r = L + min(a.K, i_row + 1 + a.rw);
       }
       int lo_rows_max = 0;
       if (a.W > 0) {
         lo_rows_max = L + a.K - a.W;
         if (lo_rows_max < 0) lo_rows_max = 0;
       }
-      const int hi_rows_min = a.future_keys ? L + a.K : L + 1;
+      const int hi_rows_min = L + min(a.K, 1 + a.rw);
       const int pos_base = (geo.t_begin - (sg.g0 - start)) * T;  // position of CTA tile 0, this pair
 
       float m_ref = ninf();

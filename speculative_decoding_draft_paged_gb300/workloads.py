@@ -44,8 +44,9 @@ class CaseSpec:
     K: int
     P: int
     window: int              # 0: unwindowed; W > 0: causal window (L+i-W, L+i]
-    future_keys: int         # 1: non-causal block; 0: causal block
+    future_keys: int         # 1: non-causal block; 0: causal block (+ right_window keys)
     ctx_lens: Sequence[int]  # context tokens before the block, per request
+    right_window: int = 0    # with future_keys = 0: later block keys each row sees
     sigma: float = 1.0
     outlier_frac: float = 0.0   # fraction of (token, kv head) key rows scaled by 8
     seed: int = 1001
@@ -96,6 +97,7 @@ class CaseSpec:
     def describe(self) -> dict:
         return {"workload": self.name, "B": self.B, "Hq": self.Hq, "Hkv": self.Hkv, "D": self.D,
                 "K": self.K, "page": self.P, "window": self.window, "future_keys": self.future_keys,
+                "right_window": self.right_window,
                 "ctx_min": min(self.ctx_lens), "ctx_max": max(self.ctx_lens), "sigma": self.sigma}
 
 

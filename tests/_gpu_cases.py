@@ -34,7 +34,8 @@ def run_lib(spec, inp, **kw):
     kw.setdefault("max_ctx_len", spec.max_ctx_len)
     return dflash.block_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"],
                              inp["ctx_lens"], block_size=spec.K, window=spec.window,
-                             future_keys=spec.future_keys, scale=spec.softmax_scale, **kw)
+                             future_keys=spec.future_keys, scale=spec.softmax_scale,
+                             right_window=spec.right_window, **kw)
 
 
 def run_oracle(spec, inp, req_ids=None, ctx_lens=None):
@@ -44,6 +45,7 @@ def run_oracle(spec, inp, req_ids=None, ctx_lens=None):
                                                                          torch.is_tensor(lens) else lens,
                                                                          dtype=np.int32),
                              block_size=spec.K, window=spec.window, future_keys=spec.future_keys,
+                             right_window=spec.right_window,
                              scale=spec.softmax_scale, req_ids=req_ids)
 
 

@@ -70,7 +70,9 @@ def base_params(**kw):
     dict(batch=0), dict(num_kv_heads=0), dict(num_q_heads=12, num_kv_heads=5),
     dict(head_dim=96), dict(head_dim=256), dict(page_size=8), dict(page_size=48),
     dict(block_size=0), dict(block_size=17), dict(num_q_heads=64, num_kv_heads=2, block_size=5),
-    dict(window=-1), dict(window=3), dict(future_keys=2), dict(scale=float("inf")),
+    dict(window=-1), dict(future_keys=2), dict(scale=float("inf")),
+    dict(future_keys=0, right_window=-1), dict(future_keys=0, right_window=7),
+    dict(future_keys=1, right_window=2),
     dict(scale=float("nan")), dict(scale=0.0), dict(scale=-0.125), dict(max_ctx_len=-1), dict(max_ctx_len=40 * 32 - 6),
     dict(num_pages=0), dict(force_path=3), dict(force_split_tiles=-1), dict(force_split_tiles=65),
 ])
@@ -93,7 +95,8 @@ def test_reserved_must_be_zero(dflash_lib):
 
 def test_boundary_params_accepted(dflash_lib):
     d = dflash_lib
-    for kw in [dict(max_ctx_len=40 * 32 - 7), dict(window=7), dict(window=4096),
+    for kw in [dict(max_ctx_len=40 * 32 - 7), dict(window=7), dict(window=4096), dict(window=3),
+               dict(window=1), dict(future_keys=0, right_window=6), dict(future_keys=0, right_window=2),
                dict(num_q_heads=128, num_kv_heads=8, block_size=8), dict(block_size=1, window=1),
                dict(head_dim=128, page_size=64, max_pages_per_req=30), dict(page_size=16,
                                                                             max_pages_per_req=90)]:

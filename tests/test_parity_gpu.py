@@ -86,6 +86,25 @@ def test_tcgen05_unit_tile_counts(cuda_device, n_tiles):
     check_case(spec, cuda_device, force_path=dflash.PATH_TCGEN05, force_split_tiles=n_tiles)
 
 
+@pytest.mark.parametrize("path", [dflash.PATH_MMA, dflash.PATH_TCGEN05])
+@pytest.mark.parametrize("win,r", [(0, 0), (0, 2), (0, 6), (300, 3), (3, 0), (3, 2), (1, 0), (5, 6)])
+def test_right_window(cuda_device, path, win, r):
+    """A right window r (row i sees block keys up to i+r) and windows shorter
+    than the block, on both kernels."""
+    lens = [0, 1, 6, 63, 64, 65, 700, 2049]
+    spec = W.CaseSpec(f"rw_W{win}_r{r}", B=len(lens), Hq=16, Hkv=1, D=128, K=7, P=64, window=win,
+                      future_keys=0, right_window=r, ctx_lens=lens, seed=41, poison=True)
+    check_case(spec, cuda_device, force_path=path)
+
+
+@pytest.mark.parametrize("win,r", [(0, 1), (2, 4)])
+def test_right_window_d64(cuda_device, win, r):
+    lens = [0, 3, 31, 32, 33, 1000]
+    spec = W.CaseSpec(f"rw64_W{win}_r{r}", B=len(lens), Hq=8, Hkv=2, D=64, K=5, P=32, window=win,
+                      future_keys=0, right_window=r, ctx_lens=lens, seed=42, poison=True)
+    check_case(spec, cuda_device)
+
+
 @pytest.mark.parametrize("kind", ["many_short", "one_long", "max_batch"])
 def test_tcgen05_flat_split_batches(cuda_device, kind):
     """The flat split over many pairs: ranges holding many whole pairs
