@@ -11,16 +11,21 @@ PR #21130 "Non-causal windowed DSpark draft block", description and change 2;
 PR #20374 "Non-causal unwindowed DFlash draft block", description):
 
 * query token ``i`` of request ``b`` (position ``L+i``, ``L = ctx_lens[b]``)
-  sees context positions ``[max(0, L+i-W+1), L)`` when ``window = W > 0``
-  (all of ``[0, L)`` when ``W = 0``) and block positions ``L+j`` for every
-  ``j < K`` (``future_keys=1``) or ``j <= i`` (``future_keys=0``);
+  sees the causal window ``(L+i-W, L+i]`` when ``window = W > 0`` (every
+  position up to ``L+i`` when ``W = 0``) plus the later block keys
+  ``L+j``, ``i < j <= i+r``, with ``r = K-1`` for ``future_keys=1`` and
+  ``r = right_window`` otherwise;
 * every key/value row is read through ``page_table`` from HND pages
   ``[num_pages, Hkv, P, D]``; query head ``hq`` reads kv head ``hq // G``;
 * ``out`` is the softmax-weighted mean of the visible values and ``lse2`` the
   base-2 log-sum-exp of ``scale * q.k`` over the visible keys.
 
+Also the block placement and the K/V append (the block's rows written into
+the pool slots of positions ``L .. L+K-1``), plain data movement.
+
 Pinned by ``tests/test_oracle_pins.py`` (dense brute force, causal decode,
-LSE merge of disjoint key sets, page-permutation invariance, closed forms).
+LSE merge of disjoint key sets, page-permutation invariance, closed forms,
+placement and append round trips).
 """
 
 from __future__ import annotations
@@ -61,6 +66,12 @@ def load_library(path: str):
     f.restype = ctypes.c_int
     i32, vp = ctypes.c_int, ctypes.c_void_p
     f.argtypes = [i32] * 11 + [ctypes.c_double] + [vp] * 6 + [i32] + [vp, vp, i32]
+    f = lib.oracle_block_placement
+    f.restype = ctypes.c_int
+    f.argtypes = [i32] * 5 + [vp] * 3
+    f = lib.oracle_append_block_kv
+    f.restype = ctypes.c_int
+    f.argtypes = [i32] * 7 + [vp] * 6
     return lib
 
 
@@ -110,6 +121,41 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window,
     if rc != 0:
         raise ValueError(f"oracle_block_attn failed with status {rc}")
     return out, lse2
+
+
+def block_placement(page_table, ctx_lens, *, block_size, page_size, num_pages, lib=None):
+    """int32 ``[B, K, 2]``: (page, offset) of block token j of request b, the
+    pool slot of logical position ``ctx_lens[b] + j``."""
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    ctx_lens = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    B, max_pages = page_table.shape
+    out = np.zeros((B, block_size, 2), dtype=np.int32)
+    rc = (lib or _load()).oracle_block_placement(B, block_size, page_size, max_pages, num_pages,
+                                                 _ptr(page_table), _ptr(ctx_lens), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_block_placement failed with status {rc}")
+    return out
+
+
+def append_block_kv(k_block, v_block, k_pages, v_pages, page_table, ctx_lens, lib=None):
+    """Copies of the pools with the block's K/V rows (uint16 bf16 bits
+    ``[B, K, Hkv, D]``) written at their placement."""
+    k_block = np.ascontiguousarray(k_block, dtype=np.uint16)
+    v_block = np.ascontiguousarray(v_block, dtype=np.uint16)
+    kp = np.array(k_pages, dtype=np.uint16, copy=True)
+    vp = np.array(v_pages, dtype=np.uint16, copy=True)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    ctx_lens = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    B, K, Hkv, D = k_block.shape
+    num_pages, Hkv2, P, D2 = kp.shape
+    if Hkv2 != Hkv or D2 != D or v_block.shape != k_block.shape or vp.shape != kp.shape:
+        raise ValueError("inconsistent shapes")
+    rc = (lib or _load()).oracle_append_block_kv(B, K, Hkv, D, P, page_table.shape[1], num_pages,
+                                                 _ptr(k_block), _ptr(v_block), _ptr(kp), _ptr(vp),
+                                                 _ptr(page_table), _ptr(ctx_lens))
+    if rc != 0:
+        raise ValueError(f"oracle_append_block_kv failed with status {rc}")
+    return kp, vp
 
 
 def bf16_bits_from_float(x) -> np.ndarray:

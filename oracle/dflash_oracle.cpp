@@ -164,4 +164,57 @@ int oracle_block_attn(int B, int Hq, int Hkv, int D, int P, int max_pages, int n
   return status.load();
 }
 
+// Block placement: the pool slot of every block token's K/V.  Block token j
+// of request b sits at logical position L_b + j (L_b = ctx_lens[b]), i.e. in
+// page page_table[b][(L_b + j) / P] at offset (L_b + j) % P (PR #20374: the
+// block's K/V are appended to the paged cache after the context; the fused
+// spec-tail kernels report these positions as the draft block placement).
+// placement[(b*K + j)*2 + 0] = page, [.. + 1] = offset.  Returns 0, -1 for bad
+// sizes, -2 for a negative length, -3 for a slot whose entry is not a page.
+int oracle_block_placement(int B, int K, int P, int max_pages, int num_pages,
+                           const int32_t* page_table, const int32_t* ctx_lens, int32_t* placement) {
+  if (B <= 0 || K <= 0 || P <= 0 || max_pages <= 0 || num_pages <= 0) return -1;
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = ctx_lens[b];
+    if (L < 0) return -2;
+    for (int j = 0; j < K; ++j) {
+      const int64_t p = L + j;
+      const int64_t slot = p / P;
+      if (slot >= max_pages) return -3;
+      const int32_t page = page_table[static_cast<int64_t>(b) * max_pages + slot];
+      if (page < 0 || page >= num_pages) return -3;
+      placement[(static_cast<int64_t>(b) * K + j) * 2 + 0] = page;
+      placement[(static_cast<int64_t>(b) * K + j) * 2 + 1] = static_cast<int32_t>(p % P);
+    }
+  }
+  return 0;
+}
+
+// K/V append: copies the block's rows k_block[b][j][h][:], v_block[b][j][h][:]
+// (bf16 bits, [B, K, Hkv, D]) into the pool rows of its placement,
+// k_pages[page][h][offset][:] and likewise V.  Every other pool row is left as
+// it was.  Same return codes as oracle_block_placement.
+int oracle_append_block_kv(int B, int K, int Hkv, int D, int P, int max_pages, int num_pages,
+                           const uint16_t* k_block, const uint16_t* v_block, uint16_t* k_pages,
+                           uint16_t* v_pages, const int32_t* page_table, const int32_t* ctx_lens) {
+  std::vector<int32_t> place(static_cast<size_t>(B) * K * 2);
+  const int rc = oracle_block_placement(B, K, P, max_pages, num_pages, page_table, ctx_lens,
+                                        place.data());
+  if (rc != 0) return rc;
+  for (int b = 0; b < B; ++b)
+    for (int j = 0; j < K; ++j) {
+      const int64_t page = place[(static_cast<int64_t>(b) * K + j) * 2 + 0];
+      const int64_t off = place[(static_cast<int64_t>(b) * K + j) * 2 + 1];
+      for (int h = 0; h < Hkv; ++h) {
+        const int64_t src = ((static_cast<int64_t>(b) * K + j) * Hkv + h) * D;
+        const int64_t dst = ((page * Hkv + h) * P + off) * D;
+        for (int d = 0; d < D; ++d) {
+          k_pages[dst + d] = k_block[src + d];
+          v_pages[dst + d] = v_block[src + d];
+        }
+      }
+    }
+  return 0;
+}
+
 }  // extern "C"

@@ -337,6 +337,83 @@ def test_hand_derived_fixture(oracle_mod, path):
 
 
 # ----------------------------------------------------------------------------
+# Block placement and K/V append (plain data movement)
+# ----------------------------------------------------------------------------
+
+def _tagged_case(rng, lens, K, Hkv, D, P):
+    """Dense K/V whose rows carry their (request, position) in the first two
+    columns (exact small integers in bf16), scattered into shuffled pages."""
+    import oracle
+
+    dk, dv = [], []
+    for b, L in enumerate(lens):
+        k = random_bf16(rng, (L + K, Hkv, D), 1.0)
+        v = random_bf16(rng, (L + K, Hkv, D), 1.0)
+        pos = np.arange(L + K, dtype=np.float32)
+        k[:, :, 0] = oracle.bf16_bits_from_float(np.broadcast_to(pos[:, None], (L + K, Hkv)))
+        k[:, :, 1] = oracle.bf16_bits_from_float(np.float32(b))
+        dk.append(k)
+        dv.append(v)
+    kp, vp, tab = scatter_to_pages(rng, dk, dv, P, Hkv, D, extra_pages=3, extra_slots=2)
+    return dk, dv, kp, vp, tab
+
+
+@pytest.mark.parametrize("P", [1, 3, 4, 16])
+def test_block_placement_points_at_the_block_rows(oracle_mod, P):
+    rng = np.random.default_rng(960 + P)
+    K, Hkv, D = 5, 2, 8
+    lens = [0, 1, P - 1 if P > 1 else 2, P, 2 * P + 3, 37]
+    dk, dv, kp, vp, tab = _tagged_case(rng, lens, K, Hkv, D, P)
+    pl = oracle_mod.block_placement(tab, np.asarray(lens, np.int32), block_size=K, page_size=P,
+                                    num_pages=kp.shape[0])
+    for b, L in enumerate(lens):
+        for j in range(K):
+            page, off = pl[b, j]
+            np.testing.assert_array_equal(kp[page, :, off, :], dk[b][L + j])
+
+
+def test_append_then_gather_is_the_dense_sequence(oracle_mod):
+    """Pages holding the context only, then the append: reading every position
+    through the table gives context + block, and no other row changes."""
+    rng = np.random.default_rng(970)
+    K, Hkv, D, P = 4, 2, 8, 3
+    lens = [0, 2, 3, 7, 11]
+    dk, dv, kp_full, vp_full, tab = _tagged_case(rng, lens, K, Hkv, D, P)
+    kp, vp = kp_full.copy(), vp_full.copy()
+    kb = np.zeros((len(lens), K, Hkv, D), np.uint16)
+    vb = np.zeros_like(kb)
+    for b, L in enumerate(lens):          # blank the block rows, keep them aside
+        kb[b], vb[b] = dk[b][L:], dv[b][L:]
+        for p in range(L, L + K):
+            kp[tab[b, p // P], :, p % P, :] = 0x7FC0
+            vp[tab[b, p // P], :, p % P, :] = 0x7FC0
+    ka, va = oracle_mod.append_block_kv(kb, vb, kp, vp, tab, np.asarray(lens, np.int32))
+    np.testing.assert_array_equal(ka, kp_full)
+    np.testing.assert_array_equal(va, vp_full)
+    np.testing.assert_array_equal(kp[tab[0, 0], :, 0, :], np.full((Hkv, D), 0x7FC0, np.uint16))
+
+
+def test_append_then_attention_equals_dense(oracle_mod):
+    rng = np.random.default_rng(980)
+    K, Hq, Hkv, D, P = 3, 4, 2, 8, 4
+    lens = [0, 5, 14]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    kb = np.stack([dk[b][L:] for b, L in enumerate(lens)])
+    vb = np.stack([dv[b][L:] for b, L in enumerate(lens)])
+    for b, L in enumerate(lens):          # overwrite the block rows with garbage first
+        for p in range(L, L + K):
+            kp[tab[b, p // P], :, p % P, :] = 0x3F80
+            vp[tab[b, p // P], :, p % P, :] = 0x3F80
+    ka, va = oracle_mod.append_block_kv(kb, vb, kp, vp, tab, ctx)
+    out, lse2 = oracle_mod.block_attn(q, ka, va, tab, ctx, block_size=K, window=0, future_keys=1,
+                                      scale=0.4)
+    for b, L in enumerate(lens):
+        ro, rl = dense_attention(q[b], dk[b], dv[b], 0.4, np.ones((K, L + K), dtype=bool))
+        np.testing.assert_allclose(out[b], ro, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
 # Errors
 # ----------------------------------------------------------------------------
 
@@ -373,6 +450,13 @@ MUTANTS = [
     ("natural-log LSE", "/ std::log(2.0)", "/ 1.0"),
     ("max not subtracted in numerator", "const double w = std::exp(s[t] - m);",
      "const double w = std::exp(s[t]);"),
+]
+
+# Planted mistakes in the placement / append, each caught by a pin above.
+MOVE_MUTANTS = [
+    ("placement offset off by one", "static_cast<int32_t>(p % P);", "static_cast<int32_t>((p + 1) % P);"),
+    ("placement from the context end", "const int64_t p = L + j;", "const int64_t p = L + j - 1;"),
+    ("append writes K into V", "v_pages[dst + d] = v_block[src + d];", "v_pages[dst + d] = k_block[src + d];"),
 ]
 
 
@@ -423,3 +507,47 @@ def test_pins_reject_planted_mistakes(oracle_mod, tmp_path):
                        check=True)
         lib = oracle.load_library(so)
         assert not _pins_pass(lib), f"planted mistake not caught: {name}"
+
+
+def _move_pins_pass(lib) -> bool:
+    import oracle
+
+    try:
+        rng = np.random.default_rng(990)
+        K, Hkv, D, P = 4, 2, 8, 3
+        lens = [0, 2, 5, 9]
+        dk, dv, kp_full, vp_full, tab = _tagged_case(rng, lens, K, Hkv, D, P)
+        pl = oracle.block_placement(tab, np.asarray(lens, np.int32), block_size=K, page_size=P,
+                                    num_pages=kp_full.shape[0], lib=lib)
+        for b, L in enumerate(lens):
+            for j in range(K):
+                if not np.array_equal(kp_full[pl[b, j, 0], :, pl[b, j, 1], :], dk[b][L + j]):
+                    return False
+        kb = np.stack([dk[b][L:] for b, L in enumerate(lens)])
+        vb = np.stack([dv[b][L:] for b, L in enumerate(lens)])
+        ka, va = oracle.append_block_kv(kb, vb, kp_full * 0, vp_full * 0, tab,
+                                        np.asarray(lens, np.int32), lib=lib)
+        for b, L in enumerate(lens):
+            for p in range(L, L + K):
+                pg = tab[b, p // P]
+                if not (np.array_equal(ka[pg, :, p % P], dk[b][p]) and
+                        np.array_equal(va[pg, :, p % P], dv[b][p])):
+                    return False
+    except ValueError:
+        return False
+    return True
+
+
+def test_move_pins_reject_planted_mistakes(oracle_mod, tmp_path):
+    import oracle
+
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "dflash_oracle.cpp")).read()
+    assert _move_pins_pass(oracle._load())
+    for name, old, new in MOVE_MUTANTS:
+        assert src.count(old) == 1, name
+        path = tmp_path / (name.replace(" ", "_") + ".cpp")
+        path.write_text(src.replace(old, new))
+        so = str(path) + ".so"
+        subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-pthread", str(path), "-o", so],
+                       check=True)
+        assert not _move_pins_pass(oracle.load_library(so)), f"planted mistake not caught: {name}"
