@@ -261,6 +261,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-append", action="store_true",
+                    help="time dflash_block_attn_append: the block's K/V append to the pages "
+                         "followed by the attention in one launch sequence")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -299,11 +302,31 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    if args.fused_append:
+        # The block's own K/V rows (already in the pages from the input
+        # recipe): re-appending them each call leaves the pools unchanged.
+        kb = torch.empty((spec.B, spec.K, spec.Hkv, spec.D), dtype=torch.bfloat16, device=dev)
+        vb = torch.empty_like(kb)
+        tab = inp["page_table"].cpu()
+        for b, L in enumerate(spec.ctx_lens):
+            for j in range(spec.K):
+                pg, off = int(tab[b, (L + j) // spec.P]), (L + j) % spec.P
+                kb[b, j] = inp["k_pages"][pg, :, off, :]
+                vb[b, j] = inp["v_pages"][pg, :, off, :]
+
     def call():
-        rc = dflash.block_attn_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
-                                   inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(),
-                                   inp["ctx_lens"].data_ptr(), out.data_ptr(), lse.data_ptr(),
-                                   ws.data_ptr(), ws_bytes, torch.cuda.current_stream().cuda_stream)
+        if args.fused_append:
+            rc = dflash.block_attn_append_raw(
+                p, inp["q"].data_ptr(), kb.data_ptr(), vb.data_ptr(), inp["k_pages"].data_ptr(),
+                inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(), inp["ctx_lens"].data_ptr(),
+                out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws_bytes,
+                torch.cuda.current_stream().cuda_stream)
+        else:
+            rc = dflash.block_attn_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
+                                       inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(),
+                                       inp["ctx_lens"].data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                       ws.data_ptr(), ws_bytes,
+                                       torch.cuda.current_stream().cuda_stream)
         if rc != 0:
             raise dflash.DflashError(rc)
 
@@ -412,7 +435,8 @@ def main():
         "config": dict(spec.describe(), parallelism=f"replicas{world}",
                        l2="flushed before every timed call (512 MiB write)",
                        kv_bytes_per_call=kv_bytes, path=kernel, split_tiles=plan["split_tiles"],
-                       max_splits=plan["max_splits"], ctas=plan["units"], cuda_graph=True),
+                       max_splits=plan["max_splits"], ctas=plan["units"], cuda_graph=True,
+                       fused_append=bool(args.fused_append)),
         "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": split_gbs / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": kernel, "kernel_us": split_ms * 1e3,
@@ -421,7 +445,10 @@ def main():
                      if peaks["source"] == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,
+        # Per call: [append] + split kernel + combine (tcgen05 path, or several
+        # units per request on the mma path).
+        "gpu_launches": args.steps * (int(bool(args.fused_append)) + 1 +
+                                      int(kernel == "split_tc" or plan["max_splits"] > 1)),
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }

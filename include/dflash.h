@@ -197,6 +197,50 @@ int dflash_block_attn_static_ws(const dflash_params* p, const void* q, const voi
                                 const void* v_pages, const int32_t* page_table,
                                 const int32_t* ctx_lens, void* out, float* lse2, void* stream);
 
+/*
+ * Block placement: the pool slot of every block token's K/V.  Block token j
+ * of request b sits at logical position L_b + j, i.e. page
+ * page_table[b][(L_b + j) / P] at offset (L_b + j) % P (PR #20374: the
+ * block's K/V are appended to the paged cache after the context; the fused
+ * spec-tail kernels of the drafter report these positions as the draft block
+ * placement).
+ *   placement  int32 [B, K, 2], device: (page id, offset) per block token;
+ *              page id -1 where the table entry is not a page of the pool.
+ *   workspace  NULL, or a workspace whose status word receives
+ *              DFLASH_STATUS_BAD_PAGE / DFLASH_STATUS_BAD_CTX_LEN.
+ * ctx_lens outside [0, max_ctx_len] are clamped as in dflash_block_attn.
+ * Stream-ordered, no allocation.  Returns DFLASH_OK, DFLASH_ERR_INVALID,
+ * DFLASH_ERR_DEVICE or DFLASH_ERR_LAUNCH.
+ */
+int dflash_block_placement(const dflash_params* p, const int32_t* page_table,
+                           const int32_t* ctx_lens, int32_t* placement, void* workspace,
+                           void* stream);
+
+/*
+ * K/V append: writes the block's K and V rows, k_block / v_block bf16
+ * [B, K, Hkv, D] (token-major, like q), into the pool rows of their
+ * placement, k_pages[page][h][offset][:] and likewise V.  Rows whose page id
+ * is not a page of the pool are skipped (and flagged when `workspace` is
+ * given).  Every other pool row is untouched.  All pointers 16-byte aligned
+ * (tables 4-byte); same return codes as dflash_block_placement.
+ */
+int dflash_append_block_kv(const dflash_params* p, const void* k_block, const void* v_block,
+                           void* k_pages, void* v_pages, const int32_t* page_table,
+                           const int32_t* ctx_lens, void* workspace, void* stream);
+
+/*
+ * The K/V append followed by the attention in one launch sequence: the split
+ * kernel is launched as a programmatic dependent of the append kernel, so
+ * its prologue (length prefix, page lookups, query load) overlaps the
+ * append and its producers read the pages once the append has finished.
+ * Arguments as dflash_append_block_kv and dflash_block_attn (workspace
+ * required); the result equals dflash_append_block_kv then dflash_block_attn.
+ */
+int dflash_block_attn_append(const dflash_params* p, const void* q, const void* k_block,
+                             const void* v_block, void* k_pages, void* v_pages,
+                             const int32_t* page_table, const int32_t* ctx_lens, void* out,
+                             float* lse2, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static text for a return code. */
 const char* dflash_status_string(int status);
 

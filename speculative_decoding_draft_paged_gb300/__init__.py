@@ -23,6 +23,7 @@ from ._lib import (DFLASH_ERR_DEVICE, DFLASH_ERR_INVALID, DFLASH_ERR_LAUNCH, DFL
 __all__ = [
     "Params", "PlanInfo", "DflashError", "make_params", "workspace_size", "plan", "block_attn",
     "block_attn_raw", "block_attn_timed_raw", "read_device_status", "clear_device_status", "version", "PATH_AUTO",
+    "block_placement", "append_block_kv", "block_attn_append", "block_attn_append_raw",
     "PATH_MMA", "PATH_TCGEN05", "DFLASH_OK", "DFLASH_ERR_INVALID", "DFLASH_ERR_WORKSPACE",
     "DFLASH_ERR_DEVICE", "DFLASH_ERR_LAUNCH", "DFLASH_STATUS_BAD_PAGE",
     "DFLASH_STATUS_BAD_CTX_LEN", "DFLASH_STATUS_TIMEOUT",
@@ -148,6 +149,97 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size: int, wi
                         page_table.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
                         lse2.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                         _stream_handle(stream))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+    return out, lse2
+
+
+def _check_block(name, t, q_like):
+    import torch
+
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    if tuple(t.shape) != tuple(q_like):
+        raise ValueError(f"{name} must have shape {tuple(q_like)}")
+
+
+def _params_from_pool(k_pages, page_table, ctx_lens, *, block_size, max_ctx_len, Hq=None):
+    num_pages, Hkv, P, D = k_pages.shape
+    B = ctx_lens.shape[0]
+    return make_params(batch=B, num_q_heads=Hq or Hkv, num_kv_heads=Hkv, head_dim=D, page_size=P,
+                       max_pages_per_req=page_table.shape[1], num_pages=num_pages,
+                       block_size=block_size, window=0, future_keys=1, scale=1.0,
+                       max_ctx_len=max_ctx_len)
+
+
+def block_placement(page_table, ctx_lens, k_pages, *, block_size: int, max_ctx_len: int,
+                    workspace=None, stream=None):
+    """int32 ``[B, K, 2]`` (page, offset) of every block token's K/V slot."""
+    import torch
+
+    p = _params_from_pool(k_pages, page_table, ctx_lens, block_size=block_size,
+                          max_ctx_len=max_ctx_len)
+    placement = torch.empty((ctx_lens.shape[0], block_size, 2), dtype=torch.int32,
+                            device=page_table.device)
+    rc = int(_lib.load().dflash_block_placement(
+        ctypes.byref(p), page_table.data_ptr(), ctx_lens.data_ptr(), placement.data_ptr(),
+        workspace.data_ptr() if workspace is not None else None, _stream_handle(stream)))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+    return placement
+
+
+def append_block_kv(k_block, v_block, k_pages, v_pages, page_table, ctx_lens, *, max_ctx_len: int,
+                    workspace=None, stream=None):
+    """Write the block's K/V rows ``[B, K, Hkv, D]`` into their page slots, in place."""
+    B, K, Hkv, D = k_block.shape
+    _check_block("k_block", k_block, (B, K, Hkv, D))
+    _check_block("v_block", v_block, (B, K, Hkv, D))
+    p = _params_from_pool(k_pages, page_table, ctx_lens, block_size=K, max_ctx_len=max_ctx_len)
+    rc = int(_lib.load().dflash_append_block_kv(
+        ctypes.byref(p), k_block.data_ptr(), v_block.data_ptr(), k_pages.data_ptr(),
+        v_pages.data_ptr(), page_table.data_ptr(), ctx_lens.data_ptr(),
+        workspace.data_ptr() if workspace is not None else None, _stream_handle(stream)))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+
+
+def block_attn_append_raw(p: Params, q_ptr, kb_ptr, vb_ptr, k_ptr, v_ptr, table_ptr, lens_ptr,
+                          out_ptr, lse_ptr, ws_ptr, ws_bytes, stream_handle) -> int:
+    """Direct C-ABI call of the fused append + attention; returns the status code."""
+    return int(_lib.load().dflash_block_attn_append(ctypes.byref(p), q_ptr, kb_ptr, vb_ptr, k_ptr,
+                                                    v_ptr, table_ptr, lens_ptr, out_ptr, lse_ptr,
+                                                    ws_ptr, ws_bytes, stream_handle))
+
+
+def block_attn_append(q, k_block, v_block, k_pages, v_pages, page_table, ctx_lens, *,
+                      block_size: int, window: int, future_keys: int, scale: float,
+                      max_ctx_len: int, out=None, lse2=None, workspace=None, stream=None,
+                      force_path: int = 0, right_window: int = 0):
+    """Append the block's K/V to the pages, then the attention (one launch
+    sequence).  Returns ``(out, lse2)``; the pools are updated in place."""
+    import torch
+
+    B, K, Hq, D = q.shape
+    _check_block("k_block", k_block, (B, K, k_pages.shape[1], D))
+    _check_block("v_block", v_block, (B, K, k_pages.shape[1], D))
+    p = params_for(q, k_pages, page_table, block_size=block_size, window=window,
+                   future_keys=future_keys, scale=scale, max_ctx_len=max_ctx_len,
+                   force_path=force_path, right_window=right_window)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse2 is None:
+        lse2 = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    need = workspace_size(p)
+    if need == 0:
+        raise DflashError(DFLASH_ERR_INVALID)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    rc = block_attn_append_raw(p, q.data_ptr(), k_block.data_ptr(), v_block.data_ptr(),
+                               k_pages.data_ptr(), v_pages.data_ptr(), page_table.data_ptr(),
+                               ctx_lens.data_ptr(), out.data_ptr(), lse2.data_ptr(),
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _stream_handle(stream))
     if rc != DFLASH_OK:
         raise DflashError(rc)
     return out, lse2

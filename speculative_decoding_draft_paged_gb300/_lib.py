@@ -33,6 +33,9 @@ EXPORTS = (
     "dflash_block_attn",
     "dflash_block_attn_timed",
     "dflash_block_attn_static_ws",
+    "dflash_block_placement",
+    "dflash_append_block_kv",
+    "dflash_block_attn_append",
     "dflash_status_string",
     "dflash_read_device_status",
     "dflash_clear_device_status",
@@ -108,6 +111,13 @@ def load() -> ctypes.CDLL:
             lib.dflash_block_attn_timed.restype = i32
             lib.dflash_block_attn_static_ws.argtypes = [ctypes.POINTER(Params)] + [vp] * 8
             lib.dflash_block_attn_static_ws.restype = i32
+            lib.dflash_block_placement.argtypes = [ctypes.POINTER(Params)] + [vp] * 5
+            lib.dflash_block_placement.restype = i32
+            lib.dflash_append_block_kv.argtypes = [ctypes.POINTER(Params)] + [vp] * 8
+            lib.dflash_append_block_kv.restype = i32
+            lib.dflash_block_attn_append.argtypes = [ctypes.POINTER(Params)] + [vp] * 10 + \
+                [ctypes.c_size_t, vp]
+            lib.dflash_block_attn_append.restype = i32
             lib.dflash_status_string.argtypes = [i32]
             lib.dflash_status_string.restype = ctypes.c_char_p
             lib.dflash_read_device_status.argtypes = [vp, vp]

@@ -289,49 +289,52 @@ bool encode_partials(CUtensorMap* map, void* part_o, const dflash_params* p, int
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-}  // namespace
-}  // namespace dflash
-
-using namespace dflash;
-
-extern "C" {
-
-size_t dflash_workspace_size(const dflash_params* p) {
-  KernelPlan k;
-  if (!make_plan(p, plan_sms(), &k)) return 0;
-  return workspace_bytes_for(p, k);
-}
-
-int dflash_plan(const dflash_params* p, dflash_plan_info* info) {
-  KernelPlan k;
-  if (info == nullptr || !make_plan(p, plan_sms(), &k)) return DFLASH_ERR_INVALID;
-  std::memset(info, 0, sizeof(*info));
-  info->path = k.path;
-  info->rows = k.R;
-  info->rows_padded = k.R_pad;
-  info->tile_keys = k.T;
-  info->split_tiles = k.C;
-  info->max_splits = k.S;
-  info->units = k.units;
-  info->threads = k.threads;
-  info->smem_bytes = k.smem_bytes;
-  info->num_sms = k.num_sms;
+// Device check shared by the entry points.
+int check_device() {
+  const DeviceInfo dev = current_device();
+  if (!dev.ok) return DFLASH_ERR_LAUNCH;
+  if (dev.cc != 103) return DFLASH_ERR_DEVICE;
   return DFLASH_OK;
 }
 
-int dflash_block_attn(const dflash_params* p, const void* q, const void* k_pages,
-                      const void* v_pages, const int32_t* page_table, const int32_t* ctx_lens,
-                      void* out, float* lse2, void* workspace, size_t workspace_bytes,
-                      void* stream) {
-  return dflash_block_attn_timed(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2,
-                                 workspace, workspace_bytes, stream, nullptr, nullptr);
+bool append_pointers_ok(const void* k_block, const void* v_block, const void* k_pages,
+                        const void* v_pages, const int32_t* page_table, const int32_t* ctx_lens,
+                        const void* workspace) {
+  if (!k_block || !v_block || !k_pages || !v_pages || !page_table || !ctx_lens) return false;
+  return aligned(k_block, 16) && aligned(v_block, 16) && aligned(k_pages, 16) &&
+         aligned(v_pages, 16) && aligned(page_table, 4) && aligned(ctx_lens, 4) &&
+         (workspace == nullptr || aligned(workspace, 256));
 }
 
-int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k_pages,
-                            const void* v_pages, const int32_t* page_table,
-                            const int32_t* ctx_lens, void* out, float* lse2, void* workspace,
-                            size_t workspace_bytes, void* stream, void* split_start,
-                            void* split_done) {
+AppendArgs append_args(const dflash_params* p, const void* k_block, const void* v_block,
+                       void* k_pages, void* v_pages, const int32_t* page_table,
+                       const int32_t* ctx_lens, void* workspace) {
+  AppendArgs ap{};
+  ap.k_block = static_cast<const uint16_t*>(k_block);
+  ap.v_block = static_cast<const uint16_t*>(v_block);
+  ap.k_pages = static_cast<uint16_t*>(k_pages);
+  ap.v_pages = static_cast<uint16_t*>(v_pages);
+  ap.page_table = page_table;
+  ap.ctx_lens = ctx_lens;
+  ap.placement = nullptr;
+  ap.status = static_cast<uint32_t*>(workspace);
+  ap.B = p->batch;
+  ap.K = p->block_size;
+  ap.Hkv = p->num_kv_heads;
+  ap.D = p->head_dim;
+  ap.P = p->page_size;
+  ap.max_pages = p->max_pages_per_req;
+  ap.num_pages = p->num_pages;
+  ap.max_ctx_len = p->max_ctx_len;
+  return ap;
+}
+
+// The attention call; with `append` given, the K/V append runs first and the
+// split kernel is its programmatic dependent (its producers wait for it).
+int run_attention(const dflash_params* p, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* page_table, const int32_t* ctx_lens, void* out, float* lse2,
+                  void* workspace, size_t workspace_bytes, void* stream, void* split_start,
+                  void* split_done, const AppendArgs* append) {
   if (!params_valid(p)) return DFLASH_ERR_INVALID;
   if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !out || !lse2 || !workspace)
     return DFLASH_ERR_INVALID;
@@ -345,6 +348,7 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   KernelPlan k;
   if (!make_plan(p, dev.sms, &k)) return DFLASH_ERR_INVALID;
   if (workspace_bytes < workspace_bytes_for(p, k)) return DFLASH_ERR_WORKSPACE;
+  k.pdl = append != nullptr;
 
   const bool tc = k.path == DFLASH_PATH_TCGEN05;
   CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_part;
@@ -393,6 +397,7 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
   if (split_start != nullptr &&
       cudaEventRecord(static_cast<cudaEvent_t>(split_start), s) != cudaSuccess)
     return DFLASH_ERR_LAUNCH;
+  if (append != nullptr && launch_append(*append, s) != cudaSuccess) return DFLASH_ERR_LAUNCH;
   int err = tc ? launch_split_tc(a, k, tm_k, tm_v, tm_q, tm_out, tm_part, s)
                : launch_split_mma(a, k, tm_k, tm_v, s);
   if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
@@ -407,6 +412,95 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
     if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
   }
   return DFLASH_OK;
+}
+
+}  // namespace
+}  // namespace dflash
+
+using namespace dflash;
+
+extern "C" {
+
+size_t dflash_workspace_size(const dflash_params* p) {
+  KernelPlan k;
+  if (!make_plan(p, plan_sms(), &k)) return 0;
+  return workspace_bytes_for(p, k);
+}
+
+int dflash_plan(const dflash_params* p, dflash_plan_info* info) {
+  KernelPlan k;
+  if (info == nullptr || !make_plan(p, plan_sms(), &k)) return DFLASH_ERR_INVALID;
+  std::memset(info, 0, sizeof(*info));
+  info->path = k.path;
+  info->rows = k.R;
+  info->rows_padded = k.R_pad;
+  info->tile_keys = k.T;
+  info->split_tiles = k.C;
+  info->max_splits = k.S;
+  info->units = k.units;
+  info->threads = k.threads;
+  info->smem_bytes = k.smem_bytes;
+  info->num_sms = k.num_sms;
+  return DFLASH_OK;
+}
+
+int dflash_block_attn(const dflash_params* p, const void* q, const void* k_pages,
+                      const void* v_pages, const int32_t* page_table, const int32_t* ctx_lens,
+                      void* out, float* lse2, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return dflash_block_attn_timed(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2,
+                                 workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k_pages,
+                            const void* v_pages, const int32_t* page_table,
+                            const int32_t* ctx_lens, void* out, float* lse2, void* workspace,
+                            size_t workspace_bytes, void* stream, void* split_start,
+                            void* split_done) {
+  return run_attention(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2, workspace,
+                       workspace_bytes, stream, split_start, split_done, nullptr);
+}
+
+int dflash_block_placement(const dflash_params* p, const int32_t* page_table,
+                           const int32_t* ctx_lens, int32_t* placement, void* workspace,
+                           void* stream) {
+  if (!params_valid(p) || !page_table || !ctx_lens || !placement) return DFLASH_ERR_INVALID;
+  if (!aligned(page_table, 4) || !aligned(ctx_lens, 4) || !aligned(placement, 4) ||
+      (workspace != nullptr && !aligned(workspace, 256)))
+    return DFLASH_ERR_INVALID;
+  const int rc = check_device();
+  if (rc != DFLASH_OK) return rc;
+  AppendArgs ap = append_args(p, nullptr, nullptr, nullptr, nullptr, page_table, ctx_lens, workspace);
+  ap.placement = placement;
+  return launch_append(ap, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFLASH_OK
+                                                                             : DFLASH_ERR_LAUNCH;
+}
+
+int dflash_append_block_kv(const dflash_params* p, const void* k_block, const void* v_block,
+                           void* k_pages, void* v_pages, const int32_t* page_table,
+                           const int32_t* ctx_lens, void* workspace, void* stream) {
+  if (!params_valid(p) || !append_pointers_ok(k_block, v_block, k_pages, v_pages, page_table,
+                                              ctx_lens, workspace))
+    return DFLASH_ERR_INVALID;
+  const int rc = check_device();
+  if (rc != DFLASH_OK) return rc;
+  const AppendArgs ap =
+      append_args(p, k_block, v_block, k_pages, v_pages, page_table, ctx_lens, workspace);
+  return launch_append(ap, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFLASH_OK
+                                                                             : DFLASH_ERR_LAUNCH;
+}
+
+int dflash_block_attn_append(const dflash_params* p, const void* q, const void* k_block,
+                             const void* v_block, void* k_pages, void* v_pages,
+                             const int32_t* page_table, const int32_t* ctx_lens, void* out,
+                             float* lse2, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!params_valid(p) || workspace == nullptr ||
+      !append_pointers_ok(k_block, v_block, k_pages, v_pages, page_table, ctx_lens, workspace))
+    return DFLASH_ERR_INVALID;
+  const AppendArgs ap =
+      append_args(p, k_block, v_block, k_pages, v_pages, page_table, ctx_lens, workspace);
+  return run_attention(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2, workspace,
+                       workspace_bytes, stream, nullptr, nullptr, &ap);
 }
 
 const char* dflash_status_string(int status) {

@@ -103,10 +103,43 @@ struct KernelPlan {
   int threads, smem_bytes;
   int kpw;          // mma path: keys per warp per tile
   int seg_cost;     // tcgen05 path: cost units of a segment's end
+  bool pdl;         // launch the split kernel as a programmatic dependent of the
+                    // preceding kernel (its producers wait before the first K/V load)
   int num_sms;
 };
 
+// Block placement / K/V append (append.cu).
+struct AppendArgs {
+  const uint16_t* k_block;    // bf16 [B, K, Hkv, D], or null: placement only
+  const uint16_t* v_block;
+  uint16_t* k_pages;          // bf16 [num_pages, Hkv, P, D]
+  uint16_t* v_pages;
+  const int32_t* page_table;  // [B, max_pages]
+  const int32_t* ctx_lens;    // [B]
+  int32_t* placement;         // [B, K, 2] (page, offset), or null
+  uint32_t* status;           // workspace status word, or null
+  int B, K, Hkv, D, P, max_pages, num_pages, max_ctx_len;
+};
+
+// Kernel launch with an optional programmatic-dependent-launch attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Launchers (defined in the .cu files).  Return a cudaError_t value.
+int launch_append(const AppendArgs& a, cudaStream_t stream);
 int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
                      const CUtensorMap& tm_v, cudaStream_t stream);
 int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,

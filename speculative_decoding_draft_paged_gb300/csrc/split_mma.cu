@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(MAXT, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // After a K/V append launched just before (programmatic dependent
+      // launch), the pages are read only once that kernel has finished.
+      pdl_wait_primary();
       for (int it = 0; it < ntiles; ++it) {
         const int st = it % NS;
         if (it >= NS) {
@@ -440,7 +443,8 @@ int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
                                          plan.smem_bytes);
   if (err != cudaSuccess) return err;
   dim3 grid(plan.S, a.Hkv, a.B);
-  kern<<<grid, plan.threads, plan.smem_bytes, stream>>>(a, tm_k, tm_v);
+  err = launch_kernel(kern, grid, dim3(plan.threads), plan.smem_bytes, stream, plan.pdl, a, tm_k, tm_v);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -349,6 +349,9 @@ __global__ void __launch_bounds__(384, 1)
     };
     int pg_cur = checked(chunk_page(a, PB, Lc, start, end, 0, lane, ppt));
     int pg_nxt = chunk_page(a, PB, Lc, start, end, 1, lane, ppt);
+    // After a K/V append launched just before (programmatic dependent
+    // launch), the pages are read only once that kernel has finished.
+    pdl_wait_primary();
     int cur_k = 0;
     Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
     for (int j = 0; j < n; ++j) {
@@ -711,9 +714,8 @@ int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
   if (err != cudaSuccess) return err;
-  kern<<<static_cast<unsigned>(plan.units), TcCfg<D>::kThreads, TcCfg<D>::kSmem, stream>>>(
-      a, tm_k, tm_v, tm_q, tm_out, tm_part);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(static_cast<unsigned>(plan.units)), dim3(TcCfg<D>::kThreads),
+                       TcCfg<D>::kSmem, stream, plan.pdl, a, tm_k, tm_v, tm_q, tm_out, tm_part);
 }
 
 }  // namespace
