@@ -65,7 +65,7 @@ def load_library(path: str):
     f = lib.oracle_block_attn
     f.restype = ctypes.c_int
     i32, vp = ctypes.c_int, ctypes.c_void_p
-    f.argtypes = [i32] * 11 + [ctypes.c_double] + [vp] * 6 + [i32] + [vp, vp, i32]
+    f.argtypes = [i32] * 11 + [ctypes.c_double] + [vp] * 8 + [i32] + [vp, vp, i32]
     f = lib.oracle_block_placement
     f.restype = ctypes.c_int
     f.argtypes = [i32] * 5 + [vp] * 3
@@ -88,7 +88,8 @@ def _ptr(a):
 
 
 def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window, future_keys,
-               scale, right_window=0, req_ids=None, nthreads=0, lib=None):
+               scale, right_window=0, k_block=None, v_block=None, req_ids=None, nthreads=0,
+               lib=None):
     """Return ``(out, lse2)`` in float64 for requests ``req_ids`` (all when None).
 
     ``q``: uint16 bf16 bits ``[B, K, Hq, D]``; ``k_pages``/``v_pages``: uint16
@@ -107,6 +108,13 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window,
         raise ValueError("inconsistent shapes")
     if page_table.shape[0] != B or ctx_lens.shape != (B,):
         raise ValueError("inconsistent batch")
+    if (k_block is None) != (v_block is None):
+        raise ValueError("k_block and v_block go together")
+    if k_block is not None:
+        k_block = np.ascontiguousarray(k_block, dtype=np.uint16)
+        v_block = np.ascontiguousarray(v_block, dtype=np.uint16)
+        if k_block.shape != (B, K, Hkv, D) or v_block.shape != k_block.shape:
+            raise ValueError("k_block / v_block must be [B, K, Hkv, D]")
     if req_ids is not None:
         req_ids = np.ascontiguousarray(req_ids, dtype=np.int32)
         n = int(req_ids.shape[0])
@@ -117,7 +125,7 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window,
     rc = (lib or _load()).oracle_block_attn(
         B, Hq, Hkv, D, P, page_table.shape[1], num_pages, K, int(window), int(future_keys),
         int(right_window), float(scale), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(ctx_lens),
-        _ptr(req_ids), n, _ptr(out), _ptr(lse2), int(nthreads))
+        _ptr(k_block), _ptr(v_block), _ptr(req_ids), n, _ptr(out), _ptr(lse2), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_block_attn failed with status {rc}")
     return out, lse2

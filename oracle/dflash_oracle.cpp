@@ -20,7 +20,11 @@
 //     the causal window plus the later keys of the block.
 // Every key row is read through the page table: the row of logical position p
 // is pages[page_table[b][p / P]][h][p % P][:] (HND page layout, PR #20374
-// kernel sweep: "page 32, HND").  Then, in double precision,
+// kernel sweep: "page 32, HND") -- or, in the dense-suffix form (PR #16150:
+// the draft context in the target's paged pool, "the dense noise suffix fused
+// into the same softmax"), the block's rows p = L+j come from dense tensors
+// k_block[b][j][h][:], v_block[b][j][h][:] and only the context is paged.
+// Then, in double precision,
 //   s_p  = scale * sum_d q_d k_{p,d}
 //   m    = max_p s_p,   Z = sum_p exp(s_p - m)
 //   out  = sum_p exp(s_p - m) v_p / Z
@@ -53,6 +57,8 @@ struct Problem {
   const uint16_t* v_pages;
   const int32_t* page_table;
   const int32_t* ctx_lens;
+  const uint16_t* k_block;  // [B, K, Hkv, D] dense block rows, or null (paged)
+  const uint16_t* v_block;
 };
 
 // Address of the key/value row of logical position p of request b, head h;
@@ -85,13 +91,26 @@ int attend_row(const Problem& pr, int b, int i, int hq, double* out_row, double*
   std::vector<double> qd(pr.D);
   for (int d = 0; d < pr.D; ++d) qd[d] = bf16_to_double(qrow[d]);
 
-  std::vector<double> s(pos.size());
-  std::vector<int64_t> off(pos.size());
+  // Key and value rows of each visible position.
+  std::vector<const uint16_t*> krow(pos.size()), vrow(pos.size());
   for (size_t t = 0; t < pos.size(); ++t) {
-    off[t] = row_offset(pr, b, h, pos[t]);
-    if (off[t] < 0) return -3;
+    if (pr.k_block != nullptr && pos[t] >= L) {
+      const int64_t j = pos[t] - L;
+      const int64_t o = ((static_cast<int64_t>(b) * pr.K + j) * pr.Hkv + h) * pr.D;
+      krow[t] = pr.k_block + o;
+      vrow[t] = pr.v_block + o;
+    } else {
+      const int64_t o = row_offset(pr, b, h, pos[t]);
+      if (o < 0) return -3;
+      krow[t] = pr.k_pages + o;
+      vrow[t] = pr.v_pages + o;
+    }
+  }
+
+  std::vector<double> s(pos.size());
+  for (size_t t = 0; t < pos.size(); ++t) {
     double acc = 0.0;
-    for (int d = 0; d < pr.D; ++d) acc += qd[d] * bf16_to_double(pr.k_pages[off[t] + d]);
+    for (int d = 0; d < pr.D; ++d) acc += qd[d] * bf16_to_double(krow[t][d]);
     s[t] = pr.scale * acc;
   }
 
@@ -102,7 +121,7 @@ int attend_row(const Problem& pr, int b, int i, int hq, double* out_row, double*
   for (int d = 0; d < pr.D; ++d) out_row[d] = 0.0;
   for (size_t t = 0; t < pos.size(); ++t) {
     const double w = std::exp(s[t] - m);
-    for (int d = 0; d < pr.D; ++d) out_row[d] += w * bf16_to_double(pr.v_pages[off[t] + d]);
+    for (int d = 0; d < pr.D; ++d) out_row[d] += w * bf16_to_double(vrow[t][d]);
   }
   for (int d = 0; d < pr.D; ++d) out_row[d] /= Z;
   *lse_row = (m + std::log(Z)) / std::log(2.0);
@@ -123,13 +142,15 @@ int oracle_block_attn(int B, int Hq, int Hkv, int D, int P, int max_pages, int n
                       int K, int W, int future_keys, int right_window, double scale,
                       const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
                       const int32_t* page_table, const int32_t* ctx_lens,
+                      const uint16_t* k_block, const uint16_t* v_block,
                       const int32_t* req_ids, int n_req,
                       double* out, double* lse2, int nthreads) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0 || K <= 0 ||
       W < 0 || max_pages <= 0 || num_pages <= 0 || right_window < 0)
     return -1;
+  if ((k_block == nullptr) != (v_block == nullptr)) return -1;
   Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, right_window, scale,
-             q, k_pages, v_pages, page_table, ctx_lens};
+             q, k_pages, v_pages, page_table, ctx_lens, k_block, v_block};
   if (req_ids == nullptr) n_req = B;
   const int G = Hq / Hkv;
   const int64_t n_items = static_cast<int64_t>(n_req) * Hkv;

@@ -413,6 +413,34 @@ def test_append_then_attention_equals_dense(oracle_mod):
         np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
 
 
+@pytest.mark.parametrize("W,fk,r", [(0, 1, 0), (5, 1, 0), (0, 0, 1), (2, 0, 2)])
+def test_dense_suffix_equals_dense_attention(oracle_mod, W, fk, r):
+    """Dense-suffix form: the pages hold the context only (block slots are NaN),
+    the block rows come from dense tensors; the result is the masked dense
+    attention over context + block, and equals appending then reading paged."""
+    rng = np.random.default_rng(1100 + 10 * W + r)
+    K, Hq, Hkv, D, P = 4, 4, 2, 8, 3
+    lens = [0, 2, 5, 16]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    kb = np.stack([dk[b][L:] for b, L in enumerate(lens)])
+    vb = np.stack([dv[b][L:] for b, L in enumerate(lens)])
+    for b, L in enumerate(lens):
+        for p in range(L, L + K):
+            kp[tab[b, p // P], :, p % P, :] = 0x7FC0
+            vp[tab[b, p // P], :, p % P, :] = 0x7FC0
+    out, lse2 = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W, future_keys=fk,
+                                      right_window=r, scale=0.47, k_block=kb, v_block=vb)
+    for b, L in enumerate(lens):
+        ro, rl = dense_attention(q[b], dk[b], dv[b], 0.47, visible_mask(L, K, W, fk, r))
+        np.testing.assert_allclose(out[b], ro, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
+    ka, va = oracle_mod.append_block_kv(kb, vb, kp, vp, tab, ctx)
+    o2, l2 = oracle_mod.block_attn(q, ka, va, tab, ctx, block_size=K, window=W, future_keys=fk,
+                                   right_window=r, scale=0.47)
+    np.testing.assert_array_equal(out, o2)
+    np.testing.assert_array_equal(lse2, l2)
+
+
 # ----------------------------------------------------------------------------
 # Errors
 # ----------------------------------------------------------------------------
