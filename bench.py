@@ -264,6 +264,9 @@ def main():
     ap.add_argument("--fused-append", action="store_true",
                     help="time dflash_block_attn_append: the block's K/V append to the pages "
                          "followed by the attention in one launch sequence")
+    ap.add_argument("--dense-suffix", action="store_true",
+                    help="time dflash_block_attn_dense_suffix: the block's K/V from dense "
+                         "tensors, the context from the pages")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -302,9 +305,10 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    if args.fused_append:
+    if args.fused_append or args.dense_suffix:
         # The block's own K/V rows (already in the pages from the input
-        # recipe): re-appending them each call leaves the pools unchanged.
+        # recipe): re-appending them each call leaves the pools unchanged,
+        # and the dense-suffix form reads the same values from these tensors.
         kb = torch.empty((spec.B, spec.K, spec.Hkv, spec.D), dtype=torch.bfloat16, device=dev)
         vb = torch.empty_like(kb)
         tab = inp["page_table"].cpu()
@@ -315,7 +319,13 @@ def main():
                 vb[b, j] = inp["v_pages"][pg, :, off, :]
 
     def call():
-        if args.fused_append:
+        if args.dense_suffix:
+            rc = dflash.block_attn_dense_suffix_raw(
+                p, inp["q"].data_ptr(), kb.data_ptr(), vb.data_ptr(), inp["k_pages"].data_ptr(),
+                inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(), inp["ctx_lens"].data_ptr(),
+                out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws_bytes,
+                torch.cuda.current_stream().cuda_stream)
+        elif args.fused_append:
             rc = dflash.block_attn_append_raw(
                 p, inp["q"].data_ptr(), kb.data_ptr(), vb.data_ptr(), inp["k_pages"].data_ptr(),
                 inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(), inp["ctx_lens"].data_ptr(),
@@ -436,7 +446,7 @@ def main():
                        l2="flushed before every timed call (512 MiB write)",
                        kv_bytes_per_call=kv_bytes, path=kernel, split_tiles=plan["split_tiles"],
                        max_splits=plan["max_splits"], ctas=plan["units"], cuda_graph=True,
-                       fused_append=bool(args.fused_append)),
+                       fused_append=bool(args.fused_append), dense_suffix=bool(args.dense_suffix)),
         "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": split_gbs / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": kernel, "kernel_us": split_ms * 1e3,

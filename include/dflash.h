@@ -241,6 +241,20 @@ int dflash_block_attn_append(const dflash_params* p, const void* q, const void* 
                              const int32_t* page_table, const int32_t* ctx_lens, void* out,
                              float* lse2, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Dense-suffix form (PR #16150: the draft context read from the target's
+ * paged pool, the dense block suffix fused into the same softmax): the
+ * block's K/V rows come from k_block / v_block, bf16 [B, K, Hkv, D]
+ * (token-major, 16-byte aligned), and the pages hold the context only --
+ * page-table slots past ceil(L_b / P) are never read.  Otherwise identical
+ * to dflash_block_attn (same parameters, workspace and return codes).
+ */
+int dflash_block_attn_dense_suffix(const dflash_params* p, const void* q, const void* k_block,
+                                   const void* v_block, const void* k_pages, const void* v_pages,
+                                   const int32_t* page_table, const int32_t* ctx_lens, void* out,
+                                   float* lse2, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
 /* Static text for a return code. */
 const char* dflash_status_string(int status);
 

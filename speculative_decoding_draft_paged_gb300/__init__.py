@@ -24,6 +24,7 @@ __all__ = [
     "Params", "PlanInfo", "DflashError", "make_params", "workspace_size", "plan", "block_attn",
     "block_attn_raw", "block_attn_timed_raw", "read_device_status", "clear_device_status", "version", "PATH_AUTO",
     "block_placement", "append_block_kv", "block_attn_append", "block_attn_append_raw",
+    "block_attn_dense_suffix", "block_attn_dense_suffix_raw",
     "PATH_MMA", "PATH_TCGEN05", "DFLASH_OK", "DFLASH_ERR_INVALID", "DFLASH_ERR_WORKSPACE",
     "DFLASH_ERR_DEVICE", "DFLASH_ERR_LAUNCH", "DFLASH_STATUS_BAD_PAGE",
     "DFLASH_STATUS_BAD_CTX_LEN", "DFLASH_STATUS_TIMEOUT",
@@ -240,6 +241,50 @@ def block_attn_append(q, k_block, v_block, k_pages, v_pages, page_table, ctx_len
                                ctx_lens.data_ptr(), out.data_ptr(), lse2.data_ptr(),
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                _stream_handle(stream))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+    return out, lse2
+
+
+def block_attn_dense_suffix_raw(p: Params, q_ptr, kb_ptr, vb_ptr, k_ptr, v_ptr, table_ptr, lens_ptr,
+                                out_ptr, lse_ptr, ws_ptr, ws_bytes, stream_handle) -> int:
+    """Direct C-ABI call of the dense-suffix form; returns the status code."""
+    return int(_lib.load().dflash_block_attn_dense_suffix(
+        ctypes.byref(p), q_ptr, kb_ptr, vb_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, out_ptr, lse_ptr,
+        ws_ptr, ws_bytes, stream_handle))
+
+
+def block_attn_dense_suffix(q, k_block, v_block, k_pages, v_pages, page_table, ctx_lens, *,
+                            block_size: int, window: int, future_keys: int, scale: float,
+                            max_ctx_len: int, out=None, lse2=None, workspace=None, stream=None,
+                            force_path: int = 0, force_split_tiles: int = 0,
+                            right_window: int = 0):
+    """Attention with the block's K/V rows ``[B, K, Hkv, D]`` from dense
+    tensors and the context from the pages.  Returns ``(out, lse2)``."""
+    import torch
+
+    B, K, Hq, D = q.shape
+    _check_block("k_block", k_block, (B, K, k_pages.shape[1], D))
+    _check_block("v_block", v_block, (B, K, k_pages.shape[1], D))
+    p = params_for(q, k_pages, page_table, block_size=block_size, window=window,
+                   future_keys=future_keys, scale=scale, max_ctx_len=max_ctx_len,
+                   force_path=force_path, force_split_tiles=force_split_tiles,
+                   right_window=right_window)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse2 is None:
+        lse2 = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    need = workspace_size(p)
+    if need == 0:
+        raise DflashError(DFLASH_ERR_INVALID)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    rc = block_attn_dense_suffix_raw(p, q.data_ptr(), k_block.data_ptr(), v_block.data_ptr(),
+                                     k_pages.data_ptr(), v_pages.data_ptr(), page_table.data_ptr(),
+                                     ctx_lens.data_ptr(), out.data_ptr(), lse2.data_ptr(),
+                                     workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream_handle(stream))
     if rc != DFLASH_OK:
         raise DflashError(rc)
     return out, lse2

@@ -36,6 +36,7 @@ EXPORTS = (
     "dflash_block_placement",
     "dflash_append_block_kv",
     "dflash_block_attn_append",
+    "dflash_block_attn_dense_suffix",
     "dflash_status_string",
     "dflash_read_device_status",
     "dflash_clear_device_status",
@@ -118,6 +119,8 @@ def load() -> ctypes.CDLL:
             lib.dflash_block_attn_append.argtypes = [ctypes.POINTER(Params)] + [vp] * 10 + \
                 [ctypes.c_size_t, vp]
             lib.dflash_block_attn_append.restype = i32
+            lib.dflash_block_attn_dense_suffix.argtypes = lib.dflash_block_attn_append.argtypes
+            lib.dflash_block_attn_dense_suffix.restype = i32
             lib.dflash_status_string.argtypes = [i32]
             lib.dflash_status_string.restype = ctypes.c_char_p
             lib.dflash_read_device_status.argtypes = [vp, vp]

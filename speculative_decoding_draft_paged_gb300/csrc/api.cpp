@@ -331,12 +331,17 @@ AppendArgs append_args(const dflash_params* p, const void* k_block, const void* 
 
 // The attention call; with `append` given, the K/V append runs first and the
 // split kernel is its programmatic dependent (its producers wait for it).
+// With dense_k / dense_v given (dense-suffix form) the block rows come from
+// them and the pages hold the context only.
 int run_attention(const dflash_params* p, const void* q, const void* k_pages, const void* v_pages,
                   const int32_t* page_table, const int32_t* ctx_lens, void* out, float* lse2,
                   void* workspace, size_t workspace_bytes, void* stream, void* split_start,
-                  void* split_done, const AppendArgs* append) {
+                  void* split_done, const AppendArgs* append, const void* dense_k = nullptr,
+                  const void* dense_v = nullptr) {
   if (!params_valid(p)) return DFLASH_ERR_INVALID;
   if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !out || !lse2 || !workspace)
+    return DFLASH_ERR_INVALID;
+  if ((dense_k == nullptr) != (dense_v == nullptr) || !aligned(dense_k, 16) || !aligned(dense_v, 16))
     return DFLASH_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
       !aligned(page_table, 4) || !aligned(ctx_lens, 4) || !aligned(lse2, 4) ||
@@ -364,6 +369,8 @@ int run_attention(const dflash_params* p, const void* q, const void* k_pages, co
   a.lse2 = lse2;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
+  a.k_block = static_cast<const uint16_t*>(dense_k);
+  a.v_block = static_cast<const uint16_t*>(dense_v);
   const size_t off_lse = kHeaderBytes;
   a.part_lse = reinterpret_cast<float*>(ws + off_lse);
   a.part_o = reinterpret_cast<float*>(ws + off_lse + align_up(partial_rows_for(k) * sizeof(float), 256));
@@ -459,6 +466,16 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
                             void* split_done) {
   return run_attention(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2, workspace,
                        workspace_bytes, stream, split_start, split_done, nullptr);
+}
+
+int dflash_block_attn_dense_suffix(const dflash_params* p, const void* q, const void* k_block,
+                                   const void* v_block, const void* k_pages, const void* v_pages,
+                                   const int32_t* page_table, const int32_t* ctx_lens, void* out,
+                                   float* lse2, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  if (k_block == nullptr || v_block == nullptr) return DFLASH_ERR_INVALID;
+  return run_attention(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2, workspace,
+                       workspace_bytes, stream, nullptr, nullptr, nullptr, k_block, v_block);
 }
 
 int dflash_block_placement(const dflash_params* p, const int32_t* page_table,

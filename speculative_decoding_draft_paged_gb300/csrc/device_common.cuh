@@ -335,6 +335,53 @@ __device__ __forceinline__ void flat_range(const AttnArgs& a, const int* PB, con
   end = flat_tile_at(a, PB, m, static_cast<long long>(c + 1) * m.q);
 }
 
+// ---- dense-suffix form: the block's K/V rows come from dense tensors and the
+// pages hold the context only.
+
+// One past the last position read from the pages.
+__device__ __forceinline__ int paged_end(const AttnArgs& a, const Geometry& g) {
+  return a.k_block != nullptr ? g.L : g.hi_max;
+}
+
+// Writes the block rows at positions [max(L, lo), min(L+K, hi)) of kv head h
+// of request b from the dense tensor `src` ([B, K, Hkv, D] bf16) into a
+// 128-byte-swizzled tile at `tile` whose row 0 is position p0 and which holds
+// T rows per 64-column half (the layout the TMA boxes give).  Threads
+// tid = 0..nthr-1 share the 16-byte pieces.
+template <int D, int T>
+__device__ __forceinline__ void write_suffix_rows(uint8_t* tile, const uint16_t* src, const AttnArgs& a,
+                                                  int b, int h, int L, int p0, int lo, int hi, int tid,
+                                                  int nthr) {
+  constexpr int CPR = D / 8;
+  const int r_lo = max(L, lo);
+  const int r_hi = min(L + a.K, hi);
+  const int n = (r_hi - r_lo) * CPR;
+  for (int e = tid; e < n; e += nthr) {
+    const int pos = r_lo + e / CPR;
+    const int c = e - (e / CPR) * CPR;
+    const int rr = pos - p0;
+    const uint4* row =
+        reinterpret_cast<const uint4*>(src + ((static_cast<size_t>(b) * a.K + (pos - L)) * a.Hkv + h) * D);
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * T * 128 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) =
+        __ldg(row + c);
+  }
+}
+
+// Pulls the block rows of kv head h of request b (K and V) into L2.
+__device__ __forceinline__ void prefetch_suffix_rows(const AttnArgs& a, int b, int h, int tid, int nthr) {
+  const int lines_per_row = (a.D * 2 + 127) / 128;
+  const int n = 2 * a.K * lines_per_row;
+  for (int e = tid; e < n; e += nthr) {
+    const int kv = e / (a.K * lines_per_row);
+    const int rem = e - kv * a.K * lines_per_row;
+    const int j = rem / lines_per_row;
+    const int l = rem - j * lines_per_row;
+    const uint16_t* src = kv ? a.v_block : a.k_block;
+    prefetch_l2(reinterpret_cast<const uint8_t*>(src + ((static_cast<size_t>(b) * a.K + j) * a.Hkv + h) * a.D) +
+                l * 128);
+  }
+}
+
 // Programmatic dependent launch controls.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -39,6 +39,8 @@ struct AttnArgs {
   float* part_o;              // [units, R, D]  normalised partial output
   float* part_lse;            // [units, R]     partial base-2 LSE
   uint32_t* status;           // workspace status word
+  const uint16_t* k_block;    // dense-suffix form: bf16 [B, K, Hkv, D] block rows, else null
+  const uint16_t* v_block;    //   (then the pages hold the context positions < L only)
   int B, Hq, Hkv, G, D, P, max_pages, num_pages, K, W, max_ctx_len;
   int rw;                     // later block keys each row sees (K-1: non-causal form)
   float scale_log2;           // scale * log2(e), applied to q.k in fp32

@@ -40,6 +40,16 @@ struct MmaTile {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Dense-suffix form: the block's K and V rows of one warp's key slice
+// [lo, hi) into stage tiles whose row 0 is position p0.  Out of line: it runs
+// on at most two tiles per unit and would otherwise crowd the tile loop.
+template <int D, int T>
+__device__ __noinline__ void write_slice_suffix(uint8_t* k_tile, uint8_t* v_tile, const AttnArgs& a,
+                                                int b, int h, int L, int p0, int lo, int hi, int lane) {
+  write_suffix_rows<D, T>(k_tile, a.k_block, a, b, h, L, p0, lo, hi, lane, 32);
+  write_suffix_rows<D, T>(v_tile, a.v_block, a, b, h, L, p0, lo, hi, lane, 32);
+}
+
 template <int D, int KPW, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1)
     split_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
@@ -98,7 +108,12 @@ __global__ void __launch_bounds__(MAXT, 1)
 
   const int pages_per_tile = T / a.P;
   load_unit_pages(a, b, tile0 * pages_per_tile, ntiles * pages_per_tile, geo.lo_min / a.P,
-                  (geo.hi_max + a.P - 1) / a.P, pg_smem, threadIdx.x, blockDim.x);
+                  (paged_end(a, geo) + a.P - 1) / a.P, pg_smem, threadIdx.x, blockDim.x);
+  // Dense-suffix form: the unit that holds the block positions reads the
+  // block rows from the dense tensors; pull them into L2 now.
+  const bool dense = a.k_block != nullptr;
+  if (dense && (tile0 + ntiles) * T > geo.L && tile0 * T < geo.L + a.K)
+    prefetch_suffix_rows(a, b, h, threadIdx.x, blockDim.x);
 
   // Packed query tile: row r = i*G + g  <-  q[b, i, h*G + g, :]; rows >= R are zero.
   {
@@ -212,6 +227,14 @@ __global__ void __launch_bounds__(MAXT, 1)
       const uint32_t k_st = base_u32 + st * kStageBytes;
       const uint32_t v_st = k_st + kTileBytes;
       const int p0 = (tile0 + it) * T + kb;  // logical position of the slice's first key
+      if (dense && p0 + KPW > L && p0 < L + a.K) {
+        // The block rows of this warp's key slice, from the dense tensors
+        // (warps of other row groups with the same slice write the same
+        // bytes; each warp reads only after its own writes).
+        uint8_t* k_tile = base + st * kStageBytes;
+        write_slice_suffix<D, T>(k_tile, k_tile + kTileBytes, a, b, h, L, p0 - kb, p0, p0 + KPW, lane);
+        __syncwarp();
+      }
 
       // S = Q K^T over this warp's 16 rows x KPW keys.
       float sacc[NT][4];

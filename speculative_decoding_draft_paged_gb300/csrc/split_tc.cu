@@ -66,8 +66,8 @@ struct TcCfg {
   static constexpr int kOffStage = kOffV + NSV * kTileBytes;
   static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
   // k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
-  // s_free[2], p_full[2], pv_done[2], q_full, q_free
-  static constexpr int kNumBars = 2 * NSK + 2 * NSV + 10;
+  // s_free[2], p_full[2], pv_done[2], q_full, q_free, k_fix[NSK]
+  static constexpr int kNumBars = 3 * NSK + 2 * NSV + 10;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffXchg = kOffMisc + 64;                 // both groups' (m, l) per row
   static constexpr int kOffPB = kOffXchg + 2 * 128 * 8;          // tile prefix per request
@@ -147,7 +147,7 @@ __device__ __forceinline__ int chunk_page(const AttnArgs& a, const int* PB, cons
   const int t = within - (within / nb) * nb;
   const Geometry geo = make_geometry(Lc[b], a.max_ctx_len, a.K, a.W, 64, 1);
   const int slot = (geo.t_begin + t) * ppt + (lane - lt * ppt);
-  if (slot < geo.lo_min / a.P || slot >= (geo.hi_max + a.P - 1) / a.P) return kNoPage;
+  if (slot < geo.lo_min / a.P || slot >= (paged_end(a, geo) + a.P - 1) / a.P) return kNoPage;
   return __ldg(&a.page_table[static_cast<size_t>(b) * a.max_pages + slot]);
 }
 
@@ -265,6 +265,9 @@ __global__ void __launch_bounds__(384, 1)
   auto pv_done = [&](int g) { return bars + 8u * (kB0 + 6 + g); };
   const uint32_t q_full = bars + 8u * (kB0 + 8);
   const uint32_t q_free = bars + 8u * (kB0 + 9);
+  // Dense-suffix form: K tile st holds its block rows once k_fix(st) completes.
+  auto k_fix = [&](int st) { return bars + 8u * (kB0 + 10 + st); };
+  const bool dense = a.k_block != nullptr;
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile uint32_t* tmem_slot = misc;          // TMEM base address from tcgen05.alloc
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -291,6 +294,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(q_free, 1);
+    for (int st = 0; st < NSK; ++st) mbar_init(k_fix(st), 1);
     *abort_flag = 0;
     *issued_k = 0;
     *issued_v = 0;
@@ -392,27 +396,63 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 11) {
     // ------------------------------------------------------------ query loader
-    if (lane == 0) {
-      Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
-      for (;;) {
+    // Lane 0 issues each segment's query boxes.  In the dense-suffix form the
+    // whole warp also writes the block's K rows into the K tiles that hold
+    // them, once they have landed, and arrives on k_fix (the MMA waits for it
+    // on those tiles); the block rows are pulled into L2 a segment ahead.
+    Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
+    uint32_t fixes = 0;  // per K slot: block-row fixes done (8 bits each)
+    if (dense) prefetch_suffix_rows(a, sg.b, sg.h, lane, 32);
+    for (;;) {
+      int stop = 0;
+      if (lane == 0) {
         if (sg.idx > 0 && !mbar_wait(q_free, (sg.idx - 1) & 1)) {
           flag_status(a.status, DFLASH_STATUS_TIMEOUT);
           *abort_flag = 1;
         }
-        if (*abort_flag) break;
-        // Box (64 columns, G heads, K tokens) lands as rows r = i*G + g with
-        // the 128-byte swizzle, one box per 64-column half.
-        mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(a.R * D * 2));
+        stop = *abort_flag;
+        if (!stop) {
+          // Box (64 columns, G heads, K tokens) lands as rows r = i*G + g with
+          // the 128-byte swizzle, one box per 64-column half.
+          mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(a.R * D * 2));
 #pragma unroll
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_3d(sQ + x * 128 * 128, &tm_q, x * 64, sg.h * a.G, sg.b * a.K, q_full);
-        *issued_q = sg.idx + 1;
-        if (sg.j1 >= n) break;
-        seg_next(sg, PB, a.Hkv, start, end);
+          for (int x = 0; x < D / 64; ++x)
+            tma_load_3d(sQ + x * 128 * 128, &tm_q, x * 64, sg.h * a.G, sg.b * a.K, q_full);
+          *issued_q = sg.idx + 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+      if (dense) {
+        const Geometry geo = make_geometry(Lc[sg.b], a.max_ctx_len, a.K, a.W, T, 1);
+        const int pos_base = (geo.t_begin - (sg.g0 - start)) * T;
+        for (int j = sg.j0; j < sg.j1 && !stop; ++j) {
+          const int p0 = pos_base + j * T;
+          if (p0 + T <= geo.L || p0 >= geo.L + a.K) continue;
+          const int st = j % NSK;
+          if (!mbar_wait_warp(k_full(st), (j / NSK) & 1)) {
+            if (lane == 0) flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+            *abort_flag = 1;
+            stop = 1;
+            break;
+          }
+          write_suffix_rows<D, T>(gbase + C::kOffK + st * C::kTileBytes, a.k_block, a, sg.b, sg.h,
+                                  geo.L, p0, p0, p0 + T, lane, 32);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(k_fix(st));
+          fixes += 1u << (8 * st);
+        }
+        if (stop) break;
+      }
+      if (sg.j1 >= n) break;
+      seg_next(sg, PB, a.Hkv, start, end);
+      if (lane == 0) {
 #pragma unroll
         for (int x = 0; x < D / 64; ++x) tma_prefetch_3d(&tm_q, x * 64, sg.h * a.G, sg.b * a.K);
       }
+      if (dense) prefetch_suffix_rows(a, sg.b, sg.h, lane, 32);
     }
+    (void)fixes;
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -428,6 +468,7 @@ __global__ void __launch_bounds__(384, 1)
       int seg_prev = 0;          // segment of tile j-1
       int pv_seg[2] = {-1, -1};  // segment of each group's latest PV
       int last_qk = -1, last_pv = -1;
+      uint32_t fixes = 0;  // per K slot: block-row fixes waited for (8 bits each)
       // S_j = Q K_j^T into TMEM S buffer j%2.
       auto issue_qk = [&](int j, int seg_j) -> bool {
         const int st = j % NSK;
@@ -436,6 +477,15 @@ __global__ void __launch_bounds__(384, 1)
           q_seg = seg_j;
         }
         if (!mbar_wait(k_full(st), (j / NSK) & 1)) return false;
+        if (dense) {
+          // A tile holding block positions waits for its block rows.
+          const Geometry geo = make_geometry(Lc[sg.b], a.max_ctx_len, a.K, a.W, T, 1);
+          const int p0 = (geo.t_begin - (sg.g0 - start)) * T + j * T;
+          if (p0 + T > geo.L && p0 < geo.L + a.K) {
+            if (!mbar_wait(k_fix(st), (fixes >> (8 * st)) & 1)) return false;
+            fixes += 1u << (8 * st);
+          }
+        }
         if (j >= 2 && !mbar_wait(s_free(j & 1), ((j >> 1) - 1) & 1)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (j & 1) * T;
@@ -611,10 +661,15 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         // Value rows outside [lo_min, L+K) may hold anything: zero them in the
-        // stage before the PV MMA reads it (boundary tiles only).
-        if (p0 < geo.lo_min || p0 + T > geo.hi_max) {
+        // stage before the PV MMA reads it (boundary tiles only).  In the
+        // dense-suffix form the block's value rows are written here too.
+        const bool v_suffix = dense && p0 + T > L && p0 < L + a.K;
+        if (p0 < geo.lo_min || p0 + T > geo.hi_max || v_suffix) {
           const int st = j % NSV;
           if (!mbar_wait_warp(v_full(st), (j / NSV) & 1)) { ok = false; break; }
+          if (v_suffix)
+            write_suffix_rows<D, T>(gbase + C::kOffV + st * C::kTileBytes, a.v_block, a, sg.b, sg.h, L,
+                                    p0, p0, p0 + T, gthread, 128);
           if (gthread < T) {
             const int pos = p0 + gthread;
             if (pos < geo.lo_min || pos >= geo.hi_max) {

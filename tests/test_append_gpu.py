@@ -139,3 +139,60 @@ def test_bad_block_page_is_flagged_and_skipped(cuda_device):
         for j in range(spec.K):
             mask[place[b, j, 0], :, place[b, j, 1]] = False
     np.testing.assert_array_equal(after_k[mask], before_k[mask])
+
+
+# ----------------------------------------------------------------------------
+# Dense-suffix form: block rows from dense tensors, context from the pages
+# ----------------------------------------------------------------------------
+
+def _dense_suffix_case(spec, device, seed):
+    """Inputs whose pages hold the context only: the block's slots are NaN and
+    every table entry past the context's last page names no page."""
+    cpu = W.make_inputs(spec, "cpu")
+    kb, vb = _block_rows(spec, seed)
+    lens = np.asarray(spec.ctx_lens, np.int32)
+    place = oracle.block_placement(cpu["page_table"].numpy(), lens, block_size=spec.K,
+                                   page_size=spec.P, num_pages=spec.num_pages)
+    inp = {k: v.to(device) for k, v in cpu.items()}
+    _stale_block_slots(inp, place)
+    tab = inp["page_table"].cpu()
+    for b, L in enumerate(spec.ctx_lens):
+        first_unused = (L + spec.P - 1) // spec.P
+        tab[b, first_unused:] = spec.num_pages + 1000
+    inp["page_table"] = tab.to(device)
+    return inp, kb, vb
+
+
+@pytest.mark.parametrize("path", [dflash.PATH_MMA, dflash.PATH_TCGEN05])
+@pytest.mark.parametrize("shape,win,fk,r,split", [
+    ("gqa8", 0, 1, 0, 0), ("gqa8", 300, 1, 0, 0), ("gqa8", 3, 0, 2, 0),
+    ("minimax", 4096, 1, 0, 0), ("minimax", 0, 0, 0, 0), ("minimax", 0, 1, 0, 1),
+    ("minimax", 2, 0, 4, 3),
+])
+def test_dense_suffix(cuda_device, path, shape, win, fk, r, split):
+    if shape == "gqa8":
+        spec = _spec("dense_gqa8", [0, 5, 25, 32, 33, 700, 2000], Hq=16, Hkv=2, K=7, P=32,
+                     window=win, future_keys=fk, right_window=r)
+    else:
+        spec = W.CaseSpec("dense_minimax", B=4, Hq=16, Hkv=1, D=128, K=7, P=64, window=win,
+                          future_keys=fk, right_window=r, ctx_lens=[5000, 64, 0, 121], seed=71,
+                          poison=True)
+    inp, kb, vb = _dense_suffix_case(spec, cuda_device, 13)
+    ws_bytes = dflash.workspace_size(dflash.params_for(
+        inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K, window=spec.window,
+        future_keys=spec.future_keys, scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len,
+        force_path=path, force_split_tiles=split, right_window=spec.right_window))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda_device)
+    out, lse = dflash.block_attn_dense_suffix(
+        inp["q"], kb.to(cuda_device), vb.to(cuda_device), inp["k_pages"], inp["v_pages"],
+        inp["page_table"], inp["ctx_lens"], block_size=spec.K, window=spec.window,
+        future_keys=spec.future_keys, scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len,
+        force_path=path, force_split_tiles=split, right_window=spec.right_window, workspace=ws)
+    torch.cuda.synchronize()
+    assert dflash.read_device_status(ws) == 0, "a page-table slot past the context was read"
+    ro, rl = oracle.block_attn(to_bits(inp["q"]), to_bits(inp["k_pages"]), to_bits(inp["v_pages"]),
+                               inp["page_table"].cpu().numpy(), np.asarray(spec.ctx_lens, np.int32),
+                               block_size=spec.K, window=spec.window, future_keys=spec.future_keys,
+                               right_window=spec.right_window, scale=spec.softmax_scale,
+                               k_block=to_bits(kb), v_block=to_bits(vb))
+    assert_parity(metrics(out, lse, ro, rl), spec.name)
