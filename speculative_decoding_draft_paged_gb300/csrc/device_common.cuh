@@ -367,6 +367,88 @@ __device__ __forceinline__ void write_suffix_rows(uint8_t* tile, const uint16_t*
   }
 }
 
+// The same rows held in registers ahead of time: thread tid of nthr holds the
+// 16-byte pieces e = tid + k*nthr (k < MAXP) of the K*D/8 pieces of the block
+// (piece e = row e / (D/8), chunk e % (D/8)).  load_suffix_pieces reads them
+// early; write_suffix_pieces stores those that fall in a tile starting at p0.
+template <int D, int MAXP>
+__device__ __forceinline__ void load_suffix_pieces(uint4 (&regs)[MAXP], const uint16_t* src,
+                                                   const AttnArgs& a, int b, int h, int tid, int nthr) {
+  constexpr int CPR = D / 8;
+  const int n = a.K * CPR;
+#pragma unroll
+  for (int k = 0; k < MAXP; ++k) {
+    const int e = tid + k * nthr;
+    if (e < n) {
+      const int j = e / CPR;
+      const int c = e - j * CPR;
+      regs[k] = __ldg(reinterpret_cast<const uint4*>(
+                          src + ((static_cast<size_t>(b) * a.K + j) * a.Hkv + h) * D) + c);
+    }
+  }
+}
+
+template <int D, int T, int MAXP>
+__device__ __forceinline__ void write_suffix_pieces(uint8_t* tile, const uint4 (&regs)[MAXP],
+                                                    const AttnArgs& a, int L, int p0, int tid, int nthr) {
+  constexpr int CPR = D / 8;
+  const int n = a.K * CPR;
+#pragma unroll
+  for (int k = 0; k < MAXP; ++k) {
+    const int e = tid + k * nthr;
+    if (e < n) {
+      const int j = e / CPR;
+      const int c = e - j * CPR;
+      const int rr = L + j - p0;
+      if (rr >= 0 && rr < T)
+        *reinterpret_cast<uint4*>(tile + (c >> 3) * T * 128 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) =
+            regs[k];
+    }
+  }
+}
+
+// The same pieces copied asynchronously (cp.async, 16 bytes each) into a
+// linear staging buffer (piece e at byte 16e), then, after the copying
+// thread's cp.async.wait_all, moved into a tile: each thread moves the pieces
+// it copied itself, so no other synchronisation is needed.
+template <int D, int MAXP>
+__device__ __forceinline__ void stage_suffix_async(uint32_t stage, const uint16_t* src, const AttnArgs& a,
+                                                   int b, int h, int tid, int nthr) {
+  constexpr int CPR = D / 8;
+  const int n = a.K * CPR;
+#pragma unroll
+  for (int k = 0; k < MAXP; ++k) {
+    const int e = tid + k * nthr;
+    if (e < n) {
+      const int j = e / CPR;
+      const int c = e - j * CPR;
+      const uint16_t* g = src + ((static_cast<size_t>(b) * a.K + j) * a.Hkv + h) * D + c * 8;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(stage + 16u * e), "l"(g) : "memory");
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int D, int T, int MAXP>
+__device__ __forceinline__ void write_staged_suffix(uint8_t* tile, const uint8_t* stage, const AttnArgs& a,
+                                                    int L, int p0, int tid, int nthr) {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  constexpr int CPR = D / 8;
+  const int n = a.K * CPR;
+#pragma unroll
+  for (int k = 0; k < MAXP; ++k) {
+    const int e = tid + k * nthr;
+    if (e < n) {
+      const int j = e / CPR;
+      const int c = e - j * CPR;
+      const int rr = L + j - p0;
+      if (rr >= 0 && rr < T)
+        *reinterpret_cast<uint4*>(tile + (c >> 3) * T * 128 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) =
+            *reinterpret_cast<const uint4*>(stage + 16 * e);
+    }
+  }
+}
+
 // Pulls the block rows of kv head h of request b (K and V) into L2.
 __device__ __forceinline__ void prefetch_suffix_rows(const AttnArgs& a, int b, int h, int tid, int nthr) {
   const int lines_per_row = (a.D * 2 + 127) / 128;

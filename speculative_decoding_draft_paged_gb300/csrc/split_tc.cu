@@ -72,7 +72,10 @@ struct TcCfg {
   static constexpr int kOffXchg = kOffMisc + 64;                 // both groups' (m, l) per row
   static constexpr int kOffPB = kOffXchg + 2 * 128 * 8;          // tile prefix per request
   static constexpr int kOffLc = kOffPB + 4 * (kTcMaxBatch + 1);  // clamped context lengths
-  static constexpr int kSmem = kOffLc + 4 * kTcMaxBatch + 1024;
+  // Dense-suffix form: per softmax group, the block's value rows in flight.
+  static constexpr int kOffVStage = (kOffLc + 4 * kTcMaxBatch + 15) / 16 * 16;
+  static constexpr int kVStageBytes = kMaxBlock * D * 2;
+  static constexpr int kSmem = kOffVStage + 2 * kVStageBytes + 1024;
   // TMEM columns: S0 [0,64) S1 [64,128) O0 [128,128+D) O1 [256,256+D)
   // P0 [384,416) P1 [416,448) (bf16 pairs).
   static constexpr int kTmemCols = 512;
@@ -402,6 +405,8 @@ __global__ void __launch_bounds__(384, 1)
     // on those tiles); the block rows are pulled into L2 a segment ahead.
     Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
     uint32_t fixes = 0;  // per K slot: block-row fixes done (8 bits each)
+    constexpr int kKPieces = (kMaxBlock * (D / 8) + 31) / 32;
+    uint4 kreg[kKPieces];
     if (dense) prefetch_suffix_rows(a, sg.b, sg.h, lane, 32);
     for (;;) {
       int stop = 0;
@@ -425,9 +430,14 @@ __global__ void __launch_bounds__(384, 1)
       if (dense) {
         const Geometry geo = make_geometry(Lc[sg.b], a.max_ctx_len, a.K, a.W, T, 1);
         const int pos_base = (geo.t_begin - (sg.g0 - start)) * T;
+        bool loaded = false;
         for (int j = sg.j0; j < sg.j1 && !stop; ++j) {
           const int p0 = pos_base + j * T;
           if (p0 + T <= geo.L || p0 >= geo.L + a.K) continue;
+          if (!loaded) {  // the block's K rows, read while the tile is in flight
+            load_suffix_pieces<D, kKPieces>(kreg, a.k_block, a, sg.b, sg.h, lane, 32);
+            loaded = true;
+          }
           const int st = j % NSK;
           if (!mbar_wait_warp(k_full(st), (j / NSK) & 1)) {
             if (lane == 0) flag_status(a.status, DFLASH_STATUS_TIMEOUT);
@@ -435,8 +445,8 @@ __global__ void __launch_bounds__(384, 1)
             stop = 1;
             break;
           }
-          write_suffix_rows<D, T>(gbase + C::kOffK + st * C::kTileBytes, a.k_block, a, sg.b, sg.h,
-                                  geo.L, p0, p0, p0 + T, lane, 32);
+          write_suffix_pieces<D, T, kKPieces>(gbase + C::kOffK + st * C::kTileBytes, kreg, a, geo.L, p0,
+                                              lane, 32);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(k_fix(st));
@@ -591,6 +601,14 @@ __global__ void __launch_bounds__(384, 1)
       int last_j = -1;  // this group's latest tile in the segment
       const int jfirst = sg.j0 + (((sg.j0 & 1) != grp) ? 1 : 0);
       for (int j = jfirst; ok && j < sg.j1; j += 2) {
+        // Dense-suffix form: a tile holding block positions takes its value
+        // rows from the dense tensor; the loads are issued before the score
+        // wait so they land meanwhile.
+        constexpr int kVPieces = (kMaxBlock * (D / 8) + 127) / 128;
+        const bool v_suffix = dense && pos_base + (j + 1) * T > L && pos_base + j * T < L + a.K;
+        if (v_suffix)
+          stage_suffix_async<D, kVPieces>(base + C::kOffVStage + grp * C::kVStageBytes, a.v_block, a,
+                                          sg.b, sg.h, gthread, 128);
         if (!mbar_wait_warp(s_full(grp), (j >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[64];
@@ -663,13 +681,13 @@ __global__ void __launch_bounds__(384, 1)
         // Value rows outside [lo_min, L+K) may hold anything: zero them in the
         // stage before the PV MMA reads it (boundary tiles only).  In the
         // dense-suffix form the block's value rows are written here too.
-        const bool v_suffix = dense && p0 + T > L && p0 < L + a.K;
         if (p0 < geo.lo_min || p0 + T > geo.hi_max || v_suffix) {
           const int st = j % NSV;
           if (!mbar_wait_warp(v_full(st), (j / NSV) & 1)) { ok = false; break; }
           if (v_suffix)
-            write_suffix_rows<D, T>(gbase + C::kOffV + st * C::kTileBytes, a.v_block, a, sg.b, sg.h, L,
-                                    p0, p0, p0 + T, gthread, 128);
+            write_staged_suffix<D, T, kVPieces>(gbase + C::kOffV + st * C::kTileBytes,
+                                                gbase + C::kOffVStage + grp * C::kVStageBytes, a, L, p0,
+                                                gthread, 128);
           if (gthread < T) {
             const int pos = p0 + gthread;
             if (pos < geo.lo_min || pos >= geo.hi_max) {
@@ -744,6 +762,7 @@ __global__ void __launch_bounds__(384, 1)
       seg_next(sg, PB, a.Hkv, start, end);
     }
     if (gthread == 0) bulk_wait_all();  // this group's output boxes are written
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no block-row copy left in flight
     tc_fence_before();
   }
 
