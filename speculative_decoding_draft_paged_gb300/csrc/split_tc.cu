@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int jj = last_pv - NSV + 1; jj <= last_pv; ++jj)
         if (jj >= 0) (void)mbar_wait(v_empty(jj % NSV), (jj / NSV) & 1);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 9) {
     // ------------------------------------------------------------ softmax (warps 2..9)
     const int sw = warp - 2;          // 0..7
     const int grp = sw >> 2;          // tiles j = grp, grp+2, ...
