@@ -144,8 +144,9 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
       k.units = (tc_tiles + k.C - 1) / k.C;
     } else {
       // A segment's end (merge, output staging, query reload) costs about as
-      // much time as this many key tiles (measured on the headline shape).
-      k.seg_cost = D == 128 ? 4 : 8;
+      // much time as this many key tiles (D = 128: 6 measured best of 4, 6, 9
+      // on the 16/1-head and 64/4-head shapes).
+      k.seg_cost = D == 128 ? 6 : 8;
       const int64_t cost = tc_tiles + static_cast<int64_t>(k.seg_cost) * p->batch * p->num_kv_heads;
       int64_t ctas = (cost + kTcMinTiles - 1) / kTcMinTiles;
       if (ctas > num_sms) ctas = num_sms;
