@@ -20,6 +20,11 @@ PR #20374 "Non-causal unwindowed DFlash draft block", description):
 * ``out`` is the softmax-weighted mean of the visible values and ``lse2`` the
   base-2 log-sum-exp of ``scale * q.k`` over the visible keys.
 
+The dense-suffix form may read fp8 context pages: OCP E4M3 codes with one
+dequantisation scale per tensor (``k = k_scale * e4m3(code)``, likewise V;
+the bf16 block rows take no scale) -- PR #16150, "supports fp8 context
+storage".
+
 Also the block placement and the K/V append (the block's rows written into
 the pool slots of positions ``L .. L+K-1``), plain data movement.
 
@@ -66,6 +71,13 @@ def load_library(path: str):
     f.restype = ctypes.c_int
     i32, vp = ctypes.c_int, ctypes.c_void_p
     f.argtypes = [i32] * 11 + [ctypes.c_double] + [vp] * 8 + [i32] + [vp, vp, i32]
+    f = lib.oracle_block_attn_fp8
+    f.restype = ctypes.c_int
+    dbl = ctypes.c_double
+    f.argtypes = [i32] * 11 + [dbl] + [vp] * 3 + [dbl, dbl] + [vp] * 5 + [i32] + [vp, vp, i32]
+    f = lib.oracle_e4m3_to_double
+    f.restype = ctypes.c_double
+    f.argtypes = [i32]
     f = lib.oracle_block_placement
     f.restype = ctypes.c_int
     f.argtypes = [i32] * 5 + [vp] * 3
@@ -129,6 +141,56 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window,
     if rc != 0:
         raise ValueError(f"oracle_block_attn failed with status {rc}")
     return out, lse2
+
+
+def block_attn_fp8(q, k_pages8, v_pages8, page_table, ctx_lens, *, k_scale, v_scale, k_block,
+                   v_block, block_size, window, future_keys, scale, right_window=0, req_ids=None,
+                   nthreads=0, lib=None):
+    """Dense-suffix form over fp8 context pages; returns ``(out, lse2)`` in float64.
+
+    ``k_pages8``/``v_pages8``: uint8 E4M3 codes ``[num_pages, Hkv, P, D]``
+    (positions < ``ctx_lens[b]`` only are read); ``k_scale``/``v_scale``: the
+    per-tensor dequantisation scales; ``k_block``/``v_block``: uint16 bf16
+    bits ``[B, K, Hkv, D]`` of the block rows.  Other arguments as
+    :func:`block_attn`.
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_pages8 = np.ascontiguousarray(k_pages8, dtype=np.uint8)
+    v_pages8 = np.ascontiguousarray(v_pages8, dtype=np.uint8)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    ctx_lens = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    k_block = np.ascontiguousarray(k_block, dtype=np.uint16)
+    v_block = np.ascontiguousarray(v_block, dtype=np.uint16)
+    B, K, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_pages8.shape
+    if K != block_size or D2 != D or v_pages8.shape != k_pages8.shape:
+        raise ValueError("inconsistent shapes")
+    if page_table.shape[0] != B or ctx_lens.shape != (B,):
+        raise ValueError("inconsistent batch")
+    if k_block.shape != (B, K, Hkv, D) or v_block.shape != k_block.shape:
+        raise ValueError("k_block / v_block must be [B, K, Hkv, D]")
+    if req_ids is not None:
+        req_ids = np.ascontiguousarray(req_ids, dtype=np.int32)
+        n = int(req_ids.shape[0])
+    else:
+        n = B
+    out = np.zeros((n, K, Hq, D), dtype=np.float64)
+    lse2 = np.zeros((n, K, Hq), dtype=np.float64)
+    rc = (lib or _load()).oracle_block_attn_fp8(
+        B, Hq, Hkv, D, P, page_table.shape[1], num_pages, K, int(window), int(future_keys),
+        int(right_window), float(scale), _ptr(q), _ptr(k_pages8), _ptr(v_pages8), float(k_scale),
+        float(v_scale), _ptr(page_table), _ptr(ctx_lens), _ptr(k_block), _ptr(v_block), _ptr(req_ids),
+        n, _ptr(out), _ptr(lse2), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_block_attn_fp8 failed with status {rc}")
+    return out, lse2
+
+
+def e4m3_to_float64(codes, lib=None) -> np.ndarray:
+    """The oracle's value of each E4M3 code (uint8 array)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    f = (lib or _load()).oracle_e4m3_to_double
+    return np.array([f(int(c)) for c in codes.ravel()], dtype=np.float64).reshape(codes.shape)
 
 
 def block_placement(page_table, ctx_lens, *, block_size, page_size, num_pages, lib=None):

@@ -24,6 +24,12 @@
 // the draft context in the target's paged pool, "the dense noise suffix fused
 // into the same softmax"), the block's rows p = L+j come from dense tensors
 // k_block[b][j][h][:], v_block[b][j][h][:] and only the context is paged.
+// The context pages of that form may also be stored in fp8 (PR #16150: the
+// drafter "supports fp8 context storage"): the OCP 8-bit E4M3 format (sign,
+// 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal,
+// S.1111.111 is NaN, no infinities) with one dequantisation scale per tensor,
+// k = k_scale * e4m3(code), v = v_scale * e4m3(code); the block rows stay
+// bf16 and take no scale.
 // Then, in double precision,
 //   s_p  = scale * sum_d q_d k_{p,d}
 //   m    = max_p s_p,   Z = sum_p exp(s_p - m)
@@ -49,6 +55,18 @@ double bf16_to_double(uint16_t bits) {
   return static_cast<double>(f);
 }
 
+// Value of an E4M3 code: (1 + m/8) * 2^(e-7) for e > 0, (m/8) * 2^-6 for
+// e = 0, NaN for e = 15, m = 7.
+double e4m3_to_double(uint8_t code) {
+  const int sign = code >> 7;
+  const int e = (code >> 3) & 15;
+  const int m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? std::ldexp(static_cast<double>(m), -9)
+                            : std::ldexp(static_cast<double>(8 + m), e - 10);
+  return sign ? -mag : mag;
+}
+
 struct Problem {
   int B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys, right_window;
   double scale;
@@ -59,6 +77,17 @@ struct Problem {
   const int32_t* ctx_lens;
   const uint16_t* k_block;  // [B, K, Hkv, D] dense block rows, or null (paged)
   const uint16_t* v_block;
+  const uint8_t* k_pages8;  // fp8 context pages (then k_pages / v_pages are unused), or null
+  const uint8_t* v_pages8;
+  double k_scale, v_scale;
+};
+
+// A key or value row: bf16 bits (scale 1), or fp8 codes with their scale.
+struct RowRef {
+  const uint16_t* bf16;
+  const uint8_t* fp8;
+  double scale;
+  double at(int d) const { return scale * (fp8 ? e4m3_to_double(fp8[d]) : bf16_to_double(bf16[d])); }
 };
 
 // Address of the key/value row of logical position p of request b, head h;
@@ -92,25 +121,30 @@ int attend_row(const Problem& pr, int b, int i, int hq, double* out_row, double*
   for (int d = 0; d < pr.D; ++d) qd[d] = bf16_to_double(qrow[d]);
 
   // Key and value rows of each visible position.
-  std::vector<const uint16_t*> krow(pos.size()), vrow(pos.size());
+  std::vector<RowRef> krow(pos.size()), vrow(pos.size());
   for (size_t t = 0; t < pos.size(); ++t) {
     if (pr.k_block != nullptr && pos[t] >= L) {
       const int64_t j = pos[t] - L;
       const int64_t o = ((static_cast<int64_t>(b) * pr.K + j) * pr.Hkv + h) * pr.D;
-      krow[t] = pr.k_block + o;
-      vrow[t] = pr.v_block + o;
+      krow[t] = RowRef{pr.k_block + o, nullptr, 1.0};
+      vrow[t] = RowRef{pr.v_block + o, nullptr, 1.0};
     } else {
       const int64_t o = row_offset(pr, b, h, pos[t]);
       if (o < 0) return -3;
-      krow[t] = pr.k_pages + o;
-      vrow[t] = pr.v_pages + o;
+      if (pr.k_pages8 != nullptr) {
+        krow[t] = RowRef{nullptr, pr.k_pages8 + o, pr.k_scale};
+        vrow[t] = RowRef{nullptr, pr.v_pages8 + o, pr.v_scale};
+      } else {
+        krow[t] = RowRef{pr.k_pages + o, nullptr, 1.0};
+        vrow[t] = RowRef{pr.v_pages + o, nullptr, 1.0};
+      }
     }
   }
 
   std::vector<double> s(pos.size());
   for (size_t t = 0; t < pos.size(); ++t) {
     double acc = 0.0;
-    for (int d = 0; d < pr.D; ++d) acc += qd[d] * bf16_to_double(krow[t][d]);
+    for (int d = 0; d < pr.D; ++d) acc += qd[d] * krow[t].at(d);
     s[t] = pr.scale * acc;
   }
 
@@ -121,36 +155,18 @@ int attend_row(const Problem& pr, int b, int i, int hq, double* out_row, double*
   for (int d = 0; d < pr.D; ++d) out_row[d] = 0.0;
   for (size_t t = 0; t < pos.size(); ++t) {
     const double w = std::exp(s[t] - m);
-    for (int d = 0; d < pr.D; ++d) out_row[d] += w * bf16_to_double(vrow[t][d]);
+    for (int d = 0; d < pr.D; ++d) out_row[d] += w * vrow[t].at(d);
   }
   for (int d = 0; d < pr.D; ++d) out_row[d] /= Z;
   *lse_row = (m + std::log(Z)) / std::log(2.0);
   return 0;
 }
 
-}  // namespace
-
-extern "C" {
-
-// Computes out[n, i, hq, :] and lse2[n, i, hq] for the requests req_ids[0..n_req)
-// (every request 0..B-1 when req_ids is NULL, n_req then ignored and taken as B).
-// Threads: nthreads workers over (request, kv head) items; nthreads <= 0 means
-// std::thread::hardware_concurrency().  Returns 0, or -1 for bad sizes, -2 for a
-// negative context length, -3 for a visible position whose page-table entry is
-// out of range.
-int oracle_block_attn(int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
-                      int K, int W, int future_keys, int right_window, double scale,
-                      const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
-                      const int32_t* page_table, const int32_t* ctx_lens,
-                      const uint16_t* k_block, const uint16_t* v_block,
-                      const int32_t* req_ids, int n_req,
-                      double* out, double* lse2, int nthreads) {
-  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0 || K <= 0 ||
-      W < 0 || max_pages <= 0 || num_pages <= 0 || right_window < 0)
-    return -1;
-  if ((k_block == nullptr) != (v_block == nullptr)) return -1;
-  Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, right_window, scale,
-             q, k_pages, v_pages, page_table, ctx_lens, k_block, v_block};
+// Every (request, kv head) item of req_ids (all requests when null) on
+// nthreads workers.
+int run_items(const Problem& pr, const int32_t* req_ids, int n_req, double* out, double* lse2,
+              int nthreads) {
+  const int B = pr.B, Hq = pr.Hq, Hkv = pr.Hkv, K = pr.K, D = pr.D;
   if (req_ids == nullptr) n_req = B;
   const int G = Hq / Hkv;
   const int64_t n_items = static_cast<int64_t>(n_req) * Hkv;
@@ -184,6 +200,57 @@ int oracle_block_attn(int B, int Hq, int Hkv, int D, int P, int max_pages, int n
   for (auto& th : pool) th.join();
   return status.load();
 }
+
+}  // namespace
+
+extern "C" {
+
+// Computes out[n, i, hq, :] and lse2[n, i, hq] for the requests req_ids[0..n_req)
+// (every request 0..B-1 when req_ids is NULL, n_req then ignored and taken as B).
+// Threads: nthreads workers over (request, kv head) items; nthreads <= 0 means
+// std::thread::hardware_concurrency().  Returns 0, or -1 for bad sizes, -2 for a
+// negative context length, -3 for a visible position whose page-table entry is
+// out of range.
+int oracle_block_attn(int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
+                      int K, int W, int future_keys, int right_window, double scale,
+                      const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                      const int32_t* page_table, const int32_t* ctx_lens,
+                      const uint16_t* k_block, const uint16_t* v_block,
+                      const int32_t* req_ids, int n_req,
+                      double* out, double* lse2, int nthreads) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0 || K <= 0 ||
+      W < 0 || max_pages <= 0 || num_pages <= 0 || right_window < 0)
+    return -1;
+  if ((k_block == nullptr) != (v_block == nullptr)) return -1;
+  Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, right_window, scale,
+             q, k_pages, v_pages, page_table, ctx_lens, k_block, v_block, nullptr, nullptr, 1.0, 1.0};
+  return run_items(pr, req_ids, n_req, out, lse2, nthreads);
+}
+
+// The dense-suffix form over fp8 (E4M3) context pages: k_pages8 / v_pages8
+// [num_pages, Hkv, P, D] hold codes, dequantised by k_scale / v_scale; the
+// block rows k_block / v_block (bf16 [B, K, Hkv, D], required) are not
+// scaled.  Same sizes, threads and return codes as oracle_block_attn.
+int oracle_block_attn_fp8(int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
+                          int K, int W, int future_keys, int right_window, double scale,
+                          const uint16_t* q, const uint8_t* k_pages8, const uint8_t* v_pages8,
+                          double k_scale, double v_scale, const int32_t* page_table,
+                          const int32_t* ctx_lens, const uint16_t* k_block, const uint16_t* v_block,
+                          const int32_t* req_ids, int n_req, double* out, double* lse2,
+                          int nthreads) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0 || K <= 0 ||
+      W < 0 || max_pages <= 0 || num_pages <= 0 || right_window < 0)
+    return -1;
+  if (k_block == nullptr || v_block == nullptr || k_pages8 == nullptr || v_pages8 == nullptr)
+    return -1;
+  Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, right_window, scale,
+             q, nullptr, nullptr, page_table, ctx_lens, k_block, v_block, k_pages8, v_pages8,
+             k_scale, v_scale};
+  return run_items(pr, req_ids, n_req, out, lse2, nthreads);
+}
+
+// The value of one E4M3 code (for the tests' decoding pin).
+double oracle_e4m3_to_double(int code) { return e4m3_to_double(static_cast<uint8_t>(code)); }
 
 // Block placement: the pool slot of every block token's K/V.  Block token j
 // of request b sits at logical position L_b + j (L_b = ctx_lens[b]), i.e. in

@@ -13,11 +13,13 @@ def random_bf16(rng, shape, sigma=1.0):
     return oracle.bf16_bits_from_float(rng.normal(0.0, sigma, size=shape).astype(np.float32))
 
 
-def scatter_to_pages(rng, dense_k, dense_v, P, Hkv, D, extra_pages=0, extra_slots=0, fill_bits=0x7FC0):
+def scatter_to_pages(rng, dense_k, dense_v, P, Hkv, D, extra_pages=0, extra_slots=0, fill_bits=0x7FC0,
+                     dtype=np.uint16):
     """Scatter per-request dense rows ``[T_b, Hkv, D]`` into shuffled pages.
 
     Returns ``k_pages, v_pages, page_table`` with every unused slot set to
-    ``fill_bits`` (bf16 NaN by default) and unused table entries -1.
+    ``fill_bits`` (bf16 NaN by default) and unused table entries -1.  ``dtype``
+    is the element type of the pools (uint16 bf16 bits, or uint8 fp8 codes).
     """
     B = len(dense_k)
     npg = [(dk.shape[0] + P - 1) // P for dk in dense_k]
@@ -25,8 +27,8 @@ def scatter_to_pages(rng, dense_k, dense_v, P, Hkv, D, extra_pages=0, extra_slot
     perm = rng.permutation(num_pages)
     max_pages = max(max(npg), 1) + extra_slots
     table = np.full((B, max_pages), -1, dtype=np.int32)
-    kp = np.full((num_pages, Hkv, P, D), fill_bits, dtype=np.uint16)
-    vp = np.full((num_pages, Hkv, P, D), fill_bits, dtype=np.uint16)
+    kp = np.full((num_pages, Hkv, P, D), fill_bits, dtype=dtype)
+    vp = np.full((num_pages, Hkv, P, D), fill_bits, dtype=dtype)
     cur = 0
     for b in range(B):
         T = dense_k[b].shape[0]

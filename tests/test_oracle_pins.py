@@ -49,9 +49,15 @@ def dense_attention(q_bits, k_bits, v_bits, scale, mask):
     """torch SDPA + logsumexp in float64.  q [K,Hq,D], k/v [T,Hkv,D], mask [K,T]."""
     import oracle
 
-    q = torch.from_numpy(oracle.bf16_bits_to_float(q_bits).astype(np.float64))
-    k = torch.from_numpy(oracle.bf16_bits_to_float(k_bits).astype(np.float64))
-    v = torch.from_numpy(oracle.bf16_bits_to_float(v_bits).astype(np.float64))
+    return dense_attention_f64(oracle.bf16_bits_to_float(q_bits), oracle.bf16_bits_to_float(k_bits),
+                               oracle.bf16_bits_to_float(v_bits), scale, mask)
+
+
+def dense_attention_f64(q, k, v, scale, mask):
+    """dense_attention over real-valued rows (numpy, any float dtype)."""
+    q = torch.from_numpy(np.asarray(q, dtype=np.float64))
+    k = torch.from_numpy(np.asarray(k, dtype=np.float64))
+    v = torch.from_numpy(np.asarray(v, dtype=np.float64))
     Hq, Hkv = q.shape[1], k.shape[1]
     G = Hq // Hkv
     qh = q.permute(1, 0, 2)                                  # [Hq, K, D]
@@ -442,6 +448,92 @@ def test_dense_suffix_equals_dense_attention(oracle_mod, W, fk, r):
 
 
 # ----------------------------------------------------------------------------
+# fp8 (E4M3) context storage
+# ----------------------------------------------------------------------------
+
+def torch_e4m3(codes):
+    """torch's own float8_e4m3fn decoding of uint8 codes, as float64."""
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def random_e4m3(rng, shape, sigma=1.0):
+    """E4M3 codes of normal samples, rounded by torch's float8_e4m3fn cast."""
+    x = torch.from_numpy(rng.normal(0.0, sigma, size=shape).astype(np.float32))
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch(oracle_mod):
+    """Every one of the 256 codes decodes as torch's float8_e4m3fn does (NaN
+    for S.1111.111 only; 448 the largest finite value; 2^-9 the smallest)."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle_mod.e4m3_to_float64(codes)
+    ref = torch_e4m3(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert set(np.flatnonzero(np.isnan(got))) == {0x7F, 0xFF}
+    np.testing.assert_array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0 and got[0xB8] == -1.0
+
+
+def _fp8_case(rng, lens, Hq, Hkv, D, K, P, sigma=1.0):
+    """Queries, dense block rows (bf16 bits), fp8 context codes scattered to
+    pages (unused slots hold the NaN code), and the context codes per request."""
+    B = len(lens)
+    q = random_bf16(rng, (B, K, Hq, D), sigma)
+    kb = random_bf16(rng, (B, K, Hkv, D), sigma)
+    vb = random_bf16(rng, (B, K, Hkv, D), sigma)
+    ck = [random_e4m3(rng, (L, Hkv, D), sigma) for L in lens]
+    cv = [random_e4m3(rng, (L, Hkv, D), sigma) for L in lens]
+    kp, vp, tab = scatter_to_pages(rng, ck, cv, P, Hkv, D, extra_pages=2, extra_slots=1,
+                                   fill_bits=0x7F, dtype=np.uint8)
+    return q, kb, vb, ck, cv, kp, vp, tab, np.asarray(lens, dtype=np.int32)
+
+
+@pytest.mark.parametrize("W,fk,r", [(0, 1, 0), (6, 1, 0), (0, 0, 2), (3, 0, 0)])
+def test_fp8_context_power_of_two_scales_is_the_bf16_form(oracle_mod, W, fk, r):
+    """With power-of-two scales every dequantised context value is a bf16
+    value: the fp8 form must equal, bit for bit, the bf16 dense-suffix form
+    over pages holding those values (a scale applied to the block rows, the
+    K scale used for V, or a decoding slip all break this)."""
+    rng = np.random.default_rng(2100 + W + 10 * r)
+    K, Hq, Hkv, D, P = 4, 4, 2, 8, 3
+    lens = [0, 2, 5, 17]
+    q, kb, vb, ck, cv, kp8, vp8, tab, ctx = _fp8_case(rng, lens, Hq, Hkv, D, K, P)
+    ks, vs = 0.25, 8.0
+    kp16 = oracle_mod.bf16_bits_from_float((torch_e4m3(kp8) * ks).astype(np.float32))
+    vp16 = oracle_mod.bf16_bits_from_float((torch_e4m3(vp8) * vs).astype(np.float32))
+    args = dict(block_size=K, window=W, future_keys=fk, right_window=r, scale=0.41)
+    out8, lse8 = oracle_mod.block_attn_fp8(q, kp8, vp8, tab, ctx, k_scale=ks, v_scale=vs, k_block=kb,
+                                           v_block=vb, **args)
+    out16, lse16 = oracle_mod.block_attn(q, kp16, vp16, tab, ctx, k_block=kb, v_block=vb, **args)
+    np.testing.assert_array_equal(out8, out16)
+    np.testing.assert_array_equal(lse8, lse16)
+
+
+@pytest.mark.parametrize("W,fk,r", [(0, 1, 0), (5, 1, 0), (2, 0, 1)])
+def test_fp8_context_equals_dense_attention(oracle_mod, W, fk, r):
+    """General scales: torch SDPA in float64 over the contiguous sequence of
+    (torch-decoded context codes x scale) followed by the bf16 block rows."""
+    import oracle
+
+    rng = np.random.default_rng(2200 + W + 10 * r)
+    K, Hq, Hkv, D, P = 3, 6, 3, 8, 4
+    lens = [0, 1, 7, 21]
+    q, kb, vb, ck, cv, kp8, vp8, tab, ctx = _fp8_case(rng, lens, Hq, Hkv, D, K, P)
+    ks, vs = 0.0371, 1.7
+    out, lse2 = oracle_mod.block_attn_fp8(q, kp8, vp8, tab, ctx, k_scale=ks, v_scale=vs, k_block=kb,
+                                          v_block=vb, block_size=K, window=W, future_keys=fk,
+                                          right_window=r, scale=0.52)
+    for b, L in enumerate(lens):
+        k = np.concatenate([torch_e4m3(ck[b]) * ks, oracle.bf16_bits_to_float(kb[b]).astype(np.float64)])
+        v = np.concatenate([torch_e4m3(cv[b]) * vs, oracle.bf16_bits_to_float(vb[b]).astype(np.float64)])
+        qf = oracle.bf16_bits_to_float(q[b]).astype(np.float64)
+        ro, rl = dense_attention_f64(qf, k, v, 0.52, visible_mask(L, K, W, fk, r))
+        np.testing.assert_allclose(out[b], ro, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse2[b], rl, rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
 # Errors
 # ----------------------------------------------------------------------------
 
@@ -564,6 +656,61 @@ def _move_pins_pass(lib) -> bool:
     except ValueError:
         return False
     return True
+
+
+# Planted mistakes in the fp8 context reading, each caught by an fp8 pin.
+FP8_MUTANTS = [
+    ("e4m3 bias off by one", "std::ldexp(static_cast<double>(8 + m), e - 10)",
+     "std::ldexp(static_cast<double>(8 + m), e - 9)"),
+    ("e4m3 subnormals read as normals", "e == 0 ? std::ldexp(static_cast<double>(m), -9)",
+     "e == 0 ? std::ldexp(static_cast<double>(8 + m), -10)"),
+    ("k scale dropped", "RowRef{nullptr, pr.k_pages8 + o, pr.k_scale}", "RowRef{nullptr, pr.k_pages8 + o, 1.0}"),
+    ("v read with the k scale", "RowRef{nullptr, pr.v_pages8 + o, pr.v_scale}",
+     "RowRef{nullptr, pr.v_pages8 + o, pr.k_scale}"),
+    ("block rows scaled too", "krow[t] = RowRef{pr.k_block + o, nullptr, 1.0};",
+     "krow[t] = RowRef{pr.k_block + o, nullptr, pr.k_pages8 ? pr.k_scale : 1.0};"),
+]
+
+
+def _fp8_pins_pass(lib) -> bool:
+    """The decoding pin and one power-of-two-scale reduction, against a build."""
+    import oracle
+
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_to_float64(codes, lib=lib)
+    ref = torch_e4m3(codes)
+    if not (np.array_equal(np.isnan(got), np.isnan(ref)) and
+            np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])):
+        return False
+    rng = np.random.default_rng(77)
+    K, Hq, Hkv, D, P = 3, 4, 2, 8, 4
+    q, kb, vb, ck, cv, kp8, vp8, tab, ctx = _fp8_case(rng, [0, 6, 13], Hq, Hkv, D, K, P)
+    ks, vs = 0.5, 4.0
+    kp16 = oracle.bf16_bits_from_float((torch_e4m3(kp8) * ks).astype(np.float32))
+    vp16 = oracle.bf16_bits_from_float((torch_e4m3(vp8) * vs).astype(np.float32))
+    args = dict(block_size=K, window=0, future_keys=1, scale=0.5)
+    try:
+        o8, l8 = oracle.block_attn_fp8(q, kp8, vp8, tab, ctx, k_scale=ks, v_scale=vs, k_block=kb,
+                                       v_block=vb, lib=lib, **args)
+    except ValueError:
+        return False
+    o16, l16 = oracle.block_attn(q, kp16, vp16, tab, ctx, k_block=kb, v_block=vb, **args)
+    return np.array_equal(o8, o16) and np.array_equal(l8, l16)
+
+
+def test_fp8_pins_reject_planted_mistakes(oracle_mod, tmp_path):
+    import oracle
+
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "dflash_oracle.cpp")).read()
+    assert _fp8_pins_pass(oracle._load())
+    for name, old, new in FP8_MUTANTS:
+        assert src.count(old) == 1, name
+        path = tmp_path / (name.replace(" ", "_") + ".cpp")
+        path.write_text(src.replace(old, new))
+        so = str(path) + ".so"
+        subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-pthread", str(path), "-o", so],
+                       check=True)
+        assert not _fp8_pins_pass(oracle.load_library(so)), f"planted mistake not caught: {name}"
 
 
 def test_move_pins_reject_planted_mistakes(oracle_mod, tmp_path):
