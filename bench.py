@@ -267,7 +267,12 @@ def main():
     ap.add_argument("--dense-suffix", action="store_true",
                     help="time dflash_block_attn_dense_suffix: the block's K/V from dense "
                          "tensors, the context from the pages")
+    ap.add_argument("--fp8-context", action="store_true",
+                    help="time dflash_block_attn_fp8_context: the dense-suffix form over E4M3 "
+                         "context pages (the seeded bf16 pages cast to fp8) with per-tensor scales")
     args = ap.parse_args()
+    if args.fp8_context:
+        args.dense_suffix = True
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
@@ -296,7 +301,8 @@ def main():
     p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K,
                           window=spec.window, future_keys=spec.future_keys,
                           scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len,
-                          right_window=spec.right_window)
+                          right_window=spec.right_window,
+                          kv_dtype=dflash.KV_FP8_E4M3 if args.fp8_context else dflash.KV_BF16)
     plan = dflash.plan(p)
     ws_bytes = dflash.workspace_size(p)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
@@ -318,8 +324,20 @@ def main():
                 kb[b, j] = inp["k_pages"][pg, :, off, :]
                 vb[b, j] = inp["v_pages"][pg, :, off, :]
 
+    if args.fp8_context:
+        # E4M3 codes of the same seeded values, with per-tensor scales.
+        kp8 = inp["k_pages"].float().to(torch.float8_e4m3fn).view(torch.uint8)
+        vp8 = inp["v_pages"].float().to(torch.float8_e4m3fn).view(torch.uint8)
+        k_scale, v_scale = 0.0431, 1.73
+
     def call():
-        if args.dense_suffix:
+        if args.fp8_context:
+            rc = dflash.block_attn_fp8_context_raw(
+                p, inp["q"].data_ptr(), kb.data_ptr(), vb.data_ptr(), kp8.data_ptr(), vp8.data_ptr(),
+                k_scale, v_scale, inp["page_table"].data_ptr(), inp["ctx_lens"].data_ptr(),
+                out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws_bytes,
+                torch.cuda.current_stream().cuda_stream)
+        elif args.dense_suffix:
             rc = dflash.block_attn_dense_suffix_raw(
                 p, inp["q"].data_ptr(), kb.data_ptr(), vb.data_ptr(), inp["k_pages"].data_ptr(),
                 inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(), inp["ctx_lens"].data_ptr(),
@@ -387,10 +405,16 @@ def main():
     e1.record(stream)
     for k in range(max(3, min(args.steps, 20))):
         flush.fill_(k & 0xFF)
-        rc = dflash.block_attn_timed_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
-                                         inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(),
-                                         inp["ctx_lens"].data_ptr(), out.data_ptr(), lse.data_ptr(),
-                                         ws.data_ptr(), ws_bytes, stream.cuda_stream, e0, e1)
+        if args.fp8_context:
+            rc = dflash.block_attn_fp8_context_timed_raw(
+                p, inp["q"].data_ptr(), kb.data_ptr(), vb.data_ptr(), kp8.data_ptr(), vp8.data_ptr(),
+                k_scale, v_scale, inp["page_table"].data_ptr(), inp["ctx_lens"].data_ptr(),
+                out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws_bytes, stream.cuda_stream, e0, e1)
+        else:
+            rc = dflash.block_attn_timed_raw(p, inp["q"].data_ptr(), inp["k_pages"].data_ptr(),
+                                             inp["v_pages"].data_ptr(), inp["page_table"].data_ptr(),
+                                             inp["ctx_lens"].data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                             ws.data_ptr(), ws_bytes, stream.cuda_stream, e0, e1)
         if rc != 0:
             raise dflash.DflashError(rc)
         e2.record(stream)
@@ -435,7 +459,7 @@ def main():
     e2e_ms = sum(a.elapsed_time(b) for a, b in ee) / len(ee)
 
     # Max over ranks (time) and sum (bytes) for the whole-job figures.
-    kv_bytes = spec.kv_bytes()
+    kv_bytes = spec.kv_bytes(1 if args.fp8_context else 2)
     (ms, split_ms, e2e_ms), total_bytes = reduce_over_ranks([ms, split_ms, e2e_ms], kv_bytes, dev)
 
     peaks = measured_peaks()
@@ -454,7 +478,8 @@ def main():
                        l2="flushed before every timed call (512 MiB write)",
                        kv_bytes_per_call=kv_bytes, path=kernel, split_tiles=plan["split_tiles"],
                        max_splits=plan["max_splits"], ctas=plan["units"], cuda_graph=True,
-                       fused_append=bool(args.fused_append), dense_suffix=bool(args.dense_suffix)),
+                       fused_append=bool(args.fused_append), dense_suffix=bool(args.dense_suffix),
+                       fp8_context=bool(args.fp8_context)),
         "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": split_gbs / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": kernel, "kernel_us": split_ms * 1e3,

@@ -61,6 +61,11 @@ extern "C" {
 #define DFLASH_STATUS_TIMEOUT        4  /* a pipeline wait ran out (never expected) */
 
 /* Kernel-path selection for dflash_params.force_path. */
+/* Element type of the page pools (dflash_params.kv_dtype). */
+#define DFLASH_KV_BF16               0  /* bf16 pages: every entry point but the fp8 one */
+#define DFLASH_KV_FP8_E4M3           1  /* E4M3 codes with per-tensor scales:
+                                           dflash_block_attn_fp8_context only */
+
 #define DFLASH_PATH_AUTO             0
 #define DFLASH_PATH_MMA              1  /* warp-level mma.sync tiles (any R <= 128) */
 #define DFLASH_PATH_TCGEN05          2  /* tcgen05 / TMEM, one 128-row tile per kv head;
@@ -86,7 +91,9 @@ typedef struct dflash_params {
                                 the tcgen05 path (tests); 0 = planner */
   int32_t right_window;      /* with future_keys = 0: row i also sees block keys
                                 i+1 .. i+right_window (0 .. K-1); 0 when future_keys = 1 */
-  int32_t reserved[3];       /* must be zero */
+  int32_t kv_dtype;          /* DFLASH_KV_BF16 or DFLASH_KV_FP8_E4M3 (pool element type;
+                                the fp8 form always runs on the tcgen05 path) */
+  int32_t reserved[2];       /* must be zero */
 } dflash_params;
 
 /*
@@ -254,6 +261,43 @@ int dflash_block_attn_dense_suffix(const dflash_params* p, const void* q, const 
                                    const int32_t* page_table, const int32_t* ctx_lens, void* out,
                                    float* lse2, void* workspace, size_t workspace_bytes,
                                    void* stream);
+
+/*
+ * Dense-suffix form over fp8 context pages (PR #16150: the drafter reads its
+ * context from the target's paged pool and "supports fp8 context storage").
+ * Requires p->kv_dtype = DFLASH_KV_FP8_E4M3.  k_pages / v_pages hold OCP
+ * E4M3 codes, uint8 [num_pages, Hkv, P, D] (HND, 16-byte aligned), read as
+ * k = k_scale * e4m3(code) and v = v_scale * e4m3(code) with one
+ * dequantisation scale per pool (finite, > 0); they hold the context
+ * positions < L_b only (slots past ceil(L_b / P) are never read).  The
+ * block rows come from k_block / v_block, bf16 [B, K, Hkv, D], unscaled.
+ * q, out, lse2, ctx_lens, page_table and the workspace as dflash_block_attn
+ * (dflash_workspace_size(p) with the same *p).  The codes are widened to
+ * bf16 exactly on the chip; the scores and the output use the scales in
+ * fp32.  Runs on the tcgen05 path for any packed row count (R <= 128) and
+ * B <= 768; other plans are refused with DFLASH_ERR_INVALID, as are a
+ * forced mma.sync path and non-positive or non-finite scales.  Same return
+ * codes as dflash_block_attn.
+ */
+int dflash_block_attn_fp8_context(const dflash_params* p, const void* q, const void* k_block,
+                                  const void* v_block, const void* k_pages, const void* v_pages,
+                                  float k_scale, float v_scale, const int32_t* page_table,
+                                  const int32_t* ctx_lens, void* out, float* lse2, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * dflash_block_attn_fp8_context with the timing marks of
+ * dflash_block_attn_timed: `split_start` / `split_done` (cudaEvent_t or NULL)
+ * recorded on `stream` immediately before the split kernel and between the
+ * split and the combine kernel (which then starts after the event).  Same
+ * computation and return codes.
+ */
+int dflash_block_attn_fp8_context_timed(const dflash_params* p, const void* q, const void* k_block,
+                                        const void* v_block, const void* k_pages, const void* v_pages,
+                                        float k_scale, float v_scale, const int32_t* page_table,
+                                        const int32_t* ctx_lens, void* out, float* lse2,
+                                        void* workspace, size_t workspace_bytes, void* stream,
+                                        void* split_start, void* split_done);
 
 /* Static text for a return code. */
 const char* dflash_status_string(int status);

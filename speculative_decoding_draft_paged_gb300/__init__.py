@@ -18,13 +18,16 @@ from typing import Optional
 from . import _lib
 from ._lib import (DFLASH_ERR_DEVICE, DFLASH_ERR_INVALID, DFLASH_ERR_LAUNCH, DFLASH_ERR_WORKSPACE,
                    DFLASH_OK, DFLASH_STATUS_BAD_CTX_LEN, DFLASH_STATUS_BAD_PAGE,
-                   DFLASH_STATUS_TIMEOUT, PATH_AUTO, PATH_MMA, PATH_TCGEN05, Params, PlanInfo)
+                   DFLASH_STATUS_TIMEOUT, KV_BF16, KV_FP8_E4M3, PATH_AUTO, PATH_MMA, PATH_TCGEN05,
+                   Params, PlanInfo)
 
 __all__ = [
     "Params", "PlanInfo", "DflashError", "make_params", "workspace_size", "plan", "block_attn",
     "block_attn_raw", "block_attn_timed_raw", "read_device_status", "clear_device_status", "version", "PATH_AUTO",
     "block_placement", "append_block_kv", "block_attn_append", "block_attn_append_raw",
     "block_attn_dense_suffix", "block_attn_dense_suffix_raw",
+    "block_attn_fp8_context", "block_attn_fp8_context_raw", "block_attn_fp8_context_timed_raw",
+    "KV_BF16", "KV_FP8_E4M3",
     "PATH_MMA", "PATH_TCGEN05", "DFLASH_OK", "DFLASH_ERR_INVALID", "DFLASH_ERR_WORKSPACE",
     "DFLASH_ERR_DEVICE", "DFLASH_ERR_LAUNCH", "DFLASH_STATUS_BAD_PAGE",
     "DFLASH_STATUS_BAD_CTX_LEN", "DFLASH_STATUS_TIMEOUT",
@@ -39,7 +42,7 @@ class DflashError(RuntimeError):
 
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_req,
                 num_pages, block_size, window, future_keys, scale, max_ctx_len, force_path=0,
-                force_split_tiles=0, right_window=0) -> Params:
+                force_split_tiles=0, right_window=0, kv_dtype=0) -> Params:
     p = Params()
     p.batch = batch
     p.num_q_heads = num_q_heads
@@ -56,11 +59,12 @@ def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pa
     p.force_path = force_path
     p.force_split_tiles = force_split_tiles
     p.right_window = right_window
+    p.kv_dtype = kv_dtype
     return p
 
 
 def params_for(q, k_pages, page_table, *, block_size, window, future_keys, scale, max_ctx_len,
-               force_path=0, force_split_tiles=0, right_window=0) -> Params:
+               force_path=0, force_split_tiles=0, right_window=0, kv_dtype=0) -> Params:
     B, K, Hq, D = q.shape
     num_pages, Hkv, P, _ = k_pages.shape
     if K != block_size:
@@ -69,7 +73,8 @@ def params_for(q, k_pages, page_table, *, block_size, window, future_keys, scale
                        max_pages_per_req=page_table.shape[1], num_pages=num_pages,
                        block_size=block_size, window=window, future_keys=future_keys, scale=scale,
                        max_ctx_len=max_ctx_len, force_path=force_path,
-                       force_split_tiles=force_split_tiles, right_window=right_window)
+                       force_split_tiles=force_split_tiles, right_window=right_window,
+                       kv_dtype=kv_dtype)
 
 
 def workspace_size(p: Params) -> int:
@@ -285,6 +290,67 @@ def block_attn_dense_suffix(q, k_block, v_block, k_pages, v_pages, page_table, c
                                      workspace.data_ptr(),
                                      workspace.numel() * workspace.element_size(),
                                      _stream_handle(stream))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+    return out, lse2
+
+
+def block_attn_fp8_context_raw(p: Params, q_ptr, kb_ptr, vb_ptr, k_ptr, v_ptr, k_scale, v_scale,
+                               table_ptr, lens_ptr, out_ptr, lse_ptr, ws_ptr, ws_bytes,
+                               stream_handle) -> int:
+    """Direct C-ABI call of the fp8-context form; returns the status code."""
+    return int(_lib.load().dflash_block_attn_fp8_context(
+        ctypes.byref(p), q_ptr, kb_ptr, vb_ptr, k_ptr, v_ptr, float(k_scale), float(v_scale),
+        table_ptr, lens_ptr, out_ptr, lse_ptr, ws_ptr, ws_bytes, stream_handle))
+
+
+def block_attn_fp8_context_timed_raw(p: Params, q_ptr, kb_ptr, vb_ptr, k_ptr, v_ptr, k_scale, v_scale,
+                                     table_ptr, lens_ptr, out_ptr, lse_ptr, ws_ptr, ws_bytes,
+                                     stream_handle, split_start=None, split_done=None) -> int:
+    """The fp8-context call with timing marks (torch.cuda.Event or None)."""
+    def handle(e):
+        return None if e is None else ctypes.c_void_p(e.cuda_event)
+
+    return int(_lib.load().dflash_block_attn_fp8_context_timed(
+        ctypes.byref(p), q_ptr, kb_ptr, vb_ptr, k_ptr, v_ptr, float(k_scale), float(v_scale),
+        table_ptr, lens_ptr, out_ptr, lse_ptr, ws_ptr, ws_bytes, stream_handle, handle(split_start),
+        handle(split_done)))
+
+
+def block_attn_fp8_context(q, k_block, v_block, k_pages, v_pages, page_table, ctx_lens, *,
+                           k_scale: float, v_scale: float, block_size: int, window: int,
+                           future_keys: int, scale: float, max_ctx_len: int, out=None, lse2=None,
+                           workspace=None, stream=None, force_split_tiles: int = 0,
+                           right_window: int = 0):
+    """Dense-suffix form over fp8 context pages: ``k_pages``/``v_pages`` are
+    uint8 E4M3 codes ``[num_pages, Hkv, P, D]`` dequantised by the per-tensor
+    scales; the block rows ``[B, K, Hkv, D]`` are bf16.  Returns ``(out, lse2)``."""
+    import torch
+
+    B, K, Hq, D = q.shape
+    if k_pages.dtype != torch.uint8 or v_pages.dtype != torch.uint8:
+        raise ValueError("fp8 pages are uint8 E4M3 codes")
+    _check_block("k_block", k_block, (B, K, k_pages.shape[1], D))
+    _check_block("v_block", v_block, (B, K, k_pages.shape[1], D))
+    p = params_for(q, k_pages, page_table, block_size=block_size, window=window,
+                   future_keys=future_keys, scale=scale, max_ctx_len=max_ctx_len,
+                   force_split_tiles=force_split_tiles, right_window=right_window,
+                   kv_dtype=KV_FP8_E4M3)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse2 is None:
+        lse2 = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    need = workspace_size(p)
+    if need == 0:
+        raise DflashError(DFLASH_ERR_INVALID)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    rc = block_attn_fp8_context_raw(p, q.data_ptr(), k_block.data_ptr(), v_block.data_ptr(),
+                                    k_pages.data_ptr(), v_pages.data_ptr(), k_scale, v_scale,
+                                    page_table.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
+                                    lse2.data_ptr(), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream_handle(stream))
     if rc != DFLASH_OK:
         raise DflashError(rc)
     return out, lse2

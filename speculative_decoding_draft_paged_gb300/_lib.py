@@ -23,6 +23,9 @@ DFLASH_STATUS_BAD_PAGE = 1
 DFLASH_STATUS_BAD_CTX_LEN = 2
 DFLASH_STATUS_TIMEOUT = 4
 
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+
 PATH_AUTO = 0
 PATH_MMA = 1
 PATH_TCGEN05 = 2
@@ -37,6 +40,8 @@ EXPORTS = (
     "dflash_append_block_kv",
     "dflash_block_attn_append",
     "dflash_block_attn_dense_suffix",
+    "dflash_block_attn_fp8_context",
+    "dflash_block_attn_fp8_context_timed",
     "dflash_status_string",
     "dflash_read_device_status",
     "dflash_clear_device_status",
@@ -61,7 +66,8 @@ class Params(ctypes.Structure):
         ("force_path", ctypes.c_int32),
         ("force_split_tiles", ctypes.c_int32),
         ("right_window", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("kv_dtype", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -121,6 +127,13 @@ def load() -> ctypes.CDLL:
             lib.dflash_block_attn_append.restype = i32
             lib.dflash_block_attn_dense_suffix.argtypes = lib.dflash_block_attn_append.argtypes
             lib.dflash_block_attn_dense_suffix.restype = i32
+            f32 = ctypes.c_float
+            lib.dflash_block_attn_fp8_context.argtypes = [ctypes.POINTER(Params)] + [vp] * 5 + \
+                [f32, f32] + [vp] * 5 + [ctypes.c_size_t, vp]
+            lib.dflash_block_attn_fp8_context.restype = i32
+            lib.dflash_block_attn_fp8_context_timed.argtypes = \
+                lib.dflash_block_attn_fp8_context.argtypes + [vp, vp]
+            lib.dflash_block_attn_fp8_context_timed.restype = i32
             lib.dflash_status_string.argtypes = [i32]
             lib.dflash_status_string.restype = ctypes.c_char_p
             lib.dflash_read_device_status.argtypes = [vp, vp]

@@ -93,6 +93,9 @@ bool params_valid(const dflash_params* p) {
     return false;
   if (p->force_path < DFLASH_PATH_AUTO || p->force_path > DFLASH_PATH_TCGEN05) return false;
   if (p->force_split_tiles < 0 || p->force_split_tiles > kMaxSplitTiles) return false;
+  if (p->kv_dtype != DFLASH_KV_BF16 && p->kv_dtype != DFLASH_KV_FP8_E4M3) return false;
+  // fp8 pages are widened by the tcgen05 kernel only.
+  if (p->kv_dtype == DFLASH_KV_FP8_E4M3 && p->force_path == DFLASH_PATH_MMA) return false;
   return true;
 }
 
@@ -115,7 +118,10 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
                            max_tiles(p->max_ctx_len, p->block_size, p->window, split_tc_tile_keys(D));
   const bool tc_ok = split_tc_available() && p->batch <= kTcMaxBatch && tc_tiles <= (int64_t(1) << 30);
   int path = p->force_path;
-  if (path == DFLASH_PATH_AUTO) path = (k.R > 64 && tc_ok) ? DFLASH_PATH_TCGEN05 : DFLASH_PATH_MMA;
+  if (path == DFLASH_PATH_AUTO)
+    path = ((k.R > 64 || p->kv_dtype == DFLASH_KV_FP8_E4M3) && tc_ok) ? DFLASH_PATH_TCGEN05
+                                                                      : DFLASH_PATH_MMA;
+  if (p->kv_dtype == DFLASH_KV_FP8_E4M3 && path != DFLASH_PATH_TCGEN05) return false;
   if (path == DFLASH_PATH_TCGEN05 && !tc_ok) return false;
   k.path = path;
   if (path == DFLASH_PATH_MMA) {
@@ -251,6 +257,29 @@ bool encode_pool(CUtensorMap* map, const void* pool, const dflash_params* p) {
   return r == CUDA_SUCCESS;
 }
 
+// fp8 context: 4-D view [num_pages][Hkv][P][D] of a pool of E4M3 codes, box
+// = (D codes, P rows, one head, one page), rows packed at D bytes with the
+// swizzle of that row length (128-byte for D = 128, 64-byte for D = 64),
+// zero fill outside the pool.
+bool encode_pool_fp8(CUtensorMap* map, const void* pool, const dflash_params* p) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(p->head_dim),
+                              static_cast<cuuint64_t>(p->page_size),
+                              static_cast<cuuint64_t>(p->num_kv_heads),
+                              static_cast<cuuint64_t>(p->num_pages)};
+  const cuuint64_t row = static_cast<cuuint64_t>(p->head_dim);
+  const cuuint64_t strides[3] = {row, row * p->page_size, row * p->page_size * p->num_kv_heads};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(p->head_dim), static_cast<cuuint32_t>(p->page_size), 1,
+                             1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(pool), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        p->head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D view [B*K][Hq][D] of the queries (or of the output), box = (64
 // columns, G heads, K tokens): one box is the packed tile of one (request,
 // kv head) pair, rows r = i*G + g, for one 64-column half; 128-byte swizzle.
@@ -333,13 +362,25 @@ AppendArgs append_args(const dflash_params* p, const void* k_block, const void* 
 // The attention call; with `append` given, the K/V append runs first and the
 // split kernel is its programmatic dependent (its producers wait for it).
 // With dense_k / dense_v given (dense-suffix form) the block rows come from
-// them and the pages hold the context only.
+// them and the pages hold the context only; with fp8 given as well, the
+// pages hold E4M3 codes dequantised by fp8->k_scale / fp8->v_scale.
+struct Fp8Scales {
+  float k_scale, v_scale;
+};
+
 int run_attention(const dflash_params* p, const void* q, const void* k_pages, const void* v_pages,
                   const int32_t* page_table, const int32_t* ctx_lens, void* out, float* lse2,
                   void* workspace, size_t workspace_bytes, void* stream, void* split_start,
                   void* split_done, const AppendArgs* append, const void* dense_k = nullptr,
-                  const void* dense_v = nullptr) {
+                  const void* dense_v = nullptr, const Fp8Scales* fp8 = nullptr) {
   if (!params_valid(p)) return DFLASH_ERR_INVALID;
+  if ((fp8 != nullptr) != (p->kv_dtype == DFLASH_KV_FP8_E4M3)) return DFLASH_ERR_INVALID;
+  if (fp8 != nullptr) {
+    if (dense_k == nullptr || append != nullptr) return DFLASH_ERR_INVALID;
+    if (!std::isfinite(fp8->k_scale) || !(fp8->k_scale > 0.f) || !std::isfinite(fp8->v_scale) ||
+        !(fp8->v_scale > 0.f))
+      return DFLASH_ERR_INVALID;
+  }
   if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !out || !lse2 || !workspace)
     return DFLASH_ERR_INVALID;
   if ((dense_k == nullptr) != (dense_v == nullptr) || !aligned(dense_k, 16) || !aligned(dense_v, 16))
@@ -358,7 +399,11 @@ int run_attention(const dflash_params* p, const void* q, const void* k_pages, co
 
   const bool tc = k.path == DFLASH_PATH_TCGEN05;
   CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_part;
-  if (!encode_pool(&tm_k, k_pages, p) || !encode_pool(&tm_v, v_pages, p)) return DFLASH_ERR_LAUNCH;
+  if (fp8 != nullptr) {
+    if (!encode_pool_fp8(&tm_k, k_pages, p) || !encode_pool_fp8(&tm_v, v_pages, p)) return DFLASH_ERR_LAUNCH;
+  } else if (!encode_pool(&tm_k, k_pages, p) || !encode_pool(&tm_v, v_pages, p)) {
+    return DFLASH_ERR_LAUNCH;
+  }
 
   AttnArgs a{};
   a.q = static_cast<const uint16_t*>(q);
@@ -400,6 +445,16 @@ int run_attention(const dflash_params* p, const void* q, const void* k_pages, co
   a.qn_force = tc ? p->force_split_tiles : 0;
   a.qn_min = kTcMinTiles;
   a.seg_cost = tc ? k.seg_cost : 0;
+  a.fp8 = fp8 != nullptr ? 1 : 0;
+  a.kblk_mul = 1.f;
+  a.pblk_mul = 1.f;
+  a.out_mul = 1.f;
+  if (fp8 != nullptr) {
+    a.scale_log2 *= fp8->k_scale;
+    a.kblk_mul = 1.f / fp8->k_scale;
+    a.pblk_mul = 1.f / fp8->v_scale;
+    a.out_mul = fp8->v_scale;
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (split_start != nullptr &&
@@ -479,6 +534,28 @@ int dflash_block_attn_dense_suffix(const dflash_params* p, const void* q, const 
                        workspace_bytes, stream, nullptr, nullptr, nullptr, k_block, v_block);
 }
 
+int dflash_block_attn_fp8_context(const dflash_params* p, const void* q, const void* k_block,
+                                  const void* v_block, const void* k_pages, const void* v_pages,
+                                  float k_scale, float v_scale, const int32_t* page_table,
+                                  const int32_t* ctx_lens, void* out, float* lse2, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return dflash_block_attn_fp8_context_timed(p, q, k_block, v_block, k_pages, v_pages, k_scale, v_scale,
+                                             page_table, ctx_lens, out, lse2, workspace, workspace_bytes,
+                                             stream, nullptr, nullptr);
+}
+
+int dflash_block_attn_fp8_context_timed(const dflash_params* p, const void* q, const void* k_block,
+                                        const void* v_block, const void* k_pages, const void* v_pages,
+                                        float k_scale, float v_scale, const int32_t* page_table,
+                                        const int32_t* ctx_lens, void* out, float* lse2,
+                                        void* workspace, size_t workspace_bytes, void* stream,
+                                        void* split_start, void* split_done) {
+  if (k_block == nullptr || v_block == nullptr) return DFLASH_ERR_INVALID;
+  const Fp8Scales sc{k_scale, v_scale};
+  return run_attention(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2, workspace,
+                       workspace_bytes, stream, split_start, split_done, nullptr, k_block, v_block, &sc);
+}
+
 int dflash_block_placement(const dflash_params* p, const int32_t* page_table,
                            const int32_t* ctx_lens, int32_t* placement, void* workspace,
                            void* stream) {
@@ -497,8 +574,9 @@ int dflash_block_placement(const dflash_params* p, const int32_t* page_table,
 int dflash_append_block_kv(const dflash_params* p, const void* k_block, const void* v_block,
                            void* k_pages, void* v_pages, const int32_t* page_table,
                            const int32_t* ctx_lens, void* workspace, void* stream) {
-  if (!params_valid(p) || !append_pointers_ok(k_block, v_block, k_pages, v_pages, page_table,
-                                              ctx_lens, workspace))
+  // The append copies bf16 rows: fp8 pools are written by their owner.
+  if (!params_valid(p) || p->kv_dtype != DFLASH_KV_BF16 ||
+      !append_pointers_ok(k_block, v_block, k_pages, v_pages, page_table, ctx_lens, workspace))
     return DFLASH_ERR_INVALID;
   const int rc = check_device();
   if (rc != DFLASH_OK) return rc;

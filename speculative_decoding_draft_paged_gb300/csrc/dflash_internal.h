@@ -56,6 +56,14 @@ struct AttnArgs {
   int qn_force;               // tiles per CTA range if > 0, else from the lengths
   int qn_min;                 // fewest cost units per CTA range (lengths-derived case)
   int seg_cost;               // cost units (tile times) of a segment's end, per pair
+  // fp8 context (tcgen05 kernel, dense-suffix form): the pages hold E4M3
+  // codes, dequantised by per-tensor scales.  scale_log2 then includes
+  // k_scale; a block key's raw score is multiplied by kblk_mul = 1/k_scale,
+  // a block value row by pblk_mul = 1/v_scale as it is written into the
+  // value tile, and the output by out_mul = v_scale.  All three are 1
+  // otherwise.
+  int fp8;
+  float kblk_mul, pblk_mul, out_mul;
 };
 
 // Per-(request, kv head) key-range geometry of the split kernel, which covers

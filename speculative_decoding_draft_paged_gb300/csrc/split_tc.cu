@@ -42,8 +42,14 @@
 //                    columns, the A operand of the PV MMA.  At the end of each
 //                    segment both groups merge the two states, each for half
 //                    of the output columns, and write them.
+// fp8 context (dense-suffix form over E4M3 pages): each tile's codes land by
+// TMA in the upper part of its bf16 ring stage and are widened there to the
+// bf16 tile the MMAs read -- the K tiles by warps 10 and 11 (even and odd
+// tiles), each V tile by the softmax group that owns it -- and the
+// per-tensor scales fold into the score scale and the output.
 // Every mbarrier wait is bounded (DFLASH_STATUS_TIMEOUT, then drain).
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -66,8 +72,12 @@ struct TcCfg {
   static constexpr int kOffStage = kOffV + NSV * kTileBytes;
   static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
   // k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
-  // s_free[2], p_full[2], pv_done[2], q_full, q_free, k_fix[NSK]
-  static constexpr int kNumBars = 3 * NSK + 2 * NSV + 10;
+  // s_free[2], p_full[2], pv_done[2], q_full, q_free, k_fix[NSK], v_read[2]
+  static constexpr int kNumBars = 3 * NSK + 2 * NSV + 12;
+  // fp8 context: a stage's codes sit at byte kCodeOff of the stage, row r in
+  // [kCodeOff + r*D, +D) (the bf16 tile's second half for D = 128), its
+  // 16-byte words permuted by the TMA swizzle.
+  static constexpr int kCodeOff = T * D;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffXchg = kOffMisc + 64;                 // both groups' (m, l) per row
   static constexpr int kOffPB = kOffXchg + 2 * 128 * 8;          // tile prefix per request
@@ -88,6 +98,162 @@ struct TcCfg {
 constexpr int kNoPage = -0x7fffffff - 1;  // page-table slot outside the keys a pair reads
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+
+// Two E4M3 codes (low 16 bits of `codes`, first code lowest) -> bf16x2,
+// exactly: cvt.rn.f16x2.e4m3x2 (every E4M3 value is an f16 value), f16 ->
+// f32, and the upper half of each f32 (at most 4 significant bits, so the
+// lower half is zero).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(codes)));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
+}
+
+// Byte offset of 16-byte word w of code row r in a stage's code area: the
+// boxes land with the TMA swizzle of their row length (128-byte swizzle for
+// D = 128: word w of row r at r*128 + (w ^ (r & 7))*16; 64-byte swizzle for
+// D = 64: at r*64 + (w ^ ((r >> 1) & 3))*16), so that a warp reading one
+// word per row hits every bank.
+template <int D>
+__device__ __forceinline__ int code_word(int r, int w) {
+  if constexpr (D == 128) return r * 128 + ((w ^ (r & 7)) << 4);
+  else return r * 64 + ((w ^ ((r >> 1) & 3)) << 4);
+}
+
+// Eight codes (two words) -> one 16-byte chunk of eight bf16 values.
+__device__ __forceinline__ uint4 widen8(uint32_t w0, uint32_t w1) {
+  return make_uint4(e4m3x2_to_bf16x2(w0), e4m3x2_to_bf16x2(w0 >> 16), e4m3x2_to_bf16x2(w1),
+                    e4m3x2_to_bf16x2(w1 >> 16));
+}
+
+// One warp widens a K tile in place: lane l takes rows l and l + 32.  With
+// D = 128 a row's bf16 bytes overwrite only its own codes (its second half
+// is where they landed): word w's two bf16 chunks land where code words
+// 2w-8 and 2w-7 were, so the words are widened in order, one at a time.
+// With D = 64 a bf16 row covers the codes of two other rows, so both rows
+// of every lane are read before any byte is written.  Rows at positions
+// >= L are left alone (block rows, written next, or keys no row sees).
+// Loops are kept rolled: this code runs beside the softmax on the same SM
+// and competes with it for instruction-cache space.
+template <int D, int T>
+__device__ __forceinline__ void widen_k_tile(uint8_t* tile, int p0, int L, int lane) {
+  if constexpr (D == 128) {
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = lane + 32 * hh;
+      if (p0 + r >= L) continue;
+#pragma unroll 1
+      for (int w = 0; w < D / 16; ++w) {
+        const uint4 c = *reinterpret_cast<const uint4*>(tile + T * D + code_word<D>(r, w));
+        *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8(c.x, c.y);
+        *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8(c.z, c.w);
+      }
+    }
+  } else {
+    uint4 raw[2][D / 16];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int w = 0; w < D / 16; ++w)
+        raw[hh][w] = *reinterpret_cast<const uint4*>(tile + T * D + code_word<D>(lane + 32 * hh, w));
+    __syncwarp();
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = lane + 32 * hh;
+      if (p0 + r >= L) continue;
+#pragma unroll
+      for (int w = 0; w < D / 16; ++w) {
+        *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8(raw[hh][w].x, raw[hh][w].y);
+        *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8(raw[hh][w].z, raw[hh][w].w);
+      }
+    }
+  }
+}
+
+// The K fix of an fp8 tile, whole warp: once the codes have landed, widen
+// them, write the dense suffix's block rows the tile holds, and arrive on
+// k_fix.  False when the wait ran out.
+template <int D, int T>
+__device__ __noinline__ bool fp8_fix_k(const AttnArgs& a, uint8_t* tile, uint32_t full, uint32_t parity,
+                                          uint32_t fix, int p0, int L, int b, int h, int lane) {
+  if (!mbar_wait_warp(full, parity)) return false;
+  widen_k_tile<D, T>(tile, p0, L, lane);
+  if (p0 + T > L && p0 < L + a.K) write_suffix_rows<D, T>(tile, a.k_block, a, b, h, L, p0, p0, p0 + T, lane, 32);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(fix);
+  return true;
+}
+
+// The dense suffix's block value rows of a tile, moved from the staging
+// buffer (as write_staged_suffix) and multiplied by `mul` (1/v_scale: the
+// PV product then carries v_scale for every key, applied to the output).
+template <int D, int T, int MAXP>
+__device__ __forceinline__ void write_staged_suffix_scaled(uint8_t* tile, const uint8_t* stage, const AttnArgs& a,
+                                                           int L, int p0, int tid, int nthr, float mul) {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  constexpr int CPR = D / 8;
+  const int n = a.K * CPR;
+#pragma unroll 1
+  for (int k = 0; k < MAXP; ++k) {
+    const int e = tid + k * nthr;
+    if (e >= n) break;
+    const int j = e / CPR;
+    const int c = e - j * CPR;
+    const int rr = L + j - p0;
+    if (rr < 0 || rr >= T) continue;
+    const uint4 x = *reinterpret_cast<const uint4*>(stage + 16 * e);
+    auto sc = [&](uint32_t w) {
+      return pack_bf16x2(bf16_bits_to_f32(w & 0xffffu) * mul, bf16_bits_to_f32(w >> 16) * mul);
+    };
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * T * 128 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) =
+        make_uint4(sc(x.x), sc(x.y), sc(x.z), sc(x.w));
+  }
+}
+
+// D = 128: thread t of a softmax group's 128 widens V row t - 64 (t >= 64)
+// when its position lies in [lo, L): a row's bf16 bytes overwrite only its
+// own codes, so no other thread need wait.
+template <int T>
+__device__ __forceinline__ void widen_v_row(uint8_t* tile, int t, int p0, int lo, int L) {
+  constexpr int D = 128;
+  const int r = t - 64;
+  if (r < 0 || p0 + r < lo || p0 + r >= L) return;
+#pragma unroll 1
+  for (int w = 0; w < D / 16; ++w) {  // in order: see widen_k_tile
+    const uint4 c = *reinterpret_cast<const uint4*>(tile + T * D + code_word<D>(r, w));
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8(c.x, c.y);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8(c.z, c.w);
+  }
+}
+
+// D = 64: a bf16 row covers the codes of two other rows, so the group reads
+// first and writes after joining.  Thread t of the group's 128 takes row
+// t % 64, half t / 64 of its codes.
+template <int D, int T>
+__device__ __forceinline__ void read_v_codes(const uint8_t* tile, int t, uint4 (&raw)[D / 32]) {
+#pragma unroll
+  for (int w = 0; w < D / 32; ++w)
+    raw[w] = *reinterpret_cast<const uint4*>(tile + T * D + code_word<D>(t & 63, (t >> 6) * (D / 32) + w));
+}
+
+// Writes those codes widened, for rows at positions in [lo, L) (the
+// context rows some key of the block sees); other rows are zeroed or
+// written by the caller.
+template <int D, int T>
+__device__ __forceinline__ void write_v_widened(uint8_t* tile, int t, int p0, int lo, int L,
+                                                const uint4 (&raw)[D / 32]) {
+  const int r = t & 63;
+  const int pos = p0 + r;
+  if (pos < lo || pos >= L) return;
+  const int c0 = (t >> 6) * (D / 16);
+#pragma unroll 1
+  for (int w = 0; w < D / 32; ++w) {
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, c0 + 2 * w, T)) = widen8(raw[w].x, raw[w].y);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, c0 + 2 * w + 1, T)) = widen8(raw[w].z, raw[w].w);
+  }
+}
 
 // One segment of a CTA's range: the part of pair (b, h) inside it.
 struct Seg {
@@ -213,7 +379,7 @@ __device__ __noinline__ void store_segment_rows(const AttnArgs& a, const CUtenso
   }
 }
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(384, 1)
     split_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
@@ -270,6 +436,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t q_free = bars + 8u * (kB0 + 9);
   // Dense-suffix form: K tile st holds its block rows once k_fix(st) completes.
   auto k_fix = [&](int st) { return bars + 8u * (kB0 + 10 + st); };
+  // fp8 context: every thread of softmax group g has read its codes of the
+  // group's current V tile.
+  auto v_read = [&](int g) { return bars + 8u * (kB0 + 10 + NSK + g); };
   const bool dense = a.k_block != nullptr;
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile uint32_t* tmem_slot = misc;          // TMEM base address from tcgen05.alloc
@@ -298,6 +467,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(q_full, 1);
     mbar_init(q_free, 1);
     for (int st = 0; st < NSK; ++st) mbar_init(k_fix(st), 1);
+    mbar_init(v_read(0), 4);
+    mbar_init(v_read(1), 4);
     *abort_flag = 0;
     *issued_k = 0;
     *issued_v = 0;
@@ -334,16 +505,31 @@ __global__ void __launch_bounds__(384, 1)
   // combine kernel may launch and start on its input-only work.
   pdl_launch_dependents();
 
-  if (warp == 0 || warp == 10) {
+  if (FP8 && warp == 0) {
+    // ------------------------------------------------------------ fp8: even K tiles
+    // Warp 0 widens the even K tiles as soon as their codes land (the odd
+    // ones are warp 11's); warp 10 loads both rings.
+    Seg sgc = seg_first(PB, a.B, a.Hkv, start, end);
+    for (int jc = 0; jc < n; jc += 2) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      while (jc >= sgc.j1) seg_next(sgc, PB, a.Hkv, start, end);
+      const Geometry geo = make_geometry(Lc[sgc.b], a.max_ctx_len, a.K, a.W, T, 1);
+      const int p0 = (geo.t_begin - (sgc.g0 - start)) * T + jc * T;
+      const int st = jc % NSK;
+      if (!fp8_fix_k<D, T>(a, gbase + C::kOffK + st * C::kTileBytes, k_full(st), (jc / NSK) & 1, k_fix(st),
+                           p0, geo.L, sgc.b, sgc.h, lane)) {
+        if (lane == 0) flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+    }
+  } else if (warp == 0 || warp == 10) {
     // ------------------------------------------------------------ producers (whole warp)
     // Warp 0 reaches its first page-table shuffle about 2 us later than the
     // other warps (measured); the V tiles are needed a softmax later than the
-    // K tiles, so warp 0 takes the V ring.
+    // K tiles, so warp 0 takes the V ring.  fp8 context: warp 10 takes both
+    // rings (K then V per tile), one box of (D codes, P rows) per page each.
     const bool is_v = warp == 0;
-    const int ns = is_v ? NSV : NSK;
-    const uint32_t ring = is_v ? sV : sK;
-    const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-    volatile int* issued = is_v ? issued_v : issued_k;
     const int ppt = T / a.P;  // pages per tile: 1, 2 or 4
     const int tpc = 32 / ppt;  // tiles per page-id chunk
     auto checked = [&](int raw) {
@@ -375,27 +561,43 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int pj = 0; pj < 4; ++pj)
         pages[pj] = __shfl_sync(0xffffffffu, pg_cur, lane0 + (pj < ppt ? pj : 0));
-      const int st = j % ns;
-      const uint32_t empty = is_v ? v_empty(st) : k_empty(st);
-      const uint32_t full = is_v ? v_full(st) : k_full(st);
-      if (j >= ns && !mbar_wait_warp(empty, ((j / ns) - 1) & 1)) {
-        if (lane == 0) flag_status(a.status, DFLASH_STATUS_TIMEOUT);
-        *abort_flag = 1;
-      }
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, C::kTileBytes);
-        const uint32_t dst = ring + st * C::kTileBytes;
 #pragma unroll
-        for (int pj = 0; pj < 4; ++pj) {
-          if (pj >= ppt) break;
-#pragma unroll
-          for (int x = 0; x < D / 64; ++x)
-            tma_load_4d(dst + x * T * 128 + pj * a.P * 128, map, x * 64, 0, sg.h, pages[pj], full);
+      for (int rr = 0; rr < (FP8 ? 2 : 1); ++rr) {
+        const bool v_ring = FP8 ? rr == 1 : is_v;
+        const int ns = v_ring ? NSV : NSK;
+        const int st = j % ns;
+        const uint32_t empty = v_ring ? v_empty(st) : k_empty(st);
+        const uint32_t full = v_ring ? v_full(st) : k_full(st);
+        if (j >= ns && !mbar_wait_warp(empty, ((j / ns) - 1) & 1)) {
+          if (lane == 0) flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+          *abort_flag = 1;
         }
-        *issued = j + 1;
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        if (lane == 0) {
+          const uint32_t dst = (v_ring ? sV : sK) + st * C::kTileBytes;
+          const CUtensorMap* map = v_ring ? &tm_v : &tm_k;
+          if constexpr (FP8) {
+            mbar_arrive_expect_tx(full, T * D);
+#pragma unroll
+            for (int pj = 0; pj < 4; ++pj) {
+              if (pj >= ppt) break;
+              tma_load_4d(dst + C::kCodeOff + pj * a.P * D, map, 0, 0, sg.h, pages[pj], full);
+            }
+          } else {
+            mbar_arrive_expect_tx(full, C::kTileBytes);
+#pragma unroll
+            for (int pj = 0; pj < 4; ++pj) {
+              if (pj >= ppt) break;
+#pragma unroll
+              for (int x = 0; x < D / 64; ++x)
+                tma_load_4d(dst + x * T * 128 + pj * a.P * 128, map, x * 64, 0, sg.h, pages[pj], full);
+            }
+          }
+          *(v_ring ? issued_v : issued_k) = j + 1;
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      if (*abort_flag != 0) break;
     }
   } else if (warp == 11) {
     // ------------------------------------------------------------ query loader
@@ -427,7 +629,22 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (__shfl_sync(0xffffffffu, stop, 0)) break;
-      if (dense) {
+      if constexpr (FP8) {
+        // The odd K tiles of the segment (the even ones are warp 10's).
+        const Geometry geo = make_geometry(Lc[sg.b], a.max_ctx_len, a.K, a.W, T, 1);
+        const int pos_base = (geo.t_begin - (sg.g0 - start)) * T;
+        for (int j = sg.j0 | 1; j < sg.j1; j += 2) {
+          const int st = j % NSK;
+          if (!fp8_fix_k<D, T>(a, gbase + C::kOffK + st * C::kTileBytes, k_full(st), (j / NSK) & 1, k_fix(st),
+                               pos_base + j * T, geo.L, sg.b, sg.h, lane)) {
+            if (lane == 0) flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+            *abort_flag = 1;
+            stop = 1;
+            break;
+          }
+        }
+        if (stop) break;
+      } else if (dense) {
         const Geometry geo = make_geometry(Lc[sg.b], a.max_ctx_len, a.K, a.W, T, 1);
         const int pos_base = (geo.t_begin - (sg.g0 - start)) * T;
         bool loaded = false;
@@ -487,7 +704,10 @@ __global__ void __launch_bounds__(384, 1)
           q_seg = seg_j;
         }
         if (!mbar_wait(k_full(st), (j / NSK) & 1)) return false;
-        if (dense) {
+        if (FP8) {
+          // Every tile is widened (warp 10 or 11) before its QK^T.
+          if (!mbar_wait(k_fix(st), (j / NSK) & 1)) return false;
+        } else if (dense) {
           // A tile holding block positions waits for its block rows.
           const Geometry geo = make_geometry(Lc[sg.b], a.max_ctx_len, a.K, a.W, T, 1);
           const int p0 = (geo.t_begin - (sg.g0 - start)) * T + j * T;
@@ -609,6 +829,42 @@ __global__ void __launch_bounds__(384, 1)
         if (v_suffix)
           stage_suffix_async<D, kVPieces>(base + C::kOffVStage + grp * C::kVStageBytes, a.v_block, a,
                                           sg.b, sg.h, gthread, 128);
+        if constexpr (FP8) {
+          // Widen this tile's value codes in place before the score wait (the
+          // codes land with the keys'; the PV product needs them only after
+          // this group's P): rows at positions in [lo_min, L) widened, rows
+          // outside [lo_min, L+K) zeroed, block rows written after the P
+          // store.  D = 64: every thread reads its codes before any writes,
+          // joining on v_read (a bounded wait).
+          const int p0v = pos_base + j * T;
+          const int st = j % NSV;
+          uint8_t* vtile = gbase + C::kOffV + st * C::kTileBytes;
+          const bool vok = mbar_wait_warp(v_full(st), (j / NSV) & 1);
+          if constexpr (D == 128) {
+            if (vok) widen_v_row<T>(vtile, gthread, p0v, geo.lo_min, L);
+          } else {
+            uint4 vraw[D / 32];
+            if (vok) read_v_codes<D, T>(vtile, gthread, vraw);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(v_read(grp));
+            const bool rok = mbar_wait_warp(v_read(grp), (j >> 1) & 1);
+            if (!vok || !rok) { ok = false; break; }
+            write_v_widened<D, T>(vtile, gthread, p0v, geo.lo_min, L, vraw);
+          }
+          if (!vok) { ok = false; break; }
+          if (gthread < T) {  // D = 128: not the threads that widen
+            const int zr = gthread;
+            const int pos = p0v + zr;
+            if (pos < geo.lo_min || pos >= geo.hi_max) {
+              uint8_t* vrow = vtile + zr * 128;
+#pragma unroll
+              for (int x2 = 0; x2 < D / 64; ++x2)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  *reinterpret_cast<uint4*>(vrow + x2 * T * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        }
         if (!mbar_wait_warp(s_full(grp), (j >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[64];
@@ -618,15 +874,21 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) mbar_arrive(s_free(grp));
 
         const int p0 = pos_base + j * T;
-        const bool need_mask = (p0 < lo_rows_max) || (p0 + T > hi_rows_min);
+        // fp8 context: a tile holding block keys is a boundary tile too.
+        const bool blk_cols = FP8 && p0 + T > L;
+        const bool need_mask = (p0 < lo_rows_max) || (p0 + T > hi_rows_min) || blk_cols;
         // Row max of the raw scores (the scale is positive), four independent
         // chains; masked keys become -inf by select.  Boundary tiles only.
+        // With fp8 context the scale includes k_scale, so a block key's score
+        // (bf16 key, no scale) is divided by k_scale first.
         float mx[4] = {ninf(), ninf(), ninf(), ninf()};
         if (need_mask) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const int pos = p0 + c;
-            const float v = (pos >= lo_r && pos < hi_r) ? __uint_as_float(sr[c]) : ninf();
+            float v = __uint_as_float(sr[c]);
+            if (FP8 && pos >= L) v *= a.kblk_mul;
+            v = (pos >= lo_r && pos < hi_r) ? v : ninf();
             sr[c] = __float_as_uint(v);
             mx[c & 3] = fmaxf(mx[c & 3], v);
           }
@@ -678,31 +940,47 @@ __global__ void __launch_bounds__(384, 1)
             tmem_wait_st();
           }
         }
-        // Value rows outside [lo_min, L+K) may hold anything: zero them in the
-        // stage before the PV MMA reads it (boundary tiles only).  In the
-        // dense-suffix form the block's value rows are written here too.
-        if (p0 < geo.lo_min || p0 + T > geo.hi_max || v_suffix) {
-          const int st = j % NSV;
-          if (!mbar_wait_warp(v_full(st), (j / NSV) & 1)) { ok = false; break; }
-          if (v_suffix)
-            write_staged_suffix<D, T, kVPieces>(gbase + C::kOffV + st * C::kTileBytes,
-                                                gbase + C::kOffVStage + grp * C::kVStageBytes, a, L, p0,
-                                                gthread, 128);
-          if (gthread < T) {
-            const int pos = p0 + gthread;
-            if (pos < geo.lo_min || pos >= geo.hi_max) {
-              uint8_t* vrow = gbase + C::kOffV + st * C::kTileBytes + gthread * 128;
+        auto v_fix = [&]() -> bool {
+          // Value rows outside [lo_min, L+K) may hold anything: zero them in the
+          // stage before the PV MMA reads it (boundary tiles only).  In the
+          // dense-suffix form the block's value rows are written here too.
+          if constexpr (FP8) {
+            // Widened and zeroed before the score wait: the block rows remain,
+            // divided by v_scale.
+            if (v_suffix)
+              write_staged_suffix_scaled<D, T, kVPieces>(gbase + C::kOffV + (j % NSV) * C::kTileBytes,
+                                                         gbase + C::kOffVStage + grp * C::kVStageBytes, a, L,
+                                                         p0, gthread, 128, a.pblk_mul);
+            return true;
+          }
+          if (p0 < geo.lo_min || p0 + T > geo.hi_max || v_suffix) {
+            const int st = j % NSV;
+            if (!mbar_wait_warp(v_full(st), (j / NSV) & 1)) return false;
+            if (v_suffix)
+              write_staged_suffix<D, T, kVPieces>(gbase + C::kOffV + st * C::kTileBytes,
+                                                  gbase + C::kOffVStage + grp * C::kVStageBytes, a, L, p0,
+                                                  gthread, 128);
+            if (gthread < T) {
+              const int pos = p0 + gthread;
+              if (pos < geo.lo_min || pos >= geo.hi_max) {
+                uint8_t* vrow = gbase + C::kOffV + st * C::kTileBytes + gthread * 128;
 #pragma unroll
-              for (int x2 = 0; x2 < D / 64; ++x2)
+                for (int x2 = 0; x2 < D / 64; ++x2)
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                  *reinterpret_cast<uint4*>(vrow + x2 * T * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+                  for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(vrow + x2 * T * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+              }
             }
           }
-        }
-        // P row -> this group's TMEM P columns (key pairs per column).
+          return true;
+        };
+        // P row -> this group's TMEM P columns (key pairs per column).  With
+        // fp8 context the block's value rows are written after the P store
+        // (fewer registers live across the cp.async wait).
+        if (!FP8 && !v_fix()) { ok = false; break; }
         tmem_st32(lane_addr + C::kColP + grp * (T / 2), pk);
         tmem_wait_st();
+        if (FP8 && !v_fix()) { ok = false; break; }
         fence_proxy_async_smem();  // the zeroed V rows, for the MMA
         tc_fence_before();
         __syncwarp();
@@ -734,7 +1012,7 @@ __global__ void __launch_bounds__(384, 1)
         const float w0 = (s0.x == ninf() || s0.y == 0.f) ? 0.f : fast_exp2(s0.x - M);
         const float w1 = (s1.x == ninf() || s1.y == 0.f) ? 0.f : fast_exp2(s1.x - M);
         const float l = w0 * s0.y + w1 * s1.y;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? a.out_mul / l : 0.f;
         // D = 128: group g writes columns [64g, 64g + 64); D = 64: group 0 all.
         if (grp * 64 < D)
           store_segment_rows<D>(a, &tm_out, &tm_part, gbase + C::kOffStage + grp * C::kStageBytes,
@@ -780,11 +1058,11 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D>
+template <int D, bool FP8>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
              const CUtensorMap& tm_v, const CUtensorMap& tm_q, const CUtensorMap& tm_out,
              const CUtensorMap& tm_part, cudaStream_t stream) {
-  auto kern = split_tc_kernel<D>;
+  auto kern = split_tc_kernel<D, FP8>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
   if (err != cudaSuccess) return err;
@@ -802,8 +1080,14 @@ int split_tc_smem_bytes(int D) { return D == 64 ? TcCfg<64>::kSmem : TcCfg<128>:
 int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
                     const CUtensorMap& tm_v, const CUtensorMap& tm_q, const CUtensorMap& tm_out,
                     const CUtensorMap& tm_part, cudaStream_t stream) {
-  if (a.D == 64) return launch_t<64>(a, plan, tm_k, tm_v, tm_q, tm_out, tm_part, stream);
-  if (a.D == 128) return launch_t<128>(a, plan, tm_k, tm_v, tm_q, tm_out, tm_part, stream);
+  if (a.fp8) {
+    if (a.k_block == nullptr) return cudaErrorInvalidValue;  // fp8 pages hold the context only
+    if (a.D == 64) return launch_t<64, true>(a, plan, tm_k, tm_v, tm_q, tm_out, tm_part, stream);
+    if (a.D == 128) return launch_t<128, true>(a, plan, tm_k, tm_v, tm_q, tm_out, tm_part, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (a.D == 64) return launch_t<64, false>(a, plan, tm_k, tm_v, tm_q, tm_out, tm_part, stream);
+  if (a.D == 128) return launch_t<128, false>(a, plan, tm_k, tm_v, tm_q, tm_out, tm_part, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -87,9 +87,12 @@ class CaseSpec:
         """Context keys the union of the block's rows reads (for byte counts)."""
         return min(L, self.window - 1) if self.window > 0 else L
 
-    def kv_bytes(self) -> int:
-        """Algorithmic K+V bytes of one call: each visible row read once."""
-        return sum(2 * self.Hkv * self.D * 2 * (self.visible_ctx(L) + self.K) for L in self.ctx_lens)
+    def kv_bytes(self, ctx_elem_bytes: int = 2) -> int:
+        """Algorithmic K+V bytes of one call: each visible row read once; the
+        context rows at ``ctx_elem_bytes`` per element (1 for fp8 pages), the
+        block rows at 2 (bf16)."""
+        return sum(2 * self.Hkv * self.D * (ctx_elem_bytes * self.visible_ctx(L) + 2 * self.K)
+                   for L in self.ctx_lens)
 
     def flops(self) -> int:
         return sum(self.Hkv * (self.visible_ctx(L) + self.K) * 4 * self.R * self.D for L in self.ctx_lens)

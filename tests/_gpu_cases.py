@@ -4,7 +4,9 @@ seeded inputs and compare them.
 Tolerances (from the stated bar for bf16 outputs, with the readings recorded
 in DESIGN.md):
 * relative L2 error of ``out`` against the unrounded fp64 oracle < 5e-3;
-* max abs error of ``out`` beyond the bf16 format's own rounding <= 1e-2:
+* max abs error of ``out`` beyond the bf16 format's own rounding <= 1e-2
+  (times the value scale where the values are not unit-variance: fp8 context
+  with v_scale > 1):
   ``max_i (|gpu_i - oracle_i| - ulp_bf16(oracle_i) / 2) <= 1e-2``.  Any bf16
   output is off by up to half an ulp from the exact value (0.0078 at
   |x| in [2, 4)), and a value near a rounding midpoint may round either way,
@@ -78,10 +80,13 @@ def metrics(gpu_out, gpu_lse, ora_out, ora_lse) -> dict:
     }
 
 
-def assert_parity(m: dict, what: str = ""):
+def assert_parity(m: dict, what: str = "", value_scale: float = 1.0):
+    """``value_scale``: the magnitude of the values relative to unit variance
+    (the fp8 form's v_scale); the absolute bound scales with it, as the bf16
+    rounding of the probabilities contributes an error proportional to |v|."""
     assert not m["nan"], f"{what}: NaN in output {m}"
     assert m["rel_l2"] < REL_L2_MAX, f"{what}: {m}"
-    assert m["max_abs_excess"] <= MAX_ABS_MAX, f"{what}: {m}"
+    assert m["max_abs_excess"] <= MAX_ABS_MAX * max(1.0, value_scale), f"{what}: {m}"
     assert m["max_abs_raw"] <= 8 * m["ulp_at_max"], f"{what}: {m}"
     assert m["lse_abs"] <= LSE_ABS_MAX, f"{what}: {m}"
 

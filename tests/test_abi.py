@@ -75,6 +75,8 @@ def base_params(**kw):
     dict(future_keys=1, right_window=2),
     dict(scale=float("nan")), dict(scale=0.0), dict(scale=-0.125), dict(max_ctx_len=-1), dict(max_ctx_len=40 * 32 - 6),
     dict(num_pages=0), dict(force_path=3), dict(force_split_tiles=-1), dict(force_split_tiles=65),
+    dict(kv_dtype=2), dict(kv_dtype=-1), dict(kv_dtype=1, force_path=1),
+    dict(kv_dtype=1, batch=900, max_ctx_len=100, max_pages_per_req=4),
 ])
 def test_invalid_params_rejected(dflash_lib, bad):
     d = dflash_lib
@@ -89,7 +91,7 @@ def test_invalid_params_rejected(dflash_lib, bad):
 
 def test_reserved_must_be_zero(dflash_lib):
     p = base_params()
-    p.reserved[2] = 1
+    p.reserved[1] = 1
     assert dflash_lib.workspace_size(p) == 0
 
 
@@ -118,6 +120,30 @@ def test_null_and_misaligned_pointers_rejected(dflash_lib):
         assert d.block_attn_raw(p, *ptrs, ws, 0) == d.DFLASH_ERR_INVALID
 
 
+def test_fp8_context_plan_and_validation(dflash_lib):
+    """fp8 pools always take the tcgen05 path; the fp8 entry point takes fp8
+    parameters and positive finite scales only, and the bf16 entry points
+    refuse fp8 parameters (all checked before any device is touched)."""
+    d = dflash_lib
+    p8 = base_params(kv_dtype=d.KV_FP8_E4M3, num_q_heads=4, num_kv_heads=2, block_size=3)
+    assert d.plan(p8)["path"] == d.PATH_TCGEN05
+    assert d.plan(base_params(num_q_heads=4, num_kv_heads=2, block_size=3))["path"] == d.PATH_MMA
+    ws = d.workspace_size(p8)
+    assert ws > 0
+    ptr = 1 << 20
+    args = [ptr] * 5
+    tail = [ptr, ptr, ptr, ptr, ptr, ws, 0]
+    for ks, vs in [(0.0, 1.0), (1.0, -2.0), (float("nan"), 1.0), (1.0, float("inf"))]:
+        assert d.block_attn_fp8_context_raw(p8, *args, ks, vs, *tail) == d.DFLASH_ERR_INVALID
+    p16 = base_params()
+    assert d.block_attn_fp8_context_raw(p16, *args, 1.0, 1.0, *tail) == d.DFLASH_ERR_INVALID
+    assert d.block_attn_raw(p8, *[ptr] * 8, ws, 0) == d.DFLASH_ERR_INVALID
+    assert d.block_attn_dense_suffix_raw(p8, *[ptr] * 10, ws, 0) == d.DFLASH_ERR_INVALID
+    assert d.block_attn_fp8_context_raw(p8, ptr, 0, ptr, ptr, ptr, 1.0, 1.0, *tail) == d.DFLASH_ERR_INVALID
+    from speculative_decoding_draft_paged_gb300 import _lib
+    assert _lib.load().dflash_append_block_kv(ctypes.byref(p8), *[ptr] * 6, 0, 0) == d.DFLASH_ERR_INVALID
+
+
 def test_status_strings(dflash_lib):
     from speculative_decoding_draft_paged_gb300 import _lib
 
@@ -142,6 +168,7 @@ def touched_tiles(L, K, W, T):
     dict(num_q_heads=64, num_kv_heads=4, batch=96, max_ctx_len=8192, max_pages_per_req=260),
     dict(num_q_heads=16, num_kv_heads=1, force_path=2, force_split_tiles=3, window=50),
     dict(num_q_heads=16, num_kv_heads=1, batch=900, max_ctx_len=100, max_pages_per_req=4),
+    dict(kv_dtype=1), dict(kv_dtype=1, num_q_heads=4, num_kv_heads=2, block_size=3, window=33),
 ])
 def test_planner_covers_every_length(dflash_lib, kw):
     """For every context length up to max_ctx_len the units cover all tiles,
