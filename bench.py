@@ -466,7 +466,7 @@ def main():
     gbs = total_bytes / (ms * 1e-3) / 1e9
     split_gbs = kv_bytes / (split_ms * 1e-3) / 1e9
     kernel = "split_tc" if plan["path"] == dflash.PATH_TCGEN05 else "split_mma"
-    traffic = stored_traffic(spec.name, kernel)
+    traffic = stored_traffic(spec.name, kernel + ("_fp8" if args.fp8_context else ""))
 
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
