@@ -86,8 +86,9 @@ typedef struct dflash_params {
                                 0: causal block plus right_window later keys */
   float   scale;             /* softmax scale > 0, applied to q.k in fp32 */
   int32_t max_ctx_len;       /* host bound on every ctx_lens[b]; sizes the plan */
-  int32_t force_path;        /* DFLASH_PATH_*; 0 picks: tcgen05 for R > 64, or D = 128
-                                with R > 32 and B*Hkv >= 32, or fp8 pages; else mma.sync */
+  int32_t force_path;        /* DFLASH_PATH_*; 0 picks: tcgen05 for R > 64 with B*Hkv > 8,
+                                D = 128 with R > 32 and B*Hkv > 32, or fp8 pages;
+                                else mma.sync */
   int32_t force_split_tiles; /* 1..64: key tiles per split unit, or per CTA range on
                                 the tcgen05 path (tests); 0 = planner */
   int32_t right_window;      /* with future_keys = 0: row i also sees block keys

@@ -117,13 +117,16 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   const int64_t tc_tiles = static_cast<int64_t>(p->batch) * p->num_kv_heads *
                            max_tiles(p->max_ctx_len, p->block_size, p->window, split_tc_tile_keys(D));
   const bool tc_ok = split_tc_available() && p->batch <= kTcMaxBatch && tc_tiles <= (int64_t(1) << 30);
-  // Path choice (measured on GB300): the tcgen05 kernel for R > 64, and for
-  // D = 128 with R > 32 once there are at least 32 (request, kv head) pairs
-  // (16/1 heads, K = 3, 64 requests at 16K context: 53 us against 61 on the
-  // mma.sync kernel); the mma.sync kernel otherwise (its D = 64 long-context
-  // shapes run at half the tcgen05 kernel's time).  fp8 pages: tcgen05 only.
+  // Path choice (measured on GB300, split + combine per call): the tcgen05
+  // kernel for R > 64 with more than 8 (request, kv head) pairs (16/1 heads,
+  // K = 7, 16K context: 34 us against 36 on the mma.sync kernel at 16 pairs,
+  // 40 against 48 at 32; 32 against 30 at 8 pairs, equal below), and for
+  // D = 128 with R > 32 and more than 32 pairs (K = 3: equal at 32 pairs, 53
+  // against 61 us at 64); the mma.sync kernel otherwise (its D = 64
+  // long-context shapes run in about half the tcgen05 kernel's time).  fp8
+  // pages: tcgen05 only.
   const int64_t pairs = static_cast<int64_t>(p->batch) * p->num_kv_heads;
-  const bool tc_pref = k.R > 64 || (D == 128 && k.R > 32 && pairs >= 32) ||
+  const bool tc_pref = (k.R > 64 && pairs > 8) || (D == 128 && k.R > 32 && pairs > 32) ||
                        p->kv_dtype == DFLASH_KV_FP8_E4M3;
   int path = p->force_path;
   if (path == DFLASH_PATH_AUTO) path = (tc_pref && tc_ok) ? DFLASH_PATH_TCGEN05 : DFLASH_PATH_MMA;
