@@ -184,8 +184,9 @@ def reduce_over_ranks(times, nbytes, device):
     return out[:-1], out[-1]
 
 
-def time_oracle_sample(spec, budget_s: float = 15.0, device_inputs=None):
-    """Run the oracle on a bounded sample of the workload's requests.
+def time_oracle_sample(spec, budget_s: float = 15.0, device_inputs=None, fp8: bool = False):
+    """Run the oracle on a bounded sample of the workload's requests (the
+    fp8-context form over E4M3 casts of the same pages when ``fp8``).
 
     Returns (kv_bytes_per_s, seconds, n_requests, threads, description)."""
     import numpy as np
@@ -214,14 +215,30 @@ def time_oracle_sample(spec, budget_s: float = 15.0, device_inputs=None):
     def bits(t):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
-    args = (bits(inp["q"]), bits(inp["k_pages"]), bits(inp["v_pages"]), inp["page_table"].numpy(),
-            inp["ctx_lens"].numpy())
-    t0 = time.perf_counter()
-    oracle.block_attn(*args, block_size=sub.K, window=sub.window, future_keys=sub.future_keys,
-                      right_window=sub.right_window, scale=sub.softmax_scale, nthreads=threads)
-    dt = time.perf_counter() - t0
-    desc = f"{len(ids)} of {spec.B} requests (same shapes and lengths), fp64, {threads} threads"
-    return sub.kv_bytes() / dt, dt, len(ids), threads, desc
+    kw = dict(block_size=sub.K, window=sub.window, future_keys=sub.future_keys,
+              right_window=sub.right_window, scale=sub.softmax_scale, nthreads=threads)
+    if fp8:
+        codes = {k: inp[k].float().to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                 for k in ("k_pages", "v_pages")}
+        shape = (sub.B, sub.K, sub.Hkv, sub.D)
+        g = torch.Generator().manual_seed(sub.seed)
+        kb = bits(torch.randn(shape, generator=g).to(torch.bfloat16))
+        vb = bits(torch.randn(shape, generator=g).to(torch.bfloat16))
+        t0 = time.perf_counter()
+        oracle.block_attn_fp8(bits(inp["q"]), codes["k_pages"], codes["v_pages"], inp["page_table"].numpy(),
+                              inp["ctx_lens"].numpy(), k_scale=0.0431, v_scale=1.73, k_block=kb,
+                              v_block=vb, **kw)
+        dt = time.perf_counter() - t0
+        nbytes = sub.kv_bytes(1)
+    else:
+        t0 = time.perf_counter()
+        oracle.block_attn(bits(inp["q"]), bits(inp["k_pages"]), bits(inp["v_pages"]),
+                          inp["page_table"].numpy(), inp["ctx_lens"].numpy(), **kw)
+        dt = time.perf_counter() - t0
+        nbytes = sub.kv_bytes()
+    desc = (f"{len(ids)} of {spec.B} requests (same shapes and lengths), fp64, {threads} threads" +
+            (", fp8-context form" if fp8 else ""))
+    return nbytes / dt, dt, len(ids), threads, desc
 
 
 def run_reference(args):
@@ -497,7 +514,7 @@ def main():
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, n, cores, desc = time_oracle_sample(spec)
+        v, dt, n, cores, desc = time_oracle_sample(spec, fp8=bool(args.fp8_context))
         line["cpu_baseline"] = {"value": v / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
     if rank == 0:
