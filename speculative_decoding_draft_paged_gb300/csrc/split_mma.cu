@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(MAXT, 1)
       // After a K/V append launched just before (programmatic dependent
       // launch), the pages are read only once that kernel has finished.
       pdl_wait_primary();
+      // K/V rows are read once: evict them first.
+      const uint64_t kv_policy = l2_policy_evict_first();
       for (int it = 0; it < ntiles; ++it) {
         const int st = it % NS;
         if (it >= NS) {
@@ -162,8 +164,8 @@ __global__ void __launch_bounds__(MAXT, 1)
 #pragma unroll
           for (int x = 0; x < D / 64; ++x) {
             const uint32_t off = x * T * 128 + j * a.P * 128;
-            tma_load_4d(k_dst + off, &tm_k, x * 64, 0, h, page, full_bar(st));
-            tma_load_4d(v_dst + off, &tm_v, x * 64, 0, h, page, full_bar(st));
+            tma_load_4d_hint(k_dst + off, &tm_k, x * 64, 0, h, page, full_bar(st), kv_policy);
+            tma_load_4d_hint(v_dst + off, &tm_v, x * 64, 0, h, page, full_bar(st), kv_policy);
           }
         }
         *issued_count = it + 1;

@@ -547,6 +547,9 @@ __global__ void __launch_bounds__(384, 1)
     pdl_wait_primary();
     int cur_k = 0;
     Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
+    // K/V rows are read once: evict them first, so that the partial states
+    // (read back by the combine kernel), queries and page table stay in L2.
+    const uint64_t kv_policy = l2_policy_evict_first();
     for (int j = 0; j < n; ++j) {
       while (j >= sg.j1) seg_next(sg, PB, a.Hkv, start, end);
       const int k = j / tpc;
@@ -581,7 +584,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int pj = 0; pj < 4; ++pj) {
               if (pj >= ppt) break;
-              tma_load_4d(dst + C::kCodeOff + pj * a.P * D, map, 0, 0, sg.h, pages[pj], full);
+              tma_load_4d_hint(dst + C::kCodeOff + pj * a.P * D, map, 0, 0, sg.h, pages[pj], full, kv_policy);
             }
           } else {
             mbar_arrive_expect_tx(full, C::kTileBytes);
@@ -590,7 +593,8 @@ __global__ void __launch_bounds__(384, 1)
               if (pj >= ppt) break;
 #pragma unroll
               for (int x = 0; x < D / 64; ++x)
-                tma_load_4d(dst + x * T * 128 + pj * a.P * 128, map, x * 64, 0, sg.h, pages[pj], full);
+                tma_load_4d_hint(dst + x * T * 128 + pj * a.P * 128, map, x * 64, 0, sg.h, pages[pj], full,
+                                 kv_policy);
             }
           }
           *(v_ring ? issued_v : issued_k) = j + 1;
