@@ -87,14 +87,14 @@ typedef struct dflash_params {
   float   scale;             /* softmax scale > 0, applied to q.k in fp32 */
   int32_t max_ctx_len;       /* host bound on every ctx_lens[b]; sizes the plan */
   int32_t force_path;        /* DFLASH_PATH_*; 0 picks: tcgen05 for R > 64 with B*Hkv > 8,
-                                D = 128 with R > 32 and B*Hkv > 32, or fp8 pages;
-                                else mma.sync */
+                                or D = 128 with R > 32 and B*Hkv > 32; else mma.sync
+                                (tcgen05 also when an fp8 mma.sync plan would not
+                                fit shared memory) */
   int32_t force_split_tiles; /* 1..64: key tiles per split unit, or per CTA range on
                                 the tcgen05 path (tests); 0 = planner */
   int32_t right_window;      /* with future_keys = 0: row i also sees block keys
                                 i+1 .. i+right_window (0 .. K-1); 0 when future_keys = 1 */
-  int32_t kv_dtype;          /* DFLASH_KV_BF16 or DFLASH_KV_FP8_E4M3 (pool element type;
-                                the fp8 form always runs on the tcgen05 path) */
+  int32_t kv_dtype;          /* DFLASH_KV_BF16 or DFLASH_KV_FP8_E4M3 (pool element type) */
   int32_t reserved[2];       /* must be zero */
 } dflash_params;
 
@@ -276,10 +276,10 @@ int dflash_block_attn_dense_suffix(const dflash_params* p, const void* q, const 
  * q, out, lse2, ctx_lens, page_table and the workspace as dflash_block_attn
  * (dflash_workspace_size(p) with the same *p).  The codes are widened to
  * bf16 exactly on the chip; the scores and the output use the scales in
- * fp32.  Runs on the tcgen05 path for any packed row count (R <= 128) and
- * B <= 768; other plans are refused with DFLASH_ERR_INVALID, as are a
- * forced mma.sync path and non-positive or non-finite scales.  Same return
- * codes as dflash_block_attn.
+ * fp32.  Both paths take it (the planner's choice as for bf16 pages; a forced
+ * mma.sync plan whose code ring would not fit shared memory is refused).
+ * Non-positive or non-finite scales are refused with DFLASH_ERR_INVALID.
+ * Same return codes as dflash_block_attn.
  */
 int dflash_block_attn_fp8_context(const dflash_params* p, const void* q, const void* k_block,
                                   const void* v_block, const void* k_pages, const void* v_pages,

@@ -320,7 +320,7 @@ def block_attn_fp8_context_timed_raw(p: Params, q_ptr, kb_ptr, vb_ptr, k_ptr, v_
 def block_attn_fp8_context(q, k_block, v_block, k_pages, v_pages, page_table, ctx_lens, *,
                            k_scale: float, v_scale: float, block_size: int, window: int,
                            future_keys: int, scale: float, max_ctx_len: int, out=None, lse2=None,
-                           workspace=None, stream=None, force_split_tiles: int = 0,
+                           workspace=None, stream=None, force_path: int = 0, force_split_tiles: int = 0,
                            right_window: int = 0):
     """Dense-suffix form over fp8 context pages: ``k_pages``/``v_pages`` are
     uint8 E4M3 codes ``[num_pages, Hkv, P, D]`` dequantised by the per-tensor
@@ -334,8 +334,8 @@ def block_attn_fp8_context(q, k_block, v_block, k_pages, v_pages, page_table, ct
     _check_block("v_block", v_block, (B, K, k_pages.shape[1], D))
     p = params_for(q, k_pages, page_table, block_size=block_size, window=window,
                    future_keys=future_keys, scale=scale, max_ctx_len=max_ctx_len,
-                   force_split_tiles=force_split_tiles, right_window=right_window,
-                   kv_dtype=KV_FP8_E4M3)
+                   force_path=force_path, force_split_tiles=force_split_tiles,
+                   right_window=right_window, kv_dtype=KV_FP8_E4M3)
     if out is None:
         out = torch.empty_like(q)
     if lse2 is None:

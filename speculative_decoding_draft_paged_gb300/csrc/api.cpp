@@ -28,6 +28,7 @@ namespace {
 constexpr int kDefaultSms = 152;       // GB300, used when no device can be queried
 constexpr int kMaxDevices = 64;
 constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kMaxSmemPerCta = 227 * 1024;  // dynamic shared memory one CTA may opt into
 
 struct DeviceInfo {
   int sms = 0;
@@ -94,8 +95,6 @@ bool params_valid(const dflash_params* p) {
   if (p->force_path < DFLASH_PATH_AUTO || p->force_path > DFLASH_PATH_TCGEN05) return false;
   if (p->force_split_tiles < 0 || p->force_split_tiles > kMaxSplitTiles) return false;
   if (p->kv_dtype != DFLASH_KV_BF16 && p->kv_dtype != DFLASH_KV_FP8_E4M3) return false;
-  // fp8 pages are widened by the tcgen05 kernel only.
-  if (p->kv_dtype == DFLASH_KV_FP8_E4M3 && p->force_path == DFLASH_PATH_MMA) return false;
   return true;
 }
 
@@ -123,14 +122,20 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   // 40 against 48 at 32; 32 against 30 at 8 pairs, equal below), and for
   // D = 128 with R > 32 and more than 32 pairs (K = 3: equal at 32 pairs, 53
   // against 61 us at 64); the mma.sync kernel otherwise (its D = 64
-  // long-context shapes run in about half the tcgen05 kernel's time).  fp8
-  // pages: tcgen05 only.
+  // long-context shapes run in about half the tcgen05 kernel's time).  Both
+  // kernels read fp8 pages (the mma.sync kernel then needs a code ring as
+  // well, which must fit its shared memory); with fp8 pages the tcgen05
+  // kernel also takes R > 64 at 8 pairs or fewer (16/1 heads, K = 7, 8
+  // requests: 35 us against 39).
   const int64_t pairs = static_cast<int64_t>(p->batch) * p->num_kv_heads;
-  const bool tc_pref = (k.R > 64 && pairs > 8) || (D == 128 && k.R > 32 && pairs > 32) ||
-                       p->kv_dtype == DFLASH_KV_FP8_E4M3;
+  const bool fp8 = p->kv_dtype == DFLASH_KV_FP8_E4M3;
+  const bool tc_pref = (k.R > 64 && (pairs > 8 || fp8)) || (D == 128 && k.R > 32 && pairs > 32);
+  const int R_pad_mma = (k.R + 15) / 16 * 16;
+  const bool mma_ok = split_mma_smem_bytes(D, R_pad_mma, split_mma_kpw(D, R_pad_mma), fp8) <= kMaxSmemPerCta;
   int path = p->force_path;
-  if (path == DFLASH_PATH_AUTO) path = (tc_pref && tc_ok) ? DFLASH_PATH_TCGEN05 : DFLASH_PATH_MMA;
-  if (p->kv_dtype == DFLASH_KV_FP8_E4M3 && path != DFLASH_PATH_TCGEN05) return false;
+  if (path == DFLASH_PATH_AUTO)
+    path = ((tc_pref || !mma_ok) && tc_ok) ? DFLASH_PATH_TCGEN05 : DFLASH_PATH_MMA;
+  if (path == DFLASH_PATH_MMA && !mma_ok) return false;
   if (path == DFLASH_PATH_TCGEN05 && !tc_ok) return false;
   k.path = path;
   if (path == DFLASH_PATH_MMA) {
@@ -139,7 +144,7 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
     k.kpw = split_mma_kpw(D, k.R_pad);
     const int consumer_warps = (k.R_pad / 16) * (k.T / k.kpw);
     k.threads = 32 * (1 + consumer_warps);
-    k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw);
+    k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8);
   } else {
     k.R_pad = 128;
     k.T = split_tc_tile_keys(D);

@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "dflash_internal.h"
 
@@ -146,6 +147,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
@@ -368,7 +374,7 @@ __device__ __forceinline__ int paged_end(const AttnArgs& a, const Geometry& g) {
 template <int D, int T>
 __device__ __forceinline__ void write_suffix_rows(uint8_t* tile, const uint16_t* src, const AttnArgs& a,
                                                   int b, int h, int L, int p0, int lo, int hi, int tid,
-                                                  int nthr) {
+                                                  int nthr, float mul = 1.f) {
   constexpr int CPR = D / 8;
   const int r_lo = max(L, lo);
   const int r_hi = min(L + a.K, hi);
@@ -379,8 +385,14 @@ __device__ __forceinline__ void write_suffix_rows(uint8_t* tile, const uint16_t*
     const int rr = pos - p0;
     const uint4* row =
         reinterpret_cast<const uint4*>(src + ((static_cast<size_t>(b) * a.K + (pos - L)) * a.Hkv + h) * D);
-    *reinterpret_cast<uint4*>(tile + (c >> 3) * T * 128 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) =
-        __ldg(row + c);
+    uint4 x = __ldg(row + c);
+    if (mul != 1.f) {  // fp8 context: value rows divided by v_scale
+      auto sc = [&](uint32_t w) {
+        return pack_bf16x2(bf16_bits_to_f32(w & 0xffffu) * mul, bf16_bits_to_f32(w >> 16) * mul);
+      };
+      x = make_uint4(sc(x.x), sc(x.y), sc(x.z), sc(x.w));
+    }
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * T * 128 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) = x;
   }
 }
 
@@ -487,6 +499,58 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait_primary() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---- fp8 (E4M3) context codes, widened to bf16 in shared memory.
+
+// Two E4M3 codes (low 16 bits of `codes`, first code lowest) -> bf16x2,
+// exactly: cvt.rn.f16x2.e4m3x2 (every E4M3 value is an f16 value), f16 ->
+// f32, and the upper half of each f32 (at most 4 significant bits, so the
+// lower half is zero).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(codes)));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
+}
+
+// Byte offset of 16-byte word w of code row r in a stage's code area: the
+// boxes land with the TMA swizzle of their row length (128-byte swizzle for
+// D = 128: word w of row r at r*128 + (w ^ (r & 7))*16; 64-byte swizzle for
+// D = 64: at r*64 + (w ^ ((r >> 1) & 3))*16), so that a warp reading one
+// word per row hits every bank.
+template <int D>
+__device__ __forceinline__ int code_word(int r, int w) {
+  if constexpr (D == 128) return r * 128 + ((w ^ (r & 7)) << 4);
+  else return r * 64 + ((w ^ ((r >> 1) & 3)) << 4);
+}
+
+// Eight codes (two words) -> one 16-byte chunk of eight bf16 values.
+__device__ __forceinline__ uint4 widen8(uint32_t w0, uint32_t w1) {
+  return make_uint4(e4m3x2_to_bf16x2(w0), e4m3x2_to_bf16x2(w0 >> 16), e4m3x2_to_bf16x2(w1),
+                    e4m3x2_to_bf16x2(w1 >> 16));
+}
+
+// Widens a stage's K and V codes (a separate code area: K codes then V
+// codes, row r of each at r*D, words swizzled as code_word) into the bf16
+// tiles the MMAs read (64-column halves of T rows x 128 B, 128-byte
+// swizzle), with threads tid = 0..nthr-1 taking words tid, tid + nthr, ...
+// The caller joins the threads afterwards.
+template <int D, int T>
+__device__ __forceinline__ void widen_stage_coop(const uint8_t* codes, uint8_t* k_tile, uint8_t* v_tile, int tid,
+                                                 int nthr) {
+  constexpr int WPR = D / 16;  // code words per row
+  constexpr int kTileWords = T * WPR;
+#pragma unroll 1
+  for (int u = tid; u < 2 * kTileWords; u += nthr) {
+    const bool is_v = u >= kTileWords;
+    const int rem = is_v ? u - kTileWords : u;
+    const int r = rem / WPR, w = rem - (rem / WPR) * WPR;
+    const uint4 c = *reinterpret_cast<const uint4*>(codes + (is_v ? T * D : 0) + code_word<D>(r, w));
+    uint8_t* tile = is_v ? v_tile : k_tile;
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8(c.x, c.y);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8(c.z, c.w);
+  }
 }
 
 }  // namespace dflash

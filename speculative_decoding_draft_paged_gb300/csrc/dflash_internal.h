@@ -158,7 +158,7 @@ int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap
 int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat);
 
 // Shared-memory bytes of each split kernel for a plan (used by the planner).
-int split_mma_smem_bytes(int D, int R_pad, int kpw);
+int split_mma_smem_bytes(int D, int R_pad, int kpw, bool fp8);
 int split_tc_smem_bytes(int D);
 
 }  // namespace dflash

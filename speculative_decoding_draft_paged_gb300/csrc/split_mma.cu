@@ -23,6 +23,12 @@
 // warps of a row group merge their states through shared memory at the end.
 // Output: the unit's normalised partial O and base-2 LSE in the workspace, or,
 // with one unit per (request, kv head), the final bf16 output and LSE.
+// fp8 context (dense-suffix form over E4M3 pages): each stage's codes land in
+// a code ring beside the bf16 ring and all consumer warps widen them into the
+// stage's bf16 tiles together before their MMAs (the per-tensor scales fold
+// into the score scale and the output, as in the tcgen05 kernel).  The TMA
+// writes only the code ring then, so the generic writes into the bf16 tiles
+// need no proxy fence.
 
 #include <cuda_runtime.h>
 
@@ -36,21 +42,27 @@ struct MmaTile {
   static constexpr int T = (D == 64) ? 128 : 64;          // keys per stage
   static constexpr int kTileBytes = T * D * 2;             // one of K or V
   static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kCodeStageBytes = 2 * T * D;        // fp8 context: K and V codes
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
 // Dense-suffix form: the block's K and V rows of one warp's key slice
-// [lo, hi) into stage tiles whose row 0 is position p0.  Out of line: it runs
-// on at most two tiles per unit and would otherwise crowd the tile loop.
-template <int D, int T>
+// [lo, hi) into stage tiles whose row 0 is position p0 (value rows divided
+// by v_scale with fp8 context).  Out of line: it runs on at most two
+// tiles per unit and would otherwise crowd the tile loop.
+template <int D, int T, bool FP8>
 __device__ __noinline__ void write_slice_suffix(uint8_t* k_tile, uint8_t* v_tile, const AttnArgs& a,
                                                 int b, int h, int L, int p0, int lo, int hi, int lane) {
   write_suffix_rows<D, T>(k_tile, a.k_block, a, b, h, L, p0, lo, hi, lane, 32);
-  write_suffix_rows<D, T>(v_tile, a.v_block, a, b, h, L, p0, lo, hi, lane, 32);
+  if constexpr (FP8) {
+    write_suffix_rows<D, T>(v_tile, a.v_block, a, b, h, L, p0, lo, hi, lane, 32, a.pblk_mul);
+  } else {
+    write_suffix_rows<D, T>(v_tile, a.v_block, a, b, h, L, p0, lo, hi, lane, 32);
+  }
 }
 
-template <int D, int KPW, int MAXT>
+template <int D, int KPW, int MAXT, bool FP8>
 __global__ void __launch_bounds__(MAXT, 1)
     split_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
@@ -80,15 +92,20 @@ __global__ void __launch_bounds__(MAXT, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
-  const uint32_t q_u32 = base_u32 + NS * kStageBytes;
-  uint8_t* q_smem = base + NS * kStageBytes;
+  // fp8 context: a code ring of NS stages after the bf16 ring.
+  constexpr int kCodeRing = FP8 ? NS * MmaTile<D>::kCodeStageBytes : 0;
+  const uint32_t code_u32 = base_u32 + NS * kStageBytes;
+  const uint32_t q_u32 = base_u32 + NS * kStageBytes + kCodeRing;
+  uint8_t* q_smem = base + NS * kStageBytes + kCodeRing;
   const uint32_t bar_u32 = q_u32 + a.R_pad * D * 2;
   uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + a.R_pad * D * 2);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + (FP8 ? 3 : 2) * NS);
   volatile int* issued_count = abort_flag + 1;
   int* pg_smem = const_cast<int*>(abort_flag) + 4;  // kMaxUnitSlots page ids
   auto full_bar = [&](int st) { return bar_u32 + 8u * st; };
   auto empty_bar = [&](int st) { return bar_u32 + 8u * (NS + st); };
+  // fp8 context: every consumer warp has widened its share of stage st.
+  auto widened_bar = [&](int st) { return bar_u32 + 8u * (2 * NS + st); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -98,6 +115,7 @@ __global__ void __launch_bounds__(MAXT, 1)
     for (int st = 0; st < NS; ++st) {
       mbar_init(full_bar(st), 1);
       mbar_init(empty_bar(st), n_consumer_warps);
+      if constexpr (FP8) mbar_init(widened_bar(st), n_consumer_warps);
     }
     *abort_flag = 0;
     *issued_count = 0;
@@ -156,16 +174,27 @@ __global__ void __launch_bounds__(MAXT, 1)
           }
         }
         if (*abort_flag) break;
-        mbar_arrive_expect_tx(full_bar(st), kStageBytes);
         const uint32_t k_dst = base_u32 + st * kStageBytes;
         const uint32_t v_dst = k_dst + kTileBytes;
-        for (int j = 0; j < pages_per_tile; ++j) {
-          const int page = pg_smem[it * pages_per_tile + j];
+        if constexpr (FP8) {
+          // One box of (D codes, P rows) per page, into the stage's codes.
+          mbar_arrive_expect_tx(full_bar(st), 2 * T * D);
+          const uint32_t kc = code_u32 + st * MmaTile<D>::kCodeStageBytes;
+          for (int j = 0; j < pages_per_tile; ++j) {
+            const int page = pg_smem[it * pages_per_tile + j];
+            tma_load_4d_hint(kc + j * a.P * D, &tm_k, 0, 0, h, page, full_bar(st), kv_policy);
+            tma_load_4d_hint(kc + T * D + j * a.P * D, &tm_v, 0, 0, h, page, full_bar(st), kv_policy);
+          }
+        } else {
+          mbar_arrive_expect_tx(full_bar(st), kStageBytes);
+          for (int j = 0; j < pages_per_tile; ++j) {
+            const int page = pg_smem[it * pages_per_tile + j];
 #pragma unroll
-          for (int x = 0; x < D / 64; ++x) {
-            const uint32_t off = x * T * 128 + j * a.P * 128;
-            tma_load_4d_hint(k_dst + off, &tm_k, x * 64, 0, h, page, full_bar(st), kv_policy);
-            tma_load_4d_hint(v_dst + off, &tm_v, x * 64, 0, h, page, full_bar(st), kv_policy);
+            for (int x = 0; x < D / 64; ++x) {
+              const uint32_t off = x * T * 128 + j * a.P * 128;
+              tma_load_4d_hint(k_dst + off, &tm_k, x * 64, 0, h, page, full_bar(st), kv_policy);
+              tma_load_4d_hint(v_dst + off, &tm_v, x * 64, 0, h, page, full_bar(st), kv_policy);
+            }
           }
         }
         *issued_count = it + 1;
@@ -229,12 +258,27 @@ __global__ void __launch_bounds__(MAXT, 1)
       const uint32_t k_st = base_u32 + st * kStageBytes;
       const uint32_t v_st = k_st + kTileBytes;
       const int p0 = (tile0 + it) * T + kb;  // logical position of the slice's first key
+      // fp8 context: all consumer warps widen the stage's codes and join on
+      // widened_bar (a bounded wait), before any block row is written into
+      // the tiles.
+      if constexpr (FP8) {
+        widen_stage_coop<D, T>(base + NS * kStageBytes + st * MmaTile<D>::kCodeStageBytes, base + st * kStageBytes,
+                               base + st * kStageBytes + kTileBytes, threadIdx.x - 32, n_consumer_warps * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(widened_bar(st));
+        if (!mbar_wait_warp(widened_bar(st), (it / NS) & 1)) {
+          flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+          *abort_flag = 1;
+          aborted = true;
+          break;
+        }
+      }
       if (dense && p0 + KPW > L && p0 < L + a.K) {
         // The block rows of this warp's key slice, from the dense tensors
         // (warps of other row groups with the same slice write the same
         // bytes; each warp reads only after its own writes).
         uint8_t* k_tile = base + st * kStageBytes;
-        write_slice_suffix<D, T>(k_tile, k_tile + kTileBytes, a, b, h, L, p0 - kb, p0, p0 + KPW, lane);
+        write_slice_suffix<D, T, FP8>(k_tile, k_tile + kTileBytes, a, b, h, L, p0 - kb, p0, p0 + KPW, lane);
         __syncwarp();
       }
 
@@ -255,8 +299,10 @@ __global__ void __launch_bounds__(MAXT, 1)
       }
 
       // Mask by select (boundary tiles only; uniform branch), then the row
-      // max of the raw scores (the scale is positive).
-      const bool need_mask = (p0 < lo_rows_max) || (p0 + KPW > hi_rows_min);
+      // max of the raw scores (the scale is positive).  With fp8 context the
+      // scale includes k_scale, so a block key's score (bf16 key, no scale)
+      // is divided by k_scale first.
+      const bool need_mask = (p0 < lo_rows_max) || (p0 + KPW > hi_rows_min) || (FP8 && p0 + KPW > L);
       if (need_mask) {
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
@@ -264,6 +310,7 @@ __global__ void __launch_bounds__(MAXT, 1)
           for (int e = 0; e < 4; ++e) {
             const int pos = p0 + n * 8 + 2 * (lane & 3) + (e & 1);
             const int ri = e >> 1;
+            if (FP8 && pos >= L) sacc[n][e] *= a.kblk_mul;
             if (pos < lo_r[ri] || pos >= hi_r[ri]) sacc[n][e] = neg_inf();
           }
         }
@@ -369,7 +416,7 @@ __global__ void __launch_bounds__(MAXT, 1)
         const int r = 16 * wr + (lane >> 2) + 8 * ri;
         if (r < a.R) {
           const float l = l_run[ri];
-          const float inv = l > 0.f ? 1.f / l : 0.f;
+          const float inv = l > 0.f ? (FP8 ? a.out_mul : 1.f) / l : 0.f;
 #pragma unroll
           for (int n = 0; n < D / 8; ++n) {
             const float v0 = o[n][2 * ri] * inv, v1 = o[n][2 * ri + 1] * inv;
@@ -429,7 +476,7 @@ __global__ void __launch_bounds__(MAXT, 1)
             den += wt * sc_l[cwi * 16 + rr];
           }
         }
-        const float v = den > 0.f ? num / den : 0.f;
+        const float v = den > 0.f ? (FP8 ? num / den * a.out_mul : num / den) : 0.f;
         const float lse = den > 0.f ? M + log2f(den) : neg_inf();
         if (direct) {
           const size_t orow = out_row_index(a, b, h, r);
@@ -463,7 +510,7 @@ int kpw_for(int D, int R_pad) {
 template <int D, int KPW, int MAXT = 288>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
              const CUtensorMap& tm_v, cudaStream_t stream) {
-  auto kern = split_mma_kernel<D, KPW, MAXT>;
+  auto kern = a.fp8 ? split_mma_kernel<D, KPW, MAXT, true> : split_mma_kernel<D, KPW, MAXT, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          plan.smem_bytes);
   if (err != cudaSuccess) return err;
@@ -475,9 +522,10 @@ int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
 
 }  // namespace
 
-int split_mma_smem_bytes(int D, int R_pad, int /*kpw*/) {
+int split_mma_smem_bytes(int D, int R_pad, int /*kpw*/, bool fp8) {
   const int stage = (D == 64) ? MmaTile<64>::kStageBytes : MmaTile<128>::kStageBytes;
-  return 1024 + kStages * stage + R_pad * D * 2 + 8 * 2 * kStages + 16 + 4 * kMaxUnitSlots;
+  const int codes = fp8 ? kStages * ((D == 64) ? MmaTile<64>::kCodeStageBytes : MmaTile<128>::kCodeStageBytes) : 0;
+  return 1024 + kStages * stage + codes + R_pad * D * 2 + 8 * (fp8 ? 3 : 2) * kStages + 16 + 4 * kMaxUnitSlots;
 }
 
 int split_mma_kpw(int D, int R_pad) { return kpw_for(D, R_pad); }

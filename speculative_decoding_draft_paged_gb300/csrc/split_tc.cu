@@ -49,7 +49,6 @@
 // per-tensor scales fold into the score scale and the output.
 // Every mbarrier wait is bounded (DFLASH_STATUS_TIMEOUT, then drain).
 
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -98,34 +97,6 @@ struct TcCfg {
 constexpr int kNoPage = -0x7fffffff - 1;  // page-table slot outside the keys a pair reads
 
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
-
-// Two E4M3 codes (low 16 bits of `codes`, first code lowest) -> bf16x2,
-// exactly: cvt.rn.f16x2.e4m3x2 (every E4M3 value is an f16 value), f16 ->
-// f32, and the upper half of each f32 (at most 4 significant bits, so the
-// lower half is zero).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(codes)));
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  return __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
-}
-
-// Byte offset of 16-byte word w of code row r in a stage's code area: the
-// boxes land with the TMA swizzle of their row length (128-byte swizzle for
-// D = 128: word w of row r at r*128 + (w ^ (r & 7))*16; 64-byte swizzle for
-// D = 64: at r*64 + (w ^ ((r >> 1) & 3))*16), so that a warp reading one
-// word per row hits every bank.
-template <int D>
-__device__ __forceinline__ int code_word(int r, int w) {
-  if constexpr (D == 128) return r * 128 + ((w ^ (r & 7)) << 4);
-  else return r * 64 + ((w ^ ((r >> 1) & 3)) << 4);
-}
-
-// Eight codes (two words) -> one 16-byte chunk of eight bf16 values.
-__device__ __forceinline__ uint4 widen8(uint32_t w0, uint32_t w1) {
-  return make_uint4(e4m3x2_to_bf16x2(w0), e4m3x2_to_bf16x2(w0 >> 16), e4m3x2_to_bf16x2(w1),
-                    e4m3x2_to_bf16x2(w1 >> 16));
-}
 
 // One warp widens a K tile in place: lane l takes rows l and l + 32.  With
 // D = 128 a row's bf16 bytes overwrite only its own codes (its second half

@@ -30,11 +30,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Shared-memory matrix descriptor, 128-byte swizzle (layout type 2),
 // descriptor version 1.  Byte offsets are encoded >> 4.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,

@@ -75,8 +75,9 @@ def base_params(**kw):
     dict(future_keys=1, right_window=2),
     dict(scale=float("nan")), dict(scale=0.0), dict(scale=-0.125), dict(max_ctx_len=-1), dict(max_ctx_len=40 * 32 - 6),
     dict(num_pages=0), dict(force_path=3), dict(force_split_tiles=-1), dict(force_split_tiles=65),
-    dict(kv_dtype=2), dict(kv_dtype=-1), dict(kv_dtype=1, force_path=1),
-    dict(kv_dtype=1, batch=900, max_ctx_len=100, max_pages_per_req=4),
+    dict(kv_dtype=2), dict(kv_dtype=-1),
+    dict(kv_dtype=1, force_path=1, head_dim=128, page_size=64, num_q_heads=16, num_kv_heads=1,
+         block_size=8, max_pages_per_req=30),
 ])
 def test_invalid_params_rejected(dflash_lib, bad):
     d = dflash_lib
@@ -121,13 +122,20 @@ def test_null_and_misaligned_pointers_rejected(dflash_lib):
 
 
 def test_fp8_context_plan_and_validation(dflash_lib):
-    """fp8 pools always take the tcgen05 path; the fp8 entry point takes fp8
-    parameters and positive finite scales only, and the bf16 entry points
-    refuse fp8 parameters (all checked before any device is touched)."""
+    """fp8 pools take the path bf16 pools would (the mma.sync plan also needs
+    room for its code ring: R = 128 at D = 128 forced onto it is refused);
+    the fp8 entry point takes fp8 parameters and positive finite scales only,
+    and the bf16 entry points refuse fp8 parameters (all checked before any
+    device is touched)."""
     d = dflash_lib
     p8 = base_params(kv_dtype=d.KV_FP8_E4M3, num_q_heads=4, num_kv_heads=2, block_size=3)
-    assert d.plan(p8)["path"] == d.PATH_TCGEN05
+    assert d.plan(p8)["path"] == d.PATH_MMA
     assert d.plan(base_params(num_q_heads=4, num_kv_heads=2, block_size=3))["path"] == d.PATH_MMA
+    big = dict(head_dim=128, page_size=64, num_q_heads=16, num_kv_heads=1, block_size=8, max_pages_per_req=30,
+               batch=64)
+    assert d.plan(base_params(kv_dtype=d.KV_FP8_E4M3, **big))["path"] == d.PATH_TCGEN05
+    for path in (d.PATH_MMA, d.PATH_TCGEN05):
+        assert d.workspace_size(base_params(kv_dtype=d.KV_FP8_E4M3, force_path=path)) > 0
     ws = d.workspace_size(p8)
     assert ws > 0
     ptr = 1 << 20

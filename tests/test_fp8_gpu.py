@@ -48,19 +48,21 @@ def _fp8_case(spec, device, seed):
     return dev
 
 
-def _check(spec, device, k_scale, v_scale, split=0, seed=17):
+def _check(spec, device, k_scale, v_scale, path, split=0, seed=17):
     d = _fp8_case(spec, device, seed)
     p = dflash.params_for(d["q"], d["kp8"], d["tab"], block_size=spec.K, window=spec.window,
                           future_keys=spec.future_keys, scale=spec.softmax_scale,
-                          max_ctx_len=spec.max_ctx_len, force_split_tiles=split,
+                          max_ctx_len=spec.max_ctx_len, force_path=path, force_split_tiles=split,
                           right_window=spec.right_window, kv_dtype=dflash.KV_FP8_E4M3)
-    assert dflash.plan(p)["path"] == dflash.PATH_TCGEN05
+    if dflash.workspace_size(p) == 0:
+        pytest.skip("no such plan (the mma.sync code ring would not fit)")
+    assert dflash.plan(p)["path"] == path
     ws = torch.zeros(dflash.workspace_size(p), dtype=torch.uint8, device=device)
     out, lse = dflash.block_attn_fp8_context(
         d["q"], d["kb"], d["vb"], d["kp8"], d["vp8"], d["tab"], d["lens"], k_scale=k_scale,
         v_scale=v_scale, block_size=spec.K, window=spec.window, future_keys=spec.future_keys,
-        scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len, force_split_tiles=split,
-        right_window=spec.right_window, workspace=ws)
+        scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len, force_path=path,
+        force_split_tiles=split, right_window=spec.right_window, workspace=ws)
     torch.cuda.synchronize()
     assert dflash.read_device_status(ws) == 0, "a page-table slot past the context was read"
     ro, rl = oracle.block_attn_fp8(
@@ -82,9 +84,13 @@ def _gqa(D, P, K, Hq, Hkv, win=0, fk=1, r=0, lens=(0, 5, 25, 32, 33, 700, 2000))
                       extra_pages=2)
 
 
+PATHS = [dflash.PATH_MMA, dflash.PATH_TCGEN05]
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("win,fk,r", [(0, 1, 0), (4096, 1, 0), (0, 0, 0), (2, 0, 4), (300, 0, 3)])
-def test_fp8_minimax(cuda_device, win, fk, r):
-    _check(_minimax(win, fk, r), cuda_device, k_scale=0.0431, v_scale=1.73)
+def test_fp8_minimax(cuda_device, path, win, fk, r):
+    _check(_minimax(win, fk, r), cuda_device, k_scale=0.0431, v_scale=1.73, path=path)
 
 
 @pytest.mark.parametrize("D,P,K,Hq,Hkv", [
@@ -94,21 +100,33 @@ def test_fp8_minimax(cuda_device, win, fk, r):
     (128, 32, 4, 64, 4),   # R = 64
     (64, 64, 16, 8, 1),    # K = 16, R = 128
 ])
-def test_fp8_shapes(cuda_device, D, P, K, Hq, Hkv):
-    _check(_gqa(D, P, K, Hq, Hkv), cuda_device, k_scale=0.27, v_scale=0.0113)
+@pytest.mark.parametrize("path", PATHS)
+def test_fp8_shapes(cuda_device, path, D, P, K, Hq, Hkv):
+    _check(_gqa(D, P, K, Hq, Hkv), cuda_device, k_scale=0.27, v_scale=0.0113, path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("split", [1, 3])
-def test_fp8_cut_ranges(cuda_device, split):
-    """Forced short CTA ranges: every pair is cut into many partials."""
-    _check(_gqa(128, 64, 7, 16, 1, win=1000), cuda_device, k_scale=3.5, v_scale=0.6, split=split)
+def test_fp8_cut_ranges(cuda_device, path, split):
+    """Forced short splits: every pair is cut into many partials."""
+    _check(_gqa(128, 64, 7, 16, 1, win=1000), cuda_device, k_scale=3.5, v_scale=0.6, path=path, split=split)
 
 
-def test_fp8_many_requests(cuda_device):
+@pytest.mark.parametrize("path", PATHS)
+def test_fp8_many_requests(cuda_device, path):
     lens = [int(x) for x in np.random.default_rng(5).integers(0, 3000, size=150)]
     lens[:4] = [0, 1, 63, 64]
-    _check(_gqa(128, 64, 7, 16, 1, lens=lens), cuda_device, k_scale=0.05, v_scale=2.0)
+    _check(_gqa(128, 64, 7, 16, 1, lens=lens), cuda_device, k_scale=0.05, v_scale=2.0, path=path)
 
 
-def test_fp8_window_smaller_than_block(cuda_device):
-    _check(_gqa(64, 32, 7, 16, 2, win=3, fk=0, r=6), cuda_device, k_scale=1.0 / 3.0, v_scale=7.0)
+@pytest.mark.parametrize("path", PATHS)
+def test_fp8_window_smaller_than_block(cuda_device, path):
+    _check(_gqa(64, 32, 7, 16, 2, win=3, fk=0, r=6), cuda_device, k_scale=1.0 / 3.0, v_scale=7.0, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_fp8_long_context_d64(cuda_device, path):
+    """The 12/2-head D = 64 shape at 20K context (R = 42: three row groups)."""
+    spec = W.CaseSpec("fp8_longctx", B=2, Hq=12, Hkv=2, D=64, K=7, P=32, window=0, future_keys=1,
+                      ctx_lens=[20000, 777], seed=87, poison=True)
+    _check(spec, cuda_device, k_scale=0.19, v_scale=1.3, path=path)
