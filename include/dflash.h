@@ -59,13 +59,15 @@ extern "C" {
 #define DFLASH_STATUS_BAD_PAGE       1  /* a visible position's page id is outside [0, num_pages) */
 #define DFLASH_STATUS_BAD_CTX_LEN    2  /* ctx_lens[b] < 0 or > max_ctx_len (clamped) */
 #define DFLASH_STATUS_TIMEOUT        4  /* a pipeline wait ran out (never expected) */
+#define DFLASH_STATUS_FP8_RANGE      8  /* fp8 context on the mma.sync path: a block row value
+                                           (k, or v / v_scale) is outside the f16 range */
 
-/* Kernel-path selection for dflash_params.force_path. */
 /* Element type of the page pools (dflash_params.kv_dtype). */
 #define DFLASH_KV_BF16               0  /* bf16 pages: every entry point but the fp8 one */
 #define DFLASH_KV_FP8_E4M3           1  /* E4M3 codes with per-tensor scales:
                                            dflash_block_attn_fp8_context only */
 
+/* Kernel-path selection for dflash_params.force_path. */
 #define DFLASH_PATH_AUTO             0
 #define DFLASH_PATH_MMA              1  /* warp-level mma.sync tiles (any R <= 128) */
 #define DFLASH_PATH_TCGEN05          2  /* tcgen05 / TMEM, one 128-row tile per kv head;
@@ -266,7 +268,7 @@ int dflash_block_attn_dense_suffix(const dflash_params* p, const void* q, const 
 
 /*
  * Dense-suffix form over fp8 context pages (PR #16150: the drafter reads its
- * context from the target's paged pool and "supports fp8 context storage").
+ * context from the target's paged pool, which may store it as fp8).
  * Requires p->kv_dtype = DFLASH_KV_FP8_E4M3.  k_pages / v_pages hold OCP
  * E4M3 codes, uint8 [num_pages, Hkv, P, D] (HND, 16-byte aligned), read as
  * k = k_scale * e4m3(code) and v = v_scale * e4m3(code) with one
@@ -274,10 +276,15 @@ int dflash_block_attn_dense_suffix(const dflash_params* p, const void* q, const 
  * positions < L_b only (slots past ceil(L_b / P) are never read).  The
  * block rows come from k_block / v_block, bf16 [B, K, Hkv, D], unscaled.
  * q, out, lse2, ctx_lens, page_table and the workspace as dflash_block_attn
- * (dflash_workspace_size(p) with the same *p).  The codes are widened to
- * bf16 exactly on the chip; the scores and the output use the scales in
- * fp32.  Both paths take it (the planner's choice as for bf16 pages; a forced
- * mma.sync plan whose code ring would not fit shared memory is refused).
+ * (dflash_workspace_size(p) with the same *p).  The codes are widened
+ * exactly on the chip (to bf16 on the tcgen05 path, to f16 on the mma.sync
+ * path); the scores and the output use the scales in fp32.  Both paths take
+ * it (the planner's choice as for bf16 pages; a forced mma.sync plan whose
+ * code ring would not fit shared memory is refused).  The mma.sync path
+ * computes in f16: q is scaled per warp by a power of two (exact), and a
+ * block row value k or v / v_scale of magnitude 65520 or more flags
+ * DFLASH_STATUS_FP8_RANGE in the device status (the output is then not
+ * meaningful).
  * Non-positive or non-finite scales are refused with DFLASH_ERR_INVALID.
  * Same return codes as dflash_block_attn.
  */

@@ -22,8 +22,8 @@ PR #20374 "Non-causal unwindowed DFlash draft block", description):
 
 The dense-suffix form may read fp8 context pages: OCP E4M3 codes with one
 dequantisation scale per tensor (``k = k_scale * e4m3(code)``, likewise V;
-the bf16 block rows take no scale) -- PR #16150, "supports fp8 context
-storage".
+the bf16 block rows take no scale) -- PR #16150: the drafter's context may
+be stored as fp8.
 
 Also the block placement and the K/V append (the block's rows written into
 the pool slots of positions ``L .. L+K-1``), plain data movement.

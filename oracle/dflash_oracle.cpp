@@ -21,11 +21,11 @@
 // Every key row is read through the page table: the row of logical position p
 // is pages[page_table[b][p / P]][h][p % P][:] (HND page layout, PR #20374
 // kernel sweep: "page 32, HND") -- or, in the dense-suffix form (PR #16150:
-// the draft context in the target's paged pool, "the dense noise suffix fused
-// into the same softmax"), the block's rows p = L+j come from dense tensors
+// the draft context in the target's paged pool, the block's noise rows a
+// dense suffix inside the one softmax), the block's rows p = L+j come from dense tensors
 // k_block[b][j][h][:], v_block[b][j][h][:] and only the context is paged.
 // The context pages of that form may also be stored in fp8 (PR #16150: the
-// drafter "supports fp8 context storage"): the OCP 8-bit E4M3 format (sign,
+// drafter's context may be kept as fp8): the OCP 8-bit E4M3 format (sign,
 // 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal,
 // S.1111.111 is NaN, no infinities) with one dequantisation scale per tensor,
 // k = k_scale * e4m3(code), v = v_scale * e4m3(code); the block rows stay

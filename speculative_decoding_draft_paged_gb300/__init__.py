@@ -18,7 +18,7 @@ from typing import Optional
 from . import _lib
 from ._lib import (DFLASH_ERR_DEVICE, DFLASH_ERR_INVALID, DFLASH_ERR_LAUNCH, DFLASH_ERR_WORKSPACE,
                    DFLASH_OK, DFLASH_STATUS_BAD_CTX_LEN, DFLASH_STATUS_BAD_PAGE,
-                   DFLASH_STATUS_TIMEOUT, KV_BF16, KV_FP8_E4M3, PATH_AUTO, PATH_MMA, PATH_TCGEN05,
+                   DFLASH_STATUS_TIMEOUT, DFLASH_STATUS_FP8_RANGE, KV_BF16, KV_FP8_E4M3, PATH_AUTO, PATH_MMA, PATH_TCGEN05,
                    Params, PlanInfo)
 
 __all__ = [
@@ -30,7 +30,7 @@ __all__ = [
     "KV_BF16", "KV_FP8_E4M3",
     "PATH_MMA", "PATH_TCGEN05", "DFLASH_OK", "DFLASH_ERR_INVALID", "DFLASH_ERR_WORKSPACE",
     "DFLASH_ERR_DEVICE", "DFLASH_ERR_LAUNCH", "DFLASH_STATUS_BAD_PAGE",
-    "DFLASH_STATUS_BAD_CTX_LEN", "DFLASH_STATUS_TIMEOUT",
+    "DFLASH_STATUS_BAD_CTX_LEN", "DFLASH_STATUS_TIMEOUT", "DFLASH_STATUS_FP8_RANGE",
 ]
 
 

@@ -22,6 +22,7 @@ DFLASH_ERR_LAUNCH = -4
 DFLASH_STATUS_BAD_PAGE = 1
 DFLASH_STATUS_BAD_CTX_LEN = 2
 DFLASH_STATUS_TIMEOUT = 4
+DFLASH_STATUS_FP8_RANGE = 8
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1

@@ -189,6 +189,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D += A * B, m16n8k16, f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Packs two fp32 values into an f16x2 word (round to nearest even).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 // Packs two fp32 values into a bf16x2 word (round to nearest even); `lo` in
 // the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -531,8 +547,20 @@ __device__ __forceinline__ uint4 widen8(uint32_t w0, uint32_t w1) {
                     e4m3x2_to_bf16x2(w1 >> 16));
 }
 
+// Two E4M3 codes -> f16x2, exactly (one conversion).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(codes)));
+  return h2;
+}
+
+__device__ __forceinline__ uint4 widen8_f16(uint32_t w0, uint32_t w1) {
+  return make_uint4(e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1),
+                    e4m3x2_to_f16x2(w1 >> 16));
+}
+
 // Widens a stage's K and V codes (a separate code area: K codes then V
-// codes, row r of each at r*D, words swizzled as code_word) into the bf16
+// codes, row r of each at r*D, words swizzled as code_word) into the f16
 // tiles the MMAs read (64-column halves of T rows x 128 B, 128-byte
 // swizzle), with threads tid = 0..nthr-1 taking words tid, tid + nthr, ...
 // The caller joins the threads afterwards.
@@ -548,8 +576,8 @@ __device__ __forceinline__ void widen_stage_coop(const uint8_t* codes, uint8_t* 
     const int r = rem / WPR, w = rem - (rem / WPR) * WPR;
     const uint4 c = *reinterpret_cast<const uint4*>(codes + (is_v ? T * D : 0) + code_word<D>(r, w));
     uint8_t* tile = is_v ? v_tile : k_tile;
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8(c.x, c.y);
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8(c.z, c.w);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8_f16(c.x, c.y);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8_f16(c.z, c.w);
   }
 }
 

@@ -24,11 +24,15 @@
 // Output: the unit's normalised partial O and base-2 LSE in the workspace, or,
 // with one unit per (request, kv head), the final bf16 output and LSE.
 // fp8 context (dense-suffix form over E4M3 pages): each stage's codes land in
-// a code ring beside the bf16 ring and all consumer warps widen them into the
-// stage's bf16 tiles together before their MMAs (the per-tensor scales fold
-// into the score scale and the output, as in the tcgen05 kernel).  The TMA
-// writes only the code ring then, so the generic writes into the bf16 tiles
-// need no proxy fence.
+// a code ring beside the tile ring and the consumer warps widen them, one
+// tile ahead of their MMAs, into the stage's tiles.  The MMAs take f16
+// operands then: every E4M3 value is an f16 value (one conversion per two
+// codes), the warp's query rows are scaled by a power of two into f16 range,
+// P is rounded to f16 with a 2^7 offset that keeps it above the f16
+// subnormals, and the block rows are written as f16 (a value outside the f16
+// range flags DFLASH_STATUS_FP8_RANGE).  The per-tensor scales fold into the
+// score scale and the output, as in the tcgen05 kernel.  The TMA writes only
+// the code ring, so the generic writes into the tiles need no proxy fence.
 
 #include <cuda_runtime.h>
 
@@ -47,17 +51,63 @@ struct MmaTile {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// m16n8k16 MMA with f16 (fp8 context) or bf16 operands.
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (F16)
+    mma_f16_16816(d, a, b0, b1);
+  else
+    mma_bf16_16816(d, a, b0, b1);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi) {
+  if constexpr (F16)
+    return pack_f16x2(lo, hi);
+  else
+    return pack_bf16x2(lo, hi);
+}
+
+// fp8 context: block rows [lo, hi) of one warp's key slice as f16 (times
+// `mul`) into a stage tile whose row 0 is position p0; a value that rounds
+// outside the f16 range flags DFLASH_STATUS_FP8_RANGE.
+template <int D, int T>
+__device__ __forceinline__ void write_suffix_rows_f16(uint8_t* tile, const uint16_t* src, const AttnArgs& a, int b,
+                                                      int h, int L, int p0, int lo, int hi, int lane, float mul) {
+  constexpr int CPR = D / 8;
+  const int r_lo = max(L, lo);
+  const int r_hi = min(L + a.K, hi);
+  const int n = (r_hi - r_lo) * CPR;
+  bool bad = false;
+  for (int e = lane; e < n; e += 32) {
+    const int pos = r_lo + e / CPR;
+    const int c = e - (e / CPR) * CPR;
+    const int rr = pos - p0;
+    const uint4 x = __ldg(
+        reinterpret_cast<const uint4*>(src + ((static_cast<size_t>(b) * a.K + (pos - L)) * a.Hkv + h) * D) + c);
+    auto cv = [&](uint32_t w) {
+      const float f0 = bf16_bits_to_f32(w & 0xffffu) * mul, f1 = bf16_bits_to_f32(w >> 16) * mul;
+      bad |= fabsf(f0) >= 65520.f || fabsf(f1) >= 65520.f;
+      return pack_f16x2(f0, f1);
+    };
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * T * 128 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) =
+        make_uint4(cv(x.x), cv(x.y), cv(x.z), cv(x.w));
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, DFLASH_STATUS_FP8_RANGE);
+}
+
 // Dense-suffix form: the block's K and V rows of one warp's key slice
-// [lo, hi) into stage tiles whose row 0 is position p0 (value rows divided
-// by v_scale with fp8 context).  Out of line: it runs on at most two
+// [lo, hi) into stage tiles whose row 0 is position p0 (f16, value rows
+// divided by v_scale, with fp8 context).  Out of line: it runs on at most two
 // tiles per unit and would otherwise crowd the tile loop.
 template <int D, int T, bool FP8>
 __device__ __noinline__ void write_slice_suffix(uint8_t* k_tile, uint8_t* v_tile, const AttnArgs& a,
                                                 int b, int h, int L, int p0, int lo, int hi, int lane) {
-  write_suffix_rows<D, T>(k_tile, a.k_block, a, b, h, L, p0, lo, hi, lane, 32);
   if constexpr (FP8) {
-    write_suffix_rows<D, T>(v_tile, a.v_block, a, b, h, L, p0, lo, hi, lane, 32, a.pblk_mul);
+    write_suffix_rows_f16<D, T>(k_tile, a.k_block, a, b, h, L, p0, lo, hi, lane, 1.f);
+    write_suffix_rows_f16<D, T>(v_tile, a.v_block, a, b, h, L, p0, lo, hi, lane, a.pblk_mul);
   } else {
+    write_suffix_rows<D, T>(k_tile, a.k_block, a, b, h, L, p0, lo, hi, lane, 32);
     write_suffix_rows<D, T>(v_tile, a.v_block, a, b, h, L, p0, lo, hi, lane, 32);
   }
 }
@@ -92,7 +142,7 @@ __global__ void __launch_bounds__(MAXT, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
-  // fp8 context: a code ring of NS stages after the bf16 ring.
+  // fp8 context: a code ring of NS stages after the tile ring.
   constexpr int kCodeRing = FP8 ? NS * MmaTile<D>::kCodeStageBytes : 0;
   const uint32_t code_u32 = base_u32 + NS * kStageBytes;
   const uint32_t q_u32 = base_u32 + NS * kStageBytes + kCodeRing;
@@ -212,6 +262,29 @@ __global__ void __launch_bounds__(MAXT, 1)
     for (int kk = 0; kk < D / 16; ++kk)
       ldmatrix_x4(q_u32 + swz_offset(16 * wr + (lane & 15), kk * 2 + (lane >> 4), a.R_pad),
                   qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+    // fp8 context: the warp's query rows as f16, times the power of two qs
+    // that puts their largest magnitude in [2^14, 2^15) (exact for every
+    // value down to 2^-29 of it); the score scale takes 1/qs.
+    float sl2 = 0.f;
+    if constexpr (FP8) {
+      float amax = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_f32(qa[kk][j] & 0xffffu)),
+                                   fabsf(bf16_bits_to_f32(qa[kk][j] >> 16))));
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      const int ex = (__float_as_int(amax) >> 23) & 0xff;
+      const float qs = __int_as_float(min(max(268 - ex, 1), 254) << 23);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          qa[kk][j] = pack_f16x2(bf16_bits_to_f32(qa[kk][j] & 0xffffu) * qs, bf16_bits_to_f32(qa[kk][j] >> 16) * qs);
+      sl2 = a.scale_log2 / qs;
+    }
 
     // Visible interval [lo, hi) of the two rows this lane accumulates.
     const int L = geo.L;
@@ -246,10 +319,37 @@ __global__ void __launch_bounds__(MAXT, 1)
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
+    // fp8 context: every consumer warp widens its share of tile it+1's codes
+    // (once they have landed) before its MMAs on tile it, and the warps join
+    // on tile it's widened_bar, whose arrivals came one iteration earlier.
+    // Tile it+1's stage is free then: its codes were loaded only after
+    // every consumer released the stage's previous tile.
+    auto widen_tile = [&](int j) -> bool {
+      const int sj = j % NS;
+      if (!mbar_wait_warp(full_bar(sj), (j / NS) & 1)) return false;
+      widen_stage_coop<D, T>(base + NS * kStageBytes + sj * MmaTile<D>::kCodeStageBytes, base + sj * kStageBytes,
+                             base + sj * kStageBytes + kTileBytes, threadIdx.x - 32, n_consumer_warps * 32);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(widened_bar(sj));
+      return true;
+    };
     bool aborted = false;
-    for (int it = 0; it < ntiles; ++it) {
+    if constexpr (FP8) {
+      if (ntiles > 0 && !widen_tile(0)) {
+        flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+        *abort_flag = 1;
+        aborted = true;
+      }
+    }
+    for (int it = 0; it < ntiles && !(FP8 && aborted); ++it) {
       const int st = it % NS;
-      if (!mbar_wait_warp(full_bar(st), (it / NS) & 1)) {
+      bool ok;
+      if constexpr (FP8) {
+        ok = (it + 1 >= ntiles || widen_tile(it + 1)) && mbar_wait_warp(widened_bar(st), (it / NS) & 1);
+      } else {
+        ok = mbar_wait_warp(full_bar(st), (it / NS) & 1);
+      }
+      if (!ok) {
         flag_status(a.status, DFLASH_STATUS_TIMEOUT);
         *abort_flag = 1;
         aborted = true;
@@ -258,21 +358,6 @@ __global__ void __launch_bounds__(MAXT, 1)
       const uint32_t k_st = base_u32 + st * kStageBytes;
       const uint32_t v_st = k_st + kTileBytes;
       const int p0 = (tile0 + it) * T + kb;  // logical position of the slice's first key
-      // fp8 context: all consumer warps widen the stage's codes and join on
-      // widened_bar (a bounded wait), before any block row is written into
-      // the tiles.
-      if constexpr (FP8) {
-        widen_stage_coop<D, T>(base + NS * kStageBytes + st * MmaTile<D>::kCodeStageBytes, base + st * kStageBytes,
-                               base + st * kStageBytes + kTileBytes, threadIdx.x - 32, n_consumer_warps * 32);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(widened_bar(st));
-        if (!mbar_wait_warp(widened_bar(st), (it / NS) & 1)) {
-          flag_status(a.status, DFLASH_STATUS_TIMEOUT);
-          *abort_flag = 1;
-          aborted = true;
-          break;
-        }
-      }
       if (dense && p0 + KPW > L && p0 < L + a.K) {
         // The block rows of this warp's key slice, from the dense tensors
         // (warps of other row groups with the same slice write the same
@@ -293,14 +378,14 @@ __global__ void __launch_bounds__(MAXT, 1)
           uint32_t b0, b1, b2, b3;
           const int key = kb + np * 16 + (lane & 7) + ((lane >> 4) << 3);
           ldmatrix_x4(k_st + swz_offset(key, kk * 2 + ((lane >> 3) & 1), T), b0, b1, b2, b3);
-          mma_bf16_16816(sacc[2 * np], qa[kk], b0, b1);
-          mma_bf16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+          mma_16816<FP8>(sacc[2 * np], qa[kk], b0, b1);
+          mma_16816<FP8>(sacc[2 * np + 1], qa[kk], b2, b3);
         }
       }
 
       // Mask by select (boundary tiles only; uniform branch), then the row
       // max of the raw scores (the scale is positive).  With fp8 context the
-      // scale includes k_scale, so a block key's score (bf16 key, no scale)
+      // scale includes k_scale, so a block key's score (f16 key, no scale)
       // is divided by k_scale first.
       const bool need_mask = (p0 < lo_rows_max) || (p0 + KPW > hi_rows_min) || (FP8 && p0 + KPW > L);
       if (need_mask) {
@@ -329,7 +414,7 @@ __global__ void __launch_bounds__(MAXT, 1)
         float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        mx *= a.scale_log2;
+        mx *= FP8 ? sl2 : a.scale_log2;
         corr[ri] = 1.f;
         if (mx > m_run[ri] + 8.f) {
           corr[ri] = (m_run[ri] == neg_inf()) ? 0.f : fast_exp2(m_run[ri] - mx);
@@ -337,12 +422,13 @@ __global__ void __launch_bounds__(MAXT, 1)
           m_run[ri] = mx;
           any_resc = true;
         }
-        const float neg_m = (m_run[ri] == neg_inf()) ? 0.f : -m_run[ri];
+        float neg_m = (m_run[ri] == neg_inf()) ? 0.f : -m_run[ri];
+        if constexpr (FP8) neg_m += 7.f;  // f16 P: p * 2^7 <= 2^15
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const float p_a = fast_exp2(fmaf(sacc[n][2 * ri], a.scale_log2, neg_m));
-          const float p_b = fast_exp2(fmaf(sacc[n][2 * ri + 1], a.scale_log2, neg_m));
+          const float p_a = fast_exp2(fmaf(sacc[n][2 * ri], FP8 ? sl2 : a.scale_log2, neg_m));
+          const float p_b = fast_exp2(fmaf(sacc[n][2 * ri + 1], FP8 ? sl2 : a.scale_log2, neg_m));
           sacc[n][2 * ri] = p_a;
           sacc[n][2 * ri + 1] = p_b;
           s4[n & 3] += p_a + p_b;
@@ -366,10 +452,10 @@ __global__ void __launch_bounds__(MAXT, 1)
 #pragma unroll
       for (int k2 = 0; k2 < KPW / 16; ++k2) {
         uint32_t pa[4];
-        pa[0] = pack_bf16x2(sacc[2 * k2][0], sacc[2 * k2][1]);
-        pa[1] = pack_bf16x2(sacc[2 * k2][2], sacc[2 * k2][3]);
-        pa[2] = pack_bf16x2(sacc[2 * k2 + 1][0], sacc[2 * k2 + 1][1]);
-        pa[3] = pack_bf16x2(sacc[2 * k2 + 1][2], sacc[2 * k2 + 1][3]);
+        pa[0] = pack_16x2<FP8>(sacc[2 * k2][0], sacc[2 * k2][1]);
+        pa[1] = pack_16x2<FP8>(sacc[2 * k2][2], sacc[2 * k2][3]);
+        pa[2] = pack_16x2<FP8>(sacc[2 * k2 + 1][0], sacc[2 * k2 + 1][1]);
+        pa[3] = pack_16x2<FP8>(sacc[2 * k2 + 1][2], sacc[2 * k2 + 1][3]);
         uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
         if (sanitize) {
           const int kp = p0 + k2 * 16 + 2 * (lane & 3);
@@ -389,8 +475,8 @@ __global__ void __launch_bounds__(MAXT, 1)
           v2 &= keep_lo;
           v1 &= keep_hi;
           v3 &= keep_hi;
-          mma_bf16_16816(o[2 * dn], pa, v0, v1);
-          mma_bf16_16816(o[2 * dn + 1], pa, v2, v3);
+          mma_16816<FP8>(o[2 * dn], pa, v0, v1);
+          mma_16816<FP8>(o[2 * dn + 1], pa, v2, v3);
         }
       }
       __syncwarp();
@@ -428,7 +514,7 @@ __global__ void __launch_bounds__(MAXT, 1)
                                          2 * (lane & 3)) = make_float2(v0, v1);
           }
           if ((lane & 3) == 0) {
-            const float lse = l > 0.f ? m_run[ri] + log2f(l) : neg_inf();
+            const float lse = l > 0.f ? m_run[ri] + (FP8 ? log2f(l) - 7.f : log2f(l)) : neg_inf();
             if (direct)
               a.lse2[out_row_index(a, b, h, r)] = lse;
             else
@@ -477,7 +563,7 @@ __global__ void __launch_bounds__(MAXT, 1)
           }
         }
         const float v = den > 0.f ? (FP8 ? num / den * a.out_mul : num / den) : 0.f;
-        const float lse = den > 0.f ? M + log2f(den) : neg_inf();
+        const float lse = den > 0.f ? M + (FP8 ? log2f(den) - 7.f : log2f(den)) : neg_inf();
         if (direct) {
           const size_t orow = out_row_index(a, b, h, r);
           a.out[orow * D + d] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);

@@ -31,6 +31,25 @@ def test_every_declared_symbol_is_exported(dflash_lib):
     assert set(names) == set(_lib.EXPORTS)
 
 
+def test_header_constants_match_binding():
+    """Every status, error, path and pool-type constant of dflash.h has the
+    same value in the Python binding."""
+    from speculative_decoding_draft_paged_gb300 import _lib
+
+    defs = dict((n, int(v)) for n, v in re.findall(r"#define\s+(DFLASH_[A-Z0-9_]+)\s+(-?\d+)", open(HEADER).read()))
+    assert "DFLASH_STATUS_FP8_RANGE" in defs
+    alias = {"DFLASH_PATH_": "PATH_", "DFLASH_KV_": "KV_"}
+    for n, v in defs.items():
+        py = n
+        for pre, rep in alias.items():
+            if n.startswith(pre):
+                py = rep + n[len(pre):]
+        if n == "DFLASH_VERSION" or not hasattr(_lib, py):
+            assert n.startswith(("DFLASH_VERSION", "DFLASH_MAX")), f"{n} has no binding constant"
+            continue
+        assert getattr(_lib, py) == v, n
+
+
 def test_struct_layout_matches_header(dflash_lib, tmp_path):
     """Compile a C program against the header and compare sizes/offsets."""
     from speculative_decoding_draft_paged_gb300 import _lib

@@ -48,8 +48,11 @@ def _fp8_case(spec, device, seed):
     return dev
 
 
-def _check(spec, device, k_scale, v_scale, path, split=0, seed=17):
+def _run(spec, device, k_scale, v_scale, path, split=0, seed=17, mutate=None):
+    """(out, lse, device status, inputs) of one fp8-context call on `path`."""
     d = _fp8_case(spec, device, seed)
+    if mutate is not None:
+        mutate(d)
     p = dflash.params_for(d["q"], d["kp8"], d["tab"], block_size=spec.K, window=spec.window,
                           future_keys=spec.future_keys, scale=spec.softmax_scale,
                           max_ctx_len=spec.max_ctx_len, force_path=path, force_split_tiles=split,
@@ -64,13 +67,22 @@ def _check(spec, device, k_scale, v_scale, path, split=0, seed=17):
         scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len, force_path=path,
         force_split_tiles=split, right_window=spec.right_window, workspace=ws)
     torch.cuda.synchronize()
-    assert dflash.read_device_status(ws) == 0, "a page-table slot past the context was read"
+    return out, lse, dflash.read_device_status(ws), d
+
+
+def _oracle_check(spec, d, out, lse, k_scale, v_scale):
     ro, rl = oracle.block_attn_fp8(
         to_bits(d["q"]), d["kp8"].cpu().numpy(), d["vp8"].cpu().numpy(), d["tab"].cpu().numpy(),
         np.asarray(spec.ctx_lens, np.int32), k_scale=k_scale, v_scale=v_scale, k_block=to_bits(d["kb"]),
         v_block=to_bits(d["vb"]), block_size=spec.K, window=spec.window, future_keys=spec.future_keys,
         right_window=spec.right_window, scale=spec.softmax_scale)
     assert_parity(metrics(out, lse, ro, rl), spec.name, value_scale=v_scale)
+
+
+def _check(spec, device, k_scale, v_scale, path, split=0, seed=17):
+    out, lse, status, d = _run(spec, device, k_scale, v_scale, path, split, seed)
+    assert status == 0, "a page-table slot past the context was read"
+    _oracle_check(spec, d, out, lse, k_scale, v_scale)
 
 
 def _minimax(win=0, fk=1, r=0, lens=(5000, 64, 0, 121, 63, 65)):
@@ -130,3 +142,20 @@ def test_fp8_long_context_d64(cuda_device, path):
     spec = W.CaseSpec("fp8_longctx", B=2, Hq=12, Hkv=2, D=64, K=7, P=32, window=0, future_keys=1,
                       ctx_lens=[20000, 777], seed=87, poison=True)
     _check(spec, cuda_device, k_scale=0.19, v_scale=1.3, path=path)
+
+
+def test_fp8_block_row_outside_f16_range(cuda_device):
+    """The mma.sync path computes in f16: a block value row element with
+    v / v_scale = 70000 is flagged in the device status; the tcgen05 path
+    (bf16 tiles) takes it and matches the oracle."""
+    spec = _gqa(64, 32, 7, 16, 2, lens=(100, 300))
+
+    def big_value(d):
+        d["vb"][1, 3, 0, 5] = 70.0
+
+    out, lse, status, d = _run(spec, cuda_device, 0.27, 0.001, dflash.PATH_MMA, mutate=big_value)
+    assert status & dflash.DFLASH_STATUS_FP8_RANGE
+    assert not (status & ~dflash.DFLASH_STATUS_FP8_RANGE)
+    out, lse, status, d = _run(spec, cuda_device, 0.27, 0.001, dflash.PATH_TCGEN05, mutate=big_value)
+    assert status == 0
+    _oracle_check(spec, d, out, lse, 0.27, 0.001)
