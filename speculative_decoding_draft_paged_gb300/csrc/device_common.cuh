@@ -559,26 +559,4 @@ __device__ __forceinline__ uint4 widen8_f16(uint32_t w0, uint32_t w1) {
                     e4m3x2_to_f16x2(w1 >> 16));
 }
 
-// Widens a stage's K and V codes (a separate code area: K codes then V
-// codes, row r of each at r*D, words swizzled as code_word) into the f16
-// tiles the MMAs read (64-column halves of T rows x 128 B, 128-byte
-// swizzle), with threads tid = 0..nthr-1 taking words tid, tid + nthr, ...
-// The caller joins the threads afterwards.
-template <int D, int T>
-__device__ __forceinline__ void widen_stage_coop(const uint8_t* codes, uint8_t* k_tile, uint8_t* v_tile, int tid,
-                                                 int nthr) {
-  constexpr int WPR = D / 16;  // code words per row
-  constexpr int kTileWords = T * WPR;
-#pragma unroll 1
-  for (int u = tid; u < 2 * kTileWords; u += nthr) {
-    const bool is_v = u >= kTileWords;
-    const int rem = is_v ? u - kTileWords : u;
-    const int r = rem / WPR, w = rem - (rem / WPR) * WPR;
-    const uint4 c = *reinterpret_cast<const uint4*>(codes + (is_v ? T * D : 0) + code_word<D>(r, w));
-    uint8_t* tile = is_v ? v_tile : k_tile;
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8_f16(c.x, c.y);
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8_f16(c.z, c.w);
-  }
-}
-
 }  // namespace dflash

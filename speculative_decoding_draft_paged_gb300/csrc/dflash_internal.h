@@ -22,6 +22,7 @@ constexpr int kHeaderBytes = 256;      // workspace header: status word + paddin
 constexpr int kMaxRows = 128;          // packed query rows per kv head (G*K)
 constexpr int kMaxBlock = 16;          // draft block size K
 constexpr int kStages = 4;             // TMA pipeline depth of the split kernels
+constexpr int kMmaWidenWarps = 2;      // mma.sync split kernel, fp8 context: code-widening warps
 constexpr int kMaxSplitTiles = 64;     // key tiles per split unit, at most
 constexpr int kMaxUnitSlots = 512;     // page-table slots one unit can touch (64 tiles x 8 pages)
 constexpr int kTcMaxBatch = 768;       // tcgen05 kernel: requests whose tile prefix fits shared memory

@@ -24,8 +24,11 @@
 // Output: the unit's normalised partial O and base-2 LSE in the workspace, or,
 // with one unit per (request, kv head), the final bf16 output and LSE.
 // fp8 context (dense-suffix form over E4M3 pages): each stage's codes land in
-// a code ring beside the tile ring and the consumer warps widen them, one
-// tile ahead of their MMAs, into the stage's tiles.  The MMAs take f16
+// a code ring beside the tile ring, and kWidenWarps extra warps widen them
+// into the stage's tiles while the consumers run their MMAs on the tiles
+// before (the consumers wait for the widened stage instead of the load).
+// A stage's tiles are free when its codes land: the producer loaded them
+// only after every consumer released the stage's previous tile.  The MMAs take f16
 // operands then: every E4M3 value is an f16 value (one conversion per two
 // codes), the warp's query rows are scaled by a power of two into f16 range,
 // P is rounded to f16 with a 2^7 offset that keeps it above the f16
@@ -50,6 +53,8 @@ struct MmaTile {
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+constexpr int kWidenWarps = kMmaWidenWarps;
 
 // m16n8k16 MMA with f16 (fp8 context) or bf16 operands.
 template <bool F16>
@@ -94,6 +99,48 @@ __device__ __forceinline__ void write_suffix_rows_f16(uint8_t* tile, const uint1
         make_uint4(cv(x.x), cv(x.y), cv(x.z), cv(x.w));
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(a.status, DFLASH_STATUS_FP8_RANGE);
+}
+
+// fp8 context: widening warp ww of nww converts the 8-row groups ww, ww+nww,
+// ... of a stage's 2T code rows (K rows, then V rows) into the stage's f16
+// tiles.  In a group, lane l takes row 2*(l/8) + (l%8)/4; at D = 64 its code
+// word l%4, at D = 128 the words wa = l%4 + 4*((l%8)/4) and wa^4, so that
+// every quarter-warp's 16-byte loads and stores fall in distinct bank groups.
+// Row offsets of a group add r0*D (codes) and r0*128 (tiles) to per-lane
+// offsets, as r0 is a multiple of 8 (both swizzles repeat every 8 rows).
+template <int D, int T>
+__device__ __forceinline__ void widen_stage_rows(const uint8_t* codes, uint8_t* k_tile, uint8_t* v_tile, int ww,
+                                                 int nww, int lane) {
+  const int r_in = 2 * (lane >> 3) + ((lane & 7) >> 2);
+  if constexpr (D == 64) {
+    const int w = lane & 3;
+    const int cw = code_word<64>(r_in, w);
+    const uint32_t t0 = swz_offset(r_in, 2 * w, T), t1 = swz_offset(r_in, 2 * w + 1, T);
+#pragma unroll 2
+    for (int g = ww; g < 2 * T / 8; g += nww) {
+      const int r0 = 8 * g;
+      const uint4 c = *reinterpret_cast<const uint4*>(codes + r0 * D + cw);
+      uint8_t* t = r0 < T ? k_tile + r0 * 128 : v_tile + (r0 - T) * 128;
+      *reinterpret_cast<uint4*>(t + t0) = widen8_f16(c.x, c.y);
+      *reinterpret_cast<uint4*>(t + t1) = widen8_f16(c.z, c.w);
+    }
+  } else {
+    const int wa = (lane & 3) + 4 * ((lane & 7) >> 2), wb = wa ^ 4;
+    const int ca = code_word<128>(r_in, wa), cb = code_word<128>(r_in, wb);
+    const uint32_t ta0 = swz_offset(r_in, 2 * wa, T), ta1 = swz_offset(r_in, 2 * wa + 1, T);
+    const uint32_t tb0 = swz_offset(r_in, 2 * wb, T), tb1 = swz_offset(r_in, 2 * wb + 1, T);
+#pragma unroll 1
+    for (int g = ww; g < 2 * T / 8; g += nww) {
+      const int r0 = 8 * g;
+      const uint4 x = *reinterpret_cast<const uint4*>(codes + r0 * D + ca);
+      const uint4 y = *reinterpret_cast<const uint4*>(codes + r0 * D + cb);
+      uint8_t* t = r0 < T ? k_tile + r0 * 128 : v_tile + (r0 - T) * 128;
+      *reinterpret_cast<uint4*>(t + ta0) = widen8_f16(x.x, x.y);
+      *reinterpret_cast<uint4*>(t + ta1) = widen8_f16(x.z, x.w);
+      *reinterpret_cast<uint4*>(t + tb0) = widen8_f16(y.x, y.y);
+      *reinterpret_cast<uint4*>(t + tb1) = widen8_f16(y.z, y.w);
+    }
+  }
 }
 
 // Dense-suffix form: the block's K and V rows of one warp's key slice
@@ -154,7 +201,7 @@ __global__ void __launch_bounds__(MAXT, 1)
   int* pg_smem = const_cast<int*>(abort_flag) + 4;  // kMaxUnitSlots page ids
   auto full_bar = [&](int st) { return bar_u32 + 8u * st; };
   auto empty_bar = [&](int st) { return bar_u32 + 8u * (NS + st); };
-  // fp8 context: every consumer warp has widened its share of stage st.
+  // fp8 context: every widening warp has widened its share of stage st.
   auto widened_bar = [&](int st) { return bar_u32 + 8u * (2 * NS + st); };
 
   const int warp = threadIdx.x >> 5;
@@ -165,7 +212,7 @@ __global__ void __launch_bounds__(MAXT, 1)
     for (int st = 0; st < NS; ++st) {
       mbar_init(full_bar(st), 1);
       mbar_init(empty_bar(st), n_consumer_warps);
-      if constexpr (FP8) mbar_init(widened_bar(st), n_consumer_warps);
+      if constexpr (FP8) mbar_init(widened_bar(st), kWidenWarps);
     }
     *abort_flag = 0;
     *issued_count = 0;
@@ -250,6 +297,22 @@ __global__ void __launch_bounds__(MAXT, 1)
         *issued_count = it + 1;
       }
     }
+  } else if (FP8 && warp > n_consumer_warps) {
+    // ------------------------------------------------------------ widening
+    const int ww = warp - 1 - n_consumer_warps;
+    for (int it = 0; it < ntiles; ++it) {
+      const int st = it % NS;
+      if (*abort_flag) break;
+      if (!mbar_wait_warp(full_bar(st), (it / NS) & 1)) {
+        flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      widen_stage_rows<D, T>(base + NS * kStageBytes + st * MmaTile<D>::kCodeStageBytes, base + st * kStageBytes,
+                             base + st * kStageBytes + kTileBytes, ww, kWidenWarps, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(widened_bar(st));
+    }
   } else {
     // ------------------------------------------------------------ consumers
     const int cw = warp - 1;
@@ -319,37 +382,10 @@ __global__ void __launch_bounds__(MAXT, 1)
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
-    // fp8 context: every consumer warp widens its share of tile it+1's codes
-    // (once they have landed) before its MMAs on tile it, and the warps join
-    // on tile it's widened_bar, whose arrivals came one iteration earlier.
-    // Tile it+1's stage is free then: its codes were loaded only after
-    // every consumer released the stage's previous tile.
-    auto widen_tile = [&](int j) -> bool {
-      const int sj = j % NS;
-      if (!mbar_wait_warp(full_bar(sj), (j / NS) & 1)) return false;
-      widen_stage_coop<D, T>(base + NS * kStageBytes + sj * MmaTile<D>::kCodeStageBytes, base + sj * kStageBytes,
-                             base + sj * kStageBytes + kTileBytes, threadIdx.x - 32, n_consumer_warps * 32);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(widened_bar(sj));
-      return true;
-    };
     bool aborted = false;
-    if constexpr (FP8) {
-      if (ntiles > 0 && !widen_tile(0)) {
-        flag_status(a.status, DFLASH_STATUS_TIMEOUT);
-        *abort_flag = 1;
-        aborted = true;
-      }
-    }
-    for (int it = 0; it < ntiles && !(FP8 && aborted); ++it) {
+    for (int it = 0; it < ntiles; ++it) {
       const int st = it % NS;
-      bool ok;
-      if constexpr (FP8) {
-        ok = (it + 1 >= ntiles || widen_tile(it + 1)) && mbar_wait_warp(widened_bar(st), (it / NS) & 1);
-      } else {
-        ok = mbar_wait_warp(full_bar(st), (it / NS) & 1);
-      }
-      if (!ok) {
+      if (!mbar_wait_warp(FP8 ? widened_bar(st) : full_bar(st), (it / NS) & 1)) {
         flag_status(a.status, DFLASH_STATUS_TIMEOUT);
         *abort_flag = 1;
         aborted = true;
@@ -596,7 +632,9 @@ int kpw_for(int D, int R_pad) {
 template <int D, int KPW, int MAXT = 288>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
              const CUtensorMap& tm_v, cudaStream_t stream) {
-  auto kern = a.fp8 ? split_mma_kernel<D, KPW, MAXT, true> : split_mma_kernel<D, KPW, MAXT, false>;
+  // fp8 context: kWidenWarps more warps (the register budget per thread
+  // follows the larger block).
+  auto kern = a.fp8 ? split_mma_kernel<D, KPW, MAXT + 32 * kWidenWarps, true> : split_mma_kernel<D, KPW, MAXT, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          plan.smem_bytes);
   if (err != cudaSuccess) return err;
@@ -626,7 +664,7 @@ int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMa
       case 32:
         // Three row groups of four key-slice warps need 416 threads; keep
         // the register budget of the 288-thread form otherwise.
-        return plan.threads > 288 ? launch_t<64, 32, 416>(a, plan, tm_k, tm_v, stream)
+        return plan.threads - (a.fp8 ? 32 * kWidenWarps : 0) > 288 ? launch_t<64, 32, 416>(a, plan, tm_k, tm_v, stream)
                                   : launch_t<64, 32, 288>(a, plan, tm_k, tm_v, stream);
       case 64: return launch_t<64, 64>(a, plan, tm_k, tm_v, stream);
       case 128: return launch_t<64, 128>(a, plan, tm_k, tm_v, stream);
