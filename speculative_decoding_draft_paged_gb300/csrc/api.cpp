@@ -143,7 +143,8 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
     k.T = split_mma_tile_keys(D);
     k.kpw = split_mma_kpw(D, k.R_pad);
     const int consumer_warps = (k.R_pad / 16) * (k.T / k.kpw);
-    k.threads = 32 * (1 + consumer_warps + (fp8 ? kMmaWidenWarps : 0));
+    k.threads = 32 * (1 + consumer_warps);
+    if (fp8) k.threads += 32 * mma_widen_warps(D, k.kpw, k.threads);
     k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8);
   } else {
     k.R_pad = 128;

@@ -547,16 +547,22 @@ __device__ __forceinline__ uint4 widen8(uint32_t w0, uint32_t w1) {
                     e4m3x2_to_bf16x2(w1 >> 16));
 }
 
-// Two E4M3 codes -> f16x2, exactly (one conversion).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(codes)));
-  return h2;
+// Four E4M3 codes (first code lowest) -> two f16x2 words, exactly; the
+// 16-bit halves of the source go to the conversions as they are.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t codes) {
+  uint2 r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(r.x), "=r"(r.y)
+      : "r"(codes));
+  return r;
 }
 
 __device__ __forceinline__ uint4 widen8_f16(uint32_t w0, uint32_t w1) {
-  return make_uint4(e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1),
-                    e4m3x2_to_f16x2(w1 >> 16));
+  const uint2 a = e4m3x4_to_f16x4(w0), b = e4m3x4_to_f16x4(w1);
+  return make_uint4(a.x, a.y, b.x, b.y);
 }
 
 }  // namespace dflash

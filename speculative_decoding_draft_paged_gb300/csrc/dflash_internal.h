@@ -22,7 +22,13 @@ constexpr int kHeaderBytes = 256;      // workspace header: status word + paddin
 constexpr int kMaxRows = 128;          // packed query rows per kv head (G*K)
 constexpr int kMaxBlock = 16;          // draft block size K
 constexpr int kStages = 4;             // TMA pipeline depth of the split kernels
-constexpr int kMmaWidenWarps = 2;      // mma.sync split kernel, fp8 context: code-widening warps
+// mma.sync split kernel, fp8 context: code-widening warps beside the block
+// of 1 + consumer warps (base_threads <= 288 or <= 416), as many as the
+// kernel's registers leave room for at one CTA per SM (the consumer code
+// takes 128 registers at D = 64, KPW <= 32 and up to 168 otherwise).
+DF_HD constexpr int mma_widen_warps(int D, int kpw, int base_threads) {
+  return base_threads > 288 ? 3 : ((D == 64 && kpw <= 32) ? 4 : 3);
+}
 constexpr int kMaxSplitTiles = 64;     // key tiles per split unit, at most
 constexpr int kMaxUnitSlots = 512;     // page-table slots one unit can touch (64 tiles x 8 pages)
 constexpr int kTcMaxBatch = 768;       // tcgen05 kernel: requests whose tile prefix fits shared memory

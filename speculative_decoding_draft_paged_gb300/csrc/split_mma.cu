@@ -24,7 +24,7 @@
 // Output: the unit's normalised partial O and base-2 LSE in the workspace, or,
 // with one unit per (request, kv head), the final bf16 output and LSE.
 // fp8 context (dense-suffix form over E4M3 pages): each stage's codes land in
-// a code ring beside the tile ring, and kWidenWarps extra warps widen them
+// a code ring beside the tile ring, and three or four extra warps widen them
 // into the stage's tiles while the consumers run their MMAs on the tiles
 // before (the consumers wait for the widened stage instead of the load).
 // A stage's tiles are free when its codes land: the producer loaded them
@@ -54,7 +54,6 @@ struct MmaTile {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-constexpr int kWidenWarps = kMmaWidenWarps;
 
 // m16n8k16 MMA with f16 (fp8 context) or bf16 operands.
 template <bool F16>
@@ -116,7 +115,7 @@ __device__ __forceinline__ void widen_stage_rows(const uint8_t* codes, uint8_t* 
     const int w = lane & 3;
     const int cw = code_word<64>(r_in, w);
     const uint32_t t0 = swz_offset(r_in, 2 * w, T), t1 = swz_offset(r_in, 2 * w + 1, T);
-#pragma unroll 2
+#pragma unroll 4
     for (int g = ww; g < 2 * T / 8; g += nww) {
       const int r0 = 8 * g;
       const uint4 c = *reinterpret_cast<const uint4*>(codes + r0 * D + cw);
@@ -129,7 +128,7 @@ __device__ __forceinline__ void widen_stage_rows(const uint8_t* codes, uint8_t* 
     const int ca = code_word<128>(r_in, wa), cb = code_word<128>(r_in, wb);
     const uint32_t ta0 = swz_offset(r_in, 2 * wa, T), ta1 = swz_offset(r_in, 2 * wa + 1, T);
     const uint32_t tb0 = swz_offset(r_in, 2 * wb, T), tb1 = swz_offset(r_in, 2 * wb + 1, T);
-#pragma unroll 1
+#pragma unroll 2
     for (int g = ww; g < 2 * T / 8; g += nww) {
       const int r0 = 8 * g;
       const uint4 x = *reinterpret_cast<const uint4*>(codes + r0 * D + ca);
@@ -159,8 +158,9 @@ __device__ __noinline__ void write_slice_suffix(uint8_t* k_tile, uint8_t* v_tile
   }
 }
 
+// MAXT: threads of the block without the widening warps (288 or 416).
 template <int D, int KPW, int MAXT, bool FP8>
-__global__ void __launch_bounds__(MAXT, 1)
+__global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAXT) : 0), 1)
     split_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
   constexpr int T = MmaTile<D>::T;
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(MAXT, 1)
   constexpr int kStageBytes = MmaTile<D>::kStageBytes;
   constexpr int NT = KPW / 8;               // 8-key accumulator tiles per warp
   static_assert(KPW % 16 == 0 && T % KPW == 0, "bad key slice");
+  constexpr int NWW = FP8 ? mma_widen_warps(D, KPW, MAXT) : 0;  // fp8 context: widening warps
 
   const int s = blockIdx.x;
   const int h = blockIdx.y;
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(MAXT, 1)
     for (int st = 0; st < NS; ++st) {
       mbar_init(full_bar(st), 1);
       mbar_init(empty_bar(st), n_consumer_warps);
-      if constexpr (FP8) mbar_init(widened_bar(st), kWidenWarps);
+      if constexpr (FP8) mbar_init(widened_bar(st), NWW);
     }
     *abort_flag = 0;
     *issued_count = 0;
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(MAXT, 1)
         break;
       }
       widen_stage_rows<D, T>(base + NS * kStageBytes + st * MmaTile<D>::kCodeStageBytes, base + st * kStageBytes,
-                             base + st * kStageBytes + kTileBytes, ww, kWidenWarps, lane);
+                             base + st * kStageBytes + kTileBytes, ww, NWW, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(widened_bar(st));
     }
@@ -632,9 +633,7 @@ int kpw_for(int D, int R_pad) {
 template <int D, int KPW, int MAXT = 288>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
              const CUtensorMap& tm_v, cudaStream_t stream) {
-  // fp8 context: kWidenWarps more warps (the register budget per thread
-  // follows the larger block).
-  auto kern = a.fp8 ? split_mma_kernel<D, KPW, MAXT + 32 * kWidenWarps, true> : split_mma_kernel<D, KPW, MAXT, false>;
+  auto kern = a.fp8 ? split_mma_kernel<D, KPW, MAXT, true> : split_mma_kernel<D, KPW, MAXT, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          plan.smem_bytes);
   if (err != cudaSuccess) return err;
@@ -664,7 +663,7 @@ int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMa
       case 32:
         // Three row groups of four key-slice warps need 416 threads; keep
         // the register budget of the 288-thread form otherwise.
-        return plan.threads - (a.fp8 ? 32 * kWidenWarps : 0) > 288 ? launch_t<64, 32, 416>(a, plan, tm_k, tm_v, stream)
+        return 32 * (1 + plan.R_pad / 16 * (MmaTile<64>::T / 32)) > 288 ? launch_t<64, 32, 416>(a, plan, tm_k, tm_v, stream)
                                   : launch_t<64, 32, 288>(a, plan, tm_k, tm_v, stream);
       case 64: return launch_t<64, 64>(a, plan, tm_k, tm_v, stream);
       case 128: return launch_t<64, 128>(a, plan, tm_k, tm_v, stream);
