@@ -123,13 +123,13 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   // D = 128 with R > 32 and more than 32 pairs (K = 3: equal at 32 pairs, 53
   // against 61 us at 64); the mma.sync kernel otherwise (its D = 64
   // long-context shapes run in about half the tcgen05 kernel's time).  Both
-  // kernels read fp8 pages (the mma.sync kernel then needs a code ring as
-  // well, which must fit its shared memory); with fp8 pages the tcgen05
-  // kernel also takes R > 64 at 8 pairs or fewer (16/1 heads, K = 7, 8
-  // requests: 35 us against 39).
+  // kernels read fp8 pages, by the same rule (16/1 heads, K = 7, fp8: 34 us
+  // on mma.sync against 36 at 8 pairs, 26 against 30 at 1, 89 against 73 on
+  // tcgen05 at 64); the mma.sync kernel then needs a code ring as well, which
+  // must fit its shared memory (R = 128 at D = 128 does not).
   const int64_t pairs = static_cast<int64_t>(p->batch) * p->num_kv_heads;
   const bool fp8 = p->kv_dtype == DFLASH_KV_FP8_E4M3;
-  const bool tc_pref = (k.R > 64 && (pairs > 8 || fp8)) || (D == 128 && k.R > 32 && pairs > 32);
+  const bool tc_pref = (k.R > 64 && pairs > 8) || (D == 128 && k.R > 32 && pairs > 32);
   const int R_pad_mma = (k.R + 15) / 16 * 16;
   const bool mma_ok = split_mma_smem_bytes(D, R_pad_mma, split_mma_kpw(D, R_pad_mma), fp8) <= kMaxSmemPerCta;
   int path = p->force_path;

@@ -519,13 +519,23 @@ __device__ __forceinline__ void pdl_wait_primary() {
 
 // ---- fp8 (E4M3) context codes, widened to bf16 in shared memory.
 
-// Two E4M3 codes (low 16 bits of `codes`, first code lowest) -> bf16x2,
-// exactly: cvt.rn.f16x2.e4m3x2 (every E4M3 value is an f16 value), f16 ->
-// f32, and the upper half of each f32 (at most 4 significant bits, so the
-// lower half is zero).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(codes)));
+// Four E4M3 codes (first code lowest) -> two f16x2 words, exactly (every
+// E4M3 value is an f16 value); the 16-bit halves of the source go to the
+// conversions as they are.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t codes) {
+  uint2 r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(r.x), "=r"(r.y)
+      : "r"(codes));
+  return r;
+}
+
+// f16x2 holding E4M3 values -> bf16x2, exactly: f16 -> f32, then the upper
+// half of each f32 (at most 4 significant bits, so the lower half is zero).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_exact(uint32_t h2) {
   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
   return __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
 }
@@ -543,23 +553,12 @@ __device__ __forceinline__ int code_word(int r, int w) {
 
 // Eight codes (two words) -> one 16-byte chunk of eight bf16 values.
 __device__ __forceinline__ uint4 widen8(uint32_t w0, uint32_t w1) {
-  return make_uint4(e4m3x2_to_bf16x2(w0), e4m3x2_to_bf16x2(w0 >> 16), e4m3x2_to_bf16x2(w1),
-                    e4m3x2_to_bf16x2(w1 >> 16));
+  const uint2 a = e4m3x4_to_f16x4(w0), b = e4m3x4_to_f16x4(w1);
+  return make_uint4(f16x2_to_bf16x2_exact(a.x), f16x2_to_bf16x2_exact(a.y), f16x2_to_bf16x2_exact(b.x),
+                    f16x2_to_bf16x2_exact(b.y));
 }
 
-// Four E4M3 codes (first code lowest) -> two f16x2 words, exactly; the
-// 16-bit halves of the source go to the conversions as they are.
-__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t codes) {
-  uint2 r;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-      : "=r"(r.x), "=r"(r.y)
-      : "r"(codes));
-  return r;
-}
-
+// Eight codes (two words) -> one 16-byte chunk of eight f16 values.
 __device__ __forceinline__ uint4 widen8_f16(uint32_t w0, uint32_t w1) {
   const uint2 a = e4m3x4_to_f16x4(w0), b = e4m3x4_to_f16x4(w1);
   return make_uint4(a.x, a.y, b.x, b.y);

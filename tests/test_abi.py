@@ -153,6 +153,9 @@ def test_fp8_context_plan_and_validation(dflash_lib):
     big = dict(head_dim=128, page_size=64, num_q_heads=16, num_kv_heads=1, block_size=8, max_pages_per_req=30,
                batch=64)
     assert d.plan(base_params(kv_dtype=d.KV_FP8_E4M3, **big))["path"] == d.PATH_TCGEN05
+    few = dict(big, batch=8, block_size=7)  # R = 112 over 8 pairs: mma.sync for both pool types
+    assert d.plan(base_params(**few))["path"] == d.PATH_MMA
+    assert d.plan(base_params(kv_dtype=d.KV_FP8_E4M3, **few))["path"] == d.PATH_MMA
     for path in (d.PATH_MMA, d.PATH_TCGEN05):
         assert d.workspace_size(base_params(kv_dtype=d.KV_FP8_E4M3, force_path=path)) > 0
     ws = d.workspace_size(p8)
