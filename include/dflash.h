@@ -59,8 +59,8 @@ extern "C" {
 #define DFLASH_STATUS_BAD_PAGE       1  /* a visible position's page id is outside [0, num_pages) */
 #define DFLASH_STATUS_BAD_CTX_LEN    2  /* ctx_lens[b] < 0 or > max_ctx_len (clamped) */
 #define DFLASH_STATUS_TIMEOUT        4  /* a pipeline wait ran out (never expected) */
-#define DFLASH_STATUS_FP8_RANGE      8  /* fp8 context on the mma.sync path: a block row value
-                                           (k, or v / v_scale) is outside the f16 range */
+#define DFLASH_STATUS_FP8_RANGE      8  /* fp8 context: a block row value outside the f16 range
+                                           (v / v_scale on both paths; k on mma.sync) */
 
 /* Element type of the page pools (dflash_params.kv_dtype). */
 #define DFLASH_KV_BF16               0  /* bf16 pages: every entry point but the fp8 one */
@@ -277,14 +277,14 @@ int dflash_block_attn_dense_suffix(const dflash_params* p, const void* q, const 
  * block rows come from k_block / v_block, bf16 [B, K, Hkv, D], unscaled.
  * q, out, lse2, ctx_lens, page_table and the workspace as dflash_block_attn
  * (dflash_workspace_size(p) with the same *p).  The codes are widened
- * exactly on the chip (to bf16 on the tcgen05 path, to f16 on the mma.sync
- * path); the scores and the output use the scales in fp32.  Both paths take
- * it (the planner's choice as for bf16 pages; a forced mma.sync plan whose
- * code ring would not fit shared memory is refused).  The mma.sync path
- * computes in f16: q is scaled per warp by a power of two (exact), and a
- * block row value k or v / v_scale of magnitude 65520 or more flags
- * DFLASH_STATUS_FP8_RANGE in the device status (the output is then not
- * meaningful).
+ * exactly on the chip; the scores and the output use the scales in fp32.
+ * Both paths take it (the planner's choice as for bf16 pages; a forced
+ * mma.sync plan whose code ring would not fit shared memory is refused).
+ * The P.V product runs on f16 operands on both paths, and Q.K^T too on the
+ * mma.sync path (q scaled per warp by a power of two, exactly; bf16 on the
+ * tcgen05 path): a block row value v / v_scale (both paths) or k (mma.sync)
+ * of magnitude 65520 or more flags DFLASH_STATUS_FP8_RANGE in the device
+ * status (the output is then not meaningful).
  * Non-positive or non-finite scales are refused with DFLASH_ERR_INVALID.
  * Same return codes as dflash_block_attn.
  */

@@ -38,15 +38,21 @@
 //                    S_j, masks by select, keeps a base-2 reference max that
 //                    moves only when a tile's max exceeds it by more than 8
 //                    (then O_g and the row sum are rescaled, exactly), and
-//                    writes P_j = 2^(s - m) in bf16 to its group's TMEM P
-//                    columns, the A operand of the PV MMA.  At the end of each
-//                    segment both groups merge the two states, each for half
-//                    of the output columns, and write them.
+//                    writes P_j = 2^(s - m) in bf16 (f16 with fp8 context)
+//                    to its group's TMEM P columns, the A operand of the PV
+//                    MMA.  At the end of each segment both groups merge the
+//                    two states, each for half of the output columns, and
+//                    write them.
 // fp8 context (dense-suffix form over E4M3 pages): each tile's codes land by
-// TMA in the upper part of its bf16 ring stage and are widened there to the
-// bf16 tile the MMAs read -- the K tiles by warps 10 and 11 (even and odd
-// tiles), each V tile by the softmax group that owns it -- and the
-// per-tensor scales fold into the score scale and the output.
+// TMA in the upper part of its ring stage and are widened there to the tile
+// the MMAs read -- the K tiles to bf16 by warps 0 and 11 (even and odd
+// tiles), each V tile to f16 by the softmax group that owns it (one
+// conversion per two codes) -- and the per-tensor scales fold into the score
+// scale and the output.  The PV product then runs on f16 operands: P is
+// written as f16 with a 2^7 offset (at most 2^15 under the lazy rescale,
+// clear of the f16 subnormals; the LSE takes it back), and the block's value
+// rows as f16, divided by v_scale (a value past the f16 range flags
+// DFLASH_STATUS_FP8_RANGE).
 // Every mbarrier wait is bounded (DFLASH_STATUS_TIMEOUT, then drain).
 
 #include <cuda_runtime.h>
@@ -158,8 +164,9 @@ __device__ __noinline__ bool fp8_fix_k(const AttnArgs& a, uint8_t* tile, uint32_
 }
 
 // The dense suffix's block value rows of a tile, moved from the staging
-// buffer (as write_staged_suffix) and multiplied by `mul` (1/v_scale: the
-// PV product then carries v_scale for every key, applied to the output).
+// buffer (as write_staged_suffix) as f16 and multiplied by `mul` (1/v_scale:
+// the PV product then carries v_scale for every key, applied to the output);
+// a value that rounds past the f16 range flags DFLASH_STATUS_FP8_RANGE.
 template <int D, int T, int MAXP>
 __device__ __forceinline__ void write_staged_suffix_scaled(uint8_t* tile, const uint8_t* stage, const AttnArgs& a,
                                                            int L, int p0, int tid, int nthr, float mul) {
@@ -175,17 +182,21 @@ __device__ __forceinline__ void write_staged_suffix_scaled(uint8_t* tile, const 
     const int rr = L + j - p0;
     if (rr < 0 || rr >= T) continue;
     const uint4 x = *reinterpret_cast<const uint4*>(stage + 16 * e);
+    bool bad = false;
     auto sc = [&](uint32_t w) {
-      return pack_bf16x2(bf16_bits_to_f32(w & 0xffffu) * mul, bf16_bits_to_f32(w >> 16) * mul);
+      const float f0 = bf16_bits_to_f32(w & 0xffffu) * mul, f1 = bf16_bits_to_f32(w >> 16) * mul;
+      bad |= fabsf(f0) >= 65520.f || fabsf(f1) >= 65520.f;
+      return pack_f16x2(f0, f1);
     };
     *reinterpret_cast<uint4*>(tile + (c >> 3) * T * 128 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) =
         make_uint4(sc(x.x), sc(x.y), sc(x.z), sc(x.w));
+    if (bad) flag_status(a.status, DFLASH_STATUS_FP8_RANGE);
   }
 }
 
 // D = 128: thread t of a softmax group's 128 widens V row t - 64 (t >= 64)
-// when its position lies in [lo, L): a row's bf16 bytes overwrite only its
-// own codes, so no other thread need wait.
+// to f16 when its position lies in [lo, L): a row's f16 bytes overwrite only
+// its own codes, so no other thread need wait.
 template <int T>
 __device__ __forceinline__ void widen_v_row(uint8_t* tile, int t, int p0, int lo, int L) {
   constexpr int D = 128;
@@ -194,8 +205,8 @@ __device__ __forceinline__ void widen_v_row(uint8_t* tile, int t, int p0, int lo
 #pragma unroll 1
   for (int w = 0; w < D / 16; ++w) {  // in order: see widen_k_tile
     const uint4 c = *reinterpret_cast<const uint4*>(tile + T * D + code_word<D>(r, w));
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8(c.x, c.y);
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8(c.z, c.w);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w, T)) = widen8_f16(c.x, c.y);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, 2 * w + 1, T)) = widen8_f16(c.z, c.w);
   }
 }
 
@@ -209,7 +220,7 @@ __device__ __forceinline__ void read_v_codes(const uint8_t* tile, int t, uint4 (
     raw[w] = *reinterpret_cast<const uint4*>(tile + T * D + code_word<D>(t & 63, (t >> 6) * (D / 32) + w));
 }
 
-// Writes those codes widened, for rows at positions in [lo, L) (the
+// Writes those codes widened to f16, for rows at positions in [lo, L) (the
 // context rows some key of the block sees); other rows are zeroed or
 // written by the caller.
 template <int D, int T>
@@ -221,8 +232,8 @@ __device__ __forceinline__ void write_v_widened(uint8_t* tile, int t, int p0, in
   const int c0 = (t >> 6) * (D / 16);
 #pragma unroll 1
   for (int w = 0; w < D / 32; ++w) {
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, c0 + 2 * w, T)) = widen8(raw[w].x, raw[w].y);
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, c0 + 2 * w + 1, T)) = widen8(raw[w].z, raw[w].w);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, c0 + 2 * w, T)) = widen8_f16(raw[w].x, raw[w].y);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, c0 + 2 * w + 1, T)) = widen8_f16(raw[w].z, raw[w].w);
   }
 }
 
@@ -659,7 +670,8 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, T, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      // fp8 context: P and the widened V tiles are f16.
+      constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(128, D, true) : idesc_bf16_f32(128, D, true);
       // Descriptors differ only in the start-address field (bits 0..13,
       // address >> 4): build each base once and add offsets >> 4.
       const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
@@ -881,7 +893,8 @@ __global__ void __launch_bounds__(384, 1)
           l_run *= corr;
           m_ref = mt;
         }
-        const float neg_m = (m_ref == ninf()) ? 0.f : -m_ref;
+        float neg_m = (m_ref == ninf()) ? 0.f : -m_ref;
+        if constexpr (FP8) neg_m += 7.f;  // f16 P: p * 2^7 <= 2^15
         float sm[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
@@ -889,7 +902,7 @@ __global__ void __launch_bounds__(384, 1)
           const float pa = fast_exp2(fmaf(__uint_as_float(sr[2 * c]), a.scale_log2, neg_m));
           const float pb = fast_exp2(fmaf(__uint_as_float(sr[2 * c + 1]), a.scale_log2, neg_m));
           sm[c & 3] += pa + pb;
-          pk[c] = pack_bf16x2(pa, pb);
+          pk[c] = FP8 ? pack_f16x2(pa, pb) : pack_bf16x2(pa, pb);
         }
         l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
 
@@ -994,7 +1007,7 @@ __global__ void __launch_bounds__(384, 1)
                                 sStage + grp * C::kStageBytes, lane_addr, grp * 64, grp, row, gthread == 0, w0, w1,
                                 inv, direct, sg.b, sg.h, static_cast<int>(unit));
         if (row < a.R && grp == 0) {
-          const float lse = l > 0.f ? M + log2f(l) : ninf();
+          const float lse = l > 0.f ? M + (FP8 ? log2f(l) - 7.f : log2f(l)) : ninf();
           if (direct)
             a.lse2[orow] = lse;
           else

@@ -44,10 +44,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor for kind::f16: bf16 A and B, fp32 accumulator,
-// A K-major, B K-major or MN-major, shape M x N.
+// A K-major, B K-major or MN-major, shape M x N.  Bits 4-5: accumulator
+// format (1 = f32); bits 7-9 / 10-12: A / B format (0 = f16, 1 = bf16);
+// bit 16: B MN-major; N >> 3 from bit 17, M >> 4 from bit 24.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with f16 A and B.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem], issued by one thread.
