@@ -1,8 +1,7 @@
 """Helpers for the GPU parity tests: run the library and the oracle on the same
 seeded inputs and compare them.
 
-Tolerances (from the stated bar for bf16 outputs, with the readings recorded
-in the design doc):
+Tolerances (the stated bar for bf16 outputs, read as follows):
 * relative L2 error of ``out`` against the unrounded fp64 oracle < 5e-3;
 * max abs error of ``out`` beyond the bf16 format's own rounding <= 1e-2
   (times the value scale where the values are not unit-variance: fp8 context
