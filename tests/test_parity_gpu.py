@@ -145,12 +145,12 @@ def test_forced_path_and_tiny_splits(cuda_device, path):
     assert m1["rel_l2"] < 5e-3 and m2["rel_l2"] < 5e-3
 
 
-@pytest.mark.parametrize("D,L", [(64, 9000), (128, 5000), (128, 1500)])
+@pytest.mark.parametrize("D,L", [(64, 9000), (128, 5000), (128, 1500), (64, 2041)])
 @pytest.mark.parametrize("window", [0, 1000])
 def test_combine_many_partials(cuda_device, D, L, window):
-    """One tile per unit on the mma.sync path: 12 to 141 partials per pair,
-    merged one lane per partial row (several rounds past 32 partials), with
-    partials that see no key (LSE -inf) under the window."""
+    """One tile per unit on the mma.sync path: 16 (L = 2041 at D = 64) to 141
+    partials per pair for the combine kernel, with partials that see no key
+    (LSE -inf) under the window."""
     spec = W.CaseSpec(f"many_partials_D{D}", B=3, Hq=8, Hkv=2, D=D, K=7, P=32, window=window,
                       future_keys=1, ctx_lens=[L, 200, L // 3], seed=13, poison=True)
     check_case(spec, cuda_device, force_path=dflash.PATH_MMA, force_split_tiles=1)
