@@ -187,13 +187,16 @@ def test_deterministic(cuda_device):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_guard_bands_untouched(cuda_device):
+@pytest.mark.parametrize("path", [dflash.PATH_MMA, dflash.PATH_TCGEN05])
+def test_guard_bands_untouched(cuda_device, path):
+    """No byte before or after out, lse2 or the workspace is written, on
+    either path (the tcgen05 path's TMA stores included)."""
     spec = W.CaseSpec("guards", B=3, Hq=16, Hkv=2, D=128, K=7, P=64, window=0, future_keys=1,
                       ctx_lens=[1500, 64, 3333], seed=12)
     inp = {k: v.to(cuda_device) for k, v in W.make_inputs(spec, "cpu").items()}
     p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K,
                           window=0, future_keys=1, scale=spec.softmax_scale,
-                          max_ctx_len=spec.max_ctx_len)
+                          max_ctx_len=spec.max_ctx_len, force_path=path)
     ws_bytes = dflash.workspace_size(p)
     G = 4096
     out_buf = torch.full((G + inp["q"].numel() * 2 + G,), 0xA5, dtype=torch.uint8, device=cuda_device)
