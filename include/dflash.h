@@ -23,14 +23,18 @@
  * The softmax statistics are returned as base-2 LSE (PR #21130 change 1) and
  * the caller sizes a workspace that includes the partial softmax statistics
  * (PR #21130 change 3); sequence lengths stay on the device so one captured
- * CUDA graph serves every step (PR #20374, "The batch size is static inside a
- * captured CUDA graph"; PR #16150 "Read the draft context K/V directly from
- * the target KV cache manager's paged pool": device-resident lengths).
+ * CUDA graph serves every step (PR #20374, description: a graph is captured
+ * for a fixed batch; PR #16150, the commit that takes the drafter's context
+ * from the target's paged pool: the lengths live on the device).
  *
- * Ownership: the caller owns every buffer.  The library allocates no device
- * or host memory, keeps no state beyond cached device attributes and the
- * per-kernel shared-memory opt-in, is thread-safe, and issues only
- * stream-ordered work (no host synchronisation) in dflash_block_attn.
+ * Ownership: the caller owns every buffer it passes.  The library allocates
+ * no device or host memory at run time and keeps no state beyond cached
+ * device attributes and the per-kernel shared-memory opt-in, with one
+ * exception: dflash_block_attn_static_ws uses a scratch array of
+ * DFLASH_STATIC_SCRATCH_BYTES that the library itself holds on every device
+ * that loads it, and caches that array's device address per context.  The
+ * library is thread-safe and issues only stream-ordered work (no host
+ * synchronisation) in dflash_block_attn.
  *
  * Errors are host-side return codes; nothing is launched when a code other
  * than DFLASH_OK is returned by validation.  Bad data found on the device (a
@@ -195,9 +199,11 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
  *   - Parameter sets whose dflash_workspace_size exceeds
  *     DFLASH_STATIC_SCRATCH_BYTES are refused with DFLASH_ERR_WORKSPACE and
  *     nothing is launched.
- *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress); make that first call before capturing a
- *     stream.
+ *   - The first call in a device's context looks up the array's device
+ *     address there (cudaGetSymbolAddress, which may also load the library's
+ *     device code) and caches it for that context; make that first call
+ *     before capturing a stream.  A context created anew (after
+ *     cudaDeviceReset, say) gets a fresh lookup on its first call.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind.  The kernels need no part of it to start at zero, and the
  *     device status word inside it is not reported here.  Calls whose work

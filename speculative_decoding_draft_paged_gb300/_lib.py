@@ -31,6 +31,22 @@ PATH_AUTO = 0
 PATH_MMA = 1
 PATH_TCGEN05 = 2
 
+
+
+def _header_static_scratch_bytes() -> int:
+    """DFLASH_STATIC_SCRATCH_BYTES as the public header defines it."""
+    import re
+
+    with open(os.path.join(_build.INCLUDE, "dflash.h")) as f:
+        m = re.search(r"#define\s+DFLASH_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", f.read())
+    if m is None:
+        raise RuntimeError("DFLASH_STATIC_SCRATCH_BYTES not found in include/dflash.h")
+    return int(m[1]) << int(m[2])
+
+
+# Size of the library-held scratch array of dflash_block_attn_static_ws.
+STATIC_SCRATCH_BYTES = _header_static_scratch_bytes()
+
 EXPORTS = (
     "dflash_workspace_size",
     "dflash_plan",

@@ -3,8 +3,8 @@
 // The draft block's K/V rows are stored in the paged cache right after the
 // request's context: block token j of request b goes to logical position
 // L_b + j, i.e. page page_table[b][(L_b + j) / P], offset (L_b + j) % P
-// (PR #20374: every block query attends the same keys once the block's K/V
-// are appended to the pages; the fused spec-tail kernels of the DFlash
+// (PR #20374: with the block's K/V appended to the pages, one key set
+// serves all block queries; the fused spec-tail kernels of the DFlash
 // drafter report these positions as the draft block placement).  One thread
 // moves one 16-byte piece of one (request, block token, kv head) row of K or
 // V, so consecutive threads write consecutive bytes of a row.  The kernel

@@ -8,7 +8,7 @@
 // in the non-causal form -- the block keys after i are merged into the row's
 // base-2 online softmax in the tile that holds them (TensorRT-LLM PR #21130,
 // "Why" and change 1) -- or L+i+1 in the causal form, where with no later key
-// the causal decode is the exact result (change 2).  The G*K query rows that share
+// the causal decode already gives the exact answer (change 2).  The G*K query rows that share
 // kv head h are packed into one tile (row r = i*G + g), so every K/V byte of
 // the unit is read from HBM once (PR #16150, split-KV rework: one tile of
 // packed query rows per kv head).

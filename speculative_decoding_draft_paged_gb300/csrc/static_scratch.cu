@@ -12,6 +12,8 @@
 
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "dflash.h"
@@ -27,12 +29,50 @@ constexpr size_t kStaticScratchBytes = DFLASH_STATIC_SCRATCH_BYTES;
 // obtained with cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
+// The array's address belongs to the context the library's device code was
+// loaded into: a context torn down and created again (cudaDeviceReset, for
+// one) loads the module anew, possibly elsewhere.  So the cached address is
+// keyed on the device and on the driver's id of its current context, which
+// is unique for the life of the process.
 constexpr int kMaxScratchDevices = 64;
+struct ScratchEntry {
+  unsigned long long ctx_id = 0;
+  void* ptr = nullptr;
+};
 std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxScratchDevices] = {};
+ScratchEntry g_scratch[kMaxScratchDevices];
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the first call on each device does it).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void* driver_fn(const char* name, unsigned version) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return fn;
+}
+
+// Id of the current context, 0 if there is none (or it cannot be read).
+unsigned long long current_ctx_id() {
+  std::call_once(g_ctx_once, [] {
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(driver_fn("cuCtxGetCurrent", 4000));
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(driver_fn("cuCtxGetId", 12000));
+  });
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context: looked
+// up with cudaGetSymbolAddress by the first call in each context (which also
+// loads the library's device code there if nothing has yet), then cached.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) {
@@ -40,15 +80,19 @@ int scratch_address(void** out) {
     return DFLASH_ERR_LAUNCH;
   }
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  const unsigned long long id = current_ctx_id();
+  ScratchEntry& e = g_scratch[dev];
+  if (e.ptr == nullptr || id == 0 || e.ctx_id != id) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
       cudaGetLastError();
       return DFLASH_ERR_LAUNCH;
     }
-    g_scratch_ptr[dev] = ptr;
+    e.ptr = ptr;
+    // The lookup makes the primary context current if it was not yet.
+    e.ctx_id = id != 0 ? id : current_ctx_id();
   }
-  *out = g_scratch_ptr[dev];
+  *out = e.ptr;
   return DFLASH_OK;
 }
 

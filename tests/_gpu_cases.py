@@ -10,7 +10,7 @@ Tolerances (the stated bar for bf16 outputs, read as follows):
   output is off by up to half an ulp from the exact value (0.0078 at
   |x| in [2, 4)), and a value near a rounding midpoint may round either way,
   so the bound is applied to the error the computation adds;
-* the pages' own form, max abs <= 8 bf16 ulp at the largest expected
+* the pages' own form, max abs <= 8 bf16 ulp of the biggest reference
   magnitude (PR #20374, test coverage), on the raw error;
 * max abs error of the base-2 LSE <= 1e-3.
 """

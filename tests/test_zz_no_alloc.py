@@ -22,7 +22,7 @@ from tests._gpu_cases import assert_parity, run_lib
 
 pytestmark = pytest.mark.gpu
 
-STATIC_BYTES = 32 << 20
+STATIC_BYTES = _lib.STATIC_SCRATCH_BYTES
 
 
 def call_static(spec, inp, out, lse):
