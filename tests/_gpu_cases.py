@@ -15,6 +15,9 @@ Tolerances (the stated bar for bf16 outputs, read as follows):
 * max abs error of the base-2 LSE <= 1e-3.
 """
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -79,10 +82,28 @@ def metrics(gpu_out, gpu_lse, ora_out, ora_lse) -> dict:
     }
 
 
+def log_parity(m: dict, what: str, value_scale: float = 1.0) -> None:
+    """Appends the achieved error figures of one comparison, with the share
+    of each bound they use, to the JSON-lines file named by
+    ``DFLASH_PARITY_LOG`` (when set), so that the headroom left under the
+    bounds can be tabulated per case."""
+    path = os.environ.get("DFLASH_PARITY_LOG")
+    if not path:
+        return
+    bound_abs = MAX_ABS_MAX * max(1.0, value_scale)
+    rec = {"case": what, **{k: v for k, v in m.items()},
+           "use_rel_l2": m["rel_l2"] / REL_L2_MAX, "use_max_abs": m["max_abs_excess"] / bound_abs,
+           "use_ulp8": m["max_abs_raw"] / (8 * m["ulp_at_max"]) if m["ulp_at_max"] else 0.0,
+           "use_lse": m["lse_abs"] / LSE_ABS_MAX, "value_scale": value_scale}
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
+
+
 def assert_parity(m: dict, what: str = "", value_scale: float = 1.0):
     """``value_scale``: the magnitude of the values relative to unit variance
     (the fp8 form's v_scale); the absolute bound scales with it, as the bf16
     rounding of the probabilities contributes an error proportional to |v|."""
+    log_parity(m, what, value_scale)
     assert not m["nan"], f"{what}: NaN in output {m}"
     assert m["rel_l2"] < REL_L2_MAX, f"{what}: {m}"
     assert m["max_abs_excess"] <= MAX_ABS_MAX * max(1.0, value_scale), f"{what}: {m}"

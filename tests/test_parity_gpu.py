@@ -298,47 +298,3 @@ def test_cuda_graph_replay_with_new_lengths(cuda_device):
         torch.cuda.synchronize()
         ro, rl = run_oracle(spec, {k: v.cpu() for k, v in inp.items()}, ctx_lens=np.array(new, np.int32))
         assert_parity(metrics(out, lse, ro, rl), f"graph replay {new}")
-
-
-# ----------------------------------------------------------------------------
-# Full-size workloads, in the launch configuration the benchmark times.
-# ----------------------------------------------------------------------------
-
-def test_full_minimax_headline(cuda_device):
-    """B=64, K=7, L=16384, W=4096, 16/1 heads, D=128, page 64: every row."""
-    spec = W.minimax(B=64, K=7, L=16384)
-    inp = W.make_inputs(spec, cuda_device)
-    out, lse = run_lib(spec, inp)
-    torch.cuda.synchronize()
-    host = {k: v.cpu() for k, v in inp.items()}
-    ro, rl = run_oracle(spec, host)
-    assert_parity(metrics(out, lse, ro, rl), spec.name)
-
-
-@pytest.mark.parametrize("Hq", [8, 12])
-def test_full_longctx_sampled(cuda_device, Hq):
-    """B=32 at 128K: the oracle checks 3 of the requests."""
-    spec = W.longctx(B=32, L=131072, Hq=Hq)
-    inp = W.make_inputs(spec, cuda_device)
-    out, lse = run_lib(spec, inp)
-    torch.cuda.synchronize()
-    ids = [0, 17, 31]
-    sub = compact_requests(inp, ids)
-    ro, rl = run_oracle(spec, sub)
-    assert_parity(metrics(out[ids], lse[ids], ro, rl), spec.name)
-
-
-def test_full_ragged_sampled(cuda_device):
-    """B=256, contexts uniform in [1K, 128K]: shortest, longest and 10 more."""
-    spec = W.ragged(B=256)
-    inp = W.make_inputs(spec, cuda_device)
-    out, lse = run_lib(spec, inp)
-    torch.cuda.synchronize()
-    lens = np.asarray(spec.ctx_lens)
-    rng = np.random.default_rng(5)
-    ids = sorted(set([int(lens.argmin()), int(lens.argmax())] + rng.choice(256, 10, replace=False).tolist()))
-    sub = compact_requests(inp, ids)
-    ro, rl = run_oracle(spec, sub)
-    assert_parity(metrics(out[ids], lse[ids], ro, rl), spec.name)
-    del inp
-    torch.cuda.empty_cache()
