@@ -129,8 +129,9 @@ typedef struct dflash_plan_info {
 /*
  * Workspace bytes dflash_block_attn needs for *p on the current device: a
  * 256-byte header (status word) and the fp32 partial softmax state of every
- * split unit or CTA slot (normalised output [units, R, D] and base-2 LSE
- * [units, R]).  Returns 0 when *p is invalid.  Deterministic for a given
+ * split unit or CTA slot (normalised output [units, R, D], base-2 LSE
+ * [units, R], and the base-2 log-sum of the rounded probabilities the output
+ * was normalised by [units, R]).  Returns 0 when *p is invalid.  Deterministic for a given
  * device model.
  */
 size_t dflash_workspace_size(const dflash_params* p);

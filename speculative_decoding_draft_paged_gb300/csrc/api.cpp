@@ -221,8 +221,9 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: header (status word) | partial LSEs | partial outputs, each
-// region 256-byte aligned.
+// Workspace: header (status word) | partial LSEs | partial output weights
+// (log-sums of the rounded probabilities) | partial outputs, each region
+// 256-byte aligned.
 
 size_t partial_rows_for(const KernelPlan& k) {
   return static_cast<size_t>(k.units) * (k.path == DFLASH_PATH_TCGEN05 ? k.S : 1) * k.R;
@@ -232,7 +233,7 @@ size_t workspace_bytes_for(const dflash_params* p, const KernelPlan& k) {
   const size_t rows = partial_rows_for(k);
   const size_t lse = align_up(rows * sizeof(float), 256);
   const size_t o = rows * p->head_dim * sizeof(float);
-  return kHeaderBytes + lse + o;
+  return kHeaderBytes + 2 * lse + o;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -433,8 +434,10 @@ int run_attention(const dflash_params* p, const void* q, const void* k_pages, co
   a.k_block = static_cast<const uint16_t*>(dense_k);
   a.v_block = static_cast<const uint16_t*>(dense_v);
   const size_t off_lse = kHeaderBytes;
+  const size_t lse_bytes = align_up(partial_rows_for(k) * sizeof(float), 256);
   a.part_lse = reinterpret_cast<float*>(ws + off_lse);
-  a.part_o = reinterpret_cast<float*>(ws + off_lse + align_up(partial_rows_for(k) * sizeof(float), 256));
+  a.part_lseo = reinterpret_cast<float*>(ws + off_lse + lse_bytes);
+  a.part_o = reinterpret_cast<float*>(ws + off_lse + 2 * lse_bytes);
   if (tc && (!encode_queries(&tm_q, q, p) || !encode_queries(&tm_out, out, p) ||
              !encode_partials(&tm_part, a.part_o, p, k.R, k.units * k.S)))
     return DFLASH_ERR_LAUNCH;

@@ -2,9 +2,10 @@
 //
 // One warp per output row (request b, block token i, query head hq): the
 // base-2 log-sum-exp combine of the row's partials (lse = log2 sum_s
-// 2^lse_s, O = sum_s 2^(lse_s - lse) O_s), the flash-decoding merge of
-// PR #16150 (split-KV rework), then out (bf16, nearest-even) and lse2 (fp32,
-// base 2).  The later block keys of the non-causal form are already folded
+// 2^lse_s, O = sum_s 2^(lseo_s) O_s / sum_s 2^(lseo_s), lseo_s the log-sum of
+// the rounded probabilities partial s was divided by), the flash-decoding
+// merge of PR #16150 (split-KV rework), then out (bf16, nearest-even) and
+// lse2 (fp32, base 2).  The later block keys of the non-causal form are already folded
 // into the partial that holds them, so there is nothing else to merge here.
 // Launched with programmatic dependent launch: everything that depends on
 // the inputs only is done before griddepcontrol.wait.
@@ -28,15 +29,19 @@ constexpr int kThreads = kWarpsPerBlock * 32;
 
 __device__ __forceinline__ float neg_inf_f() { return __int_as_float(0xff800000); }
 
-// Weighted sum of a row's partials into this lane's D/32 columns.  Few
-// partials (the usual case): one LSE per lane, then the partial rows four
+// Weighted sum of a row's partials into this lane's D/32 columns.  The LSE
+// combines the partial LSEs (exact probability sums); the outputs, each
+// divided by the sum of its rounded probabilities, are weighted by those
+// rounded sums (part_lseo), so the result is divided by the row's whole
+// rounded sum as it would be without a split.  Few partials (the usual
+// case): one partial per lane for the weights, then the partial rows four
 // at a time with their loads in flight together.  Otherwise lanes take
-// partials lane, lane+32, ... for the max and the sum, and the rows eight
+// partials lane, lane+32, ... for the max and the sums, and the rows eight
 // at a time.
 template <int D, typename UnitOf>
 __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, UnitOf unit_of,
                                             int lane, float (&acc)[D / 32], float& M_out,
-                                            float& den_out) {
+                                            float& den_out, float& deno_out) {
   constexpr int V = D / 32;
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
@@ -54,17 +59,26 @@ __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, Un
       o[3] = v.w;
     }
   };
+  auto warp_max = [](float x) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
+    return x;
+  };
+  auto warp_sum = [](float x) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+  };
   if (ns <= 32) {
-    const float ls = lane < ns ? a.part_lse[unit_of(lane) * a.R + r] : neg_inf_f();
-    float M = ls;
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+    const size_t u = lane < ns ? unit_of(lane) * a.R + r : 0;
+    const float ls = lane < ns ? a.part_lse[u] : neg_inf_f();
+    const float lo = lane < ns ? a.part_lseo[u] : neg_inf_f();
+    const float M = warp_max(ls);
     const float w = (ls == neg_inf_f()) ? 0.f : exp2f(ls - M);
-    float den = w;
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
+    const float wo = (lo == neg_inf_f()) ? 0.f : exp2f(lo - M);
     M_out = M;
-    den_out = den;
+    den_out = warp_sum(w);
+    deno_out = warp_sum(wo);
     if (M == neg_inf_f()) return;
     for (int s0 = 0; s0 < ns; s0 += 4) {
       float ov[4][V];
@@ -72,7 +86,7 @@ __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, Un
       for (int t = 0; t < 4; ++t) load_row(s0 + t < ns ? s0 + t : ns - 1, ov[t]);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const float wt = __shfl_sync(0xffffffffu, w, (s0 + t) & 31);
+        const float wt = __shfl_sync(0xffffffffu, wo, (s0 + t) & 31);
         const float wv = s0 + t < ns ? wt : 0.f;
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] = fmaf(wv, ov[t][e], acc[e]);
@@ -82,17 +96,18 @@ __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, Un
   }
   float M = neg_inf_f();
   for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, a.part_lse[unit_of(sp) * a.R + r]);
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-  float den = 0.f;
+  M = warp_max(M);
+  float den = 0.f, deno = 0.f;
   for (int sp = lane; sp < ns; sp += 32) {
-    const float ls = a.part_lse[unit_of(sp) * a.R + r];
+    const size_t u = unit_of(sp) * a.R + r;
+    const float ls = a.part_lse[u];
+    const float lo = a.part_lseo[u];
     den += (ls == neg_inf_f()) ? 0.f : exp2f(ls - M);
+    deno += (lo == neg_inf_f()) ? 0.f : exp2f(lo - M);
   }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) den += __shfl_xor_sync(0xffffffffu, den, m);
   M_out = M;
-  den_out = den;
+  den_out = warp_sum(den);
+  deno_out = warp_sum(deno);
   if (M == neg_inf_f()) return;
   for (int s0 = 0; s0 < ns; s0 += 8) {
     float ov[8][V];
@@ -101,8 +116,8 @@ __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, Un
     for (int t = 0; t < 8; ++t) {
       const int sp = s0 + t < ns ? s0 + t : ns - 1;
       load_row(sp, ov[t]);
-      const float ls = a.part_lse[unit_of(sp) * a.R + r];
-      wv[t] = (s0 + t < ns && ls != neg_inf_f()) ? exp2f(ls - M) : 0.f;
+      const float lo = a.part_lseo[unit_of(sp) * a.R + r];
+      wv[t] = (s0 + t < ns && lo != neg_inf_f()) ? exp2f(lo - M) : 0.f;
     }
 #pragma unroll
     for (int t = 0; t < 8; ++t)
@@ -113,9 +128,9 @@ __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, Un
 
 template <int D>
 __device__ __forceinline__ void write_row(const AttnArgs& a, long long row_id, int lane,
-                                          const float (&acc)[D / 32], float M, float den) {
+                                          const float (&acc)[D / 32], float M, float den, float deno) {
   constexpr int V = D / 32;
-  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const float inv = deno > 0.f ? 1.f / deno : 0.f;
   uint16_t* dst = a.out + static_cast<size_t>(row_id) * D + lane * V;
   if constexpr (V == 2) {
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
@@ -155,9 +170,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const AttnArgs a) {
 
   pdl_wait_primary();
   if (!active) return;
-  float acc[D / 32], M, den;
-  combine_row<D>(a, r, ns, [&](int sp) -> size_t { return unit0 + sp; }, lane, acc, M, den);
-  write_row<D>(a, row_id, lane, acc, M, den);
+  float acc[D / 32], M, den, deno;
+  combine_row<D>(a, r, ns, [&](int sp) -> size_t { return unit0 + sp; }, lane, acc, M, den, deno);
+  write_row<D>(a, row_id, lane, acc, M, den, deno);
 }
 
 template <int D>
@@ -186,12 +201,12 @@ __global__ void __launch_bounds__(kThreads, 6) combine_flat_kernel(const AttnArg
   const int slot0 = flat_tile_at(a, PB, fmap, static_cast<long long>(c0) * fmap.q) < g0 ? 1 : 0;
 
   pdl_wait_primary();
-  float acc[D / 32], M, den;
+  float acc[D / 32], M, den, deno;
   combine_row<D>(
       a, r, c1 - c0 + 1,
       [&](int sp) -> size_t { return static_cast<size_t>(c0 + sp) * 2 + (sp == 0 ? slot0 : 0); },
-      lane, acc, M, den);
-  write_row<D>(a, row_id, lane, acc, M, den);
+      lane, acc, M, den, deno);
+  write_row<D>(a, row_id, lane, acc, M, den, deno);
 }
 
 template <int D>

@@ -45,6 +45,11 @@ struct AttnArgs {
   float* lse2;                // [B, K, Hq]
   float* part_o;              // [units, R, D]  normalised partial output
   float* part_lse;            // [units, R]     partial base-2 LSE
+  // [units, R]: m + log2 of the sum of the probabilities as rounded for the
+  // P.V product, which the partial output was divided by.  The combine
+  // weights the outputs by it (and the LSE by part_lse), so a row's output is
+  // normalised by the same rounded sum whatever the split.
+  float* part_lseo;
   uint32_t* status;           // workspace status word
   const uint16_t* k_block;    // dense-suffix form: bf16 [B, K, Hkv, D] block rows, else null
   const uint16_t* v_block;    //   (then the pages hold the context positions < L only)

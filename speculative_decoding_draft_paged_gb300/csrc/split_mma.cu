@@ -21,6 +21,11 @@
 // owns query rows [16 wr, 16 wr + 16) and keys [wk KPW, (wk+1) KPW) of every
 // tile, keeps its own online-softmax state in registers (base 2), and the
 // warps of a row group merge their states through shared memory at the end.
+// Two row sums are kept: the exact one (for the LSE) and the sum of the
+// probabilities as rounded for the P.V product (one more MMA per 16 keys,
+// against an all-ones B fragment), which the output is divided by, so that
+// the rounding of a dominant probability cancels instead of reaching the
+// output.
 // Output: the unit's normalised partial O and base-2 LSE in the workspace, or,
 // with one unit per (request, kv head), the final bf16 output and LSE.
 // fp8 context (dense-suffix form over E4M3 pages): each stage's codes land in
@@ -379,6 +384,14 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
 
     float m_run[2] = {neg_inf(), neg_inf()};
     float l_run[2] = {0.f, 0.f};
+    // Row sums of the probabilities as rounded for the P.V product, from one
+    // extra MMA per 16 keys against an all-ones B fragment: lt[0..1] for row
+    // lane/4, lt[2..3] for row lane/4 + 8 (every column holds the sum, and
+    // every lane of a quad the whole sum over the warp's key slice).  The
+    // output is divided by it, so the rounding of a dominant probability
+    // cancels; the LSE keeps the exact sum l_run.
+    float lt[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr uint32_t kOnes = FP8 ? 0x3C003C00u : 0x3F803F80u;  // 1.0 in both halves
     float o[D / 8][4];
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -480,6 +493,10 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
           o[n][2] *= corr[1];
           o[n][3] *= corr[1];
         }
+        lt[0] *= corr[0];
+        lt[1] *= corr[0];
+        lt[2] *= corr[1];
+        lt[3] *= corr[1];
       }
 
       // O += P V.  Value rows outside the unit's visible range may hold
@@ -493,6 +510,7 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
         pa[1] = pack_16x2<FP8>(sacc[2 * k2][2], sacc[2 * k2][3]);
         pa[2] = pack_16x2<FP8>(sacc[2 * k2 + 1][0], sacc[2 * k2 + 1][1]);
         pa[3] = pack_16x2<FP8>(sacc[2 * k2 + 1][2], sacc[2 * k2 + 1][3]);
+        mma_16816<FP8>(lt, pa, kOnes, kOnes);
         uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
         if (sanitize) {
           const int kp = p0 + k2 * 16 + 2 * (lane & 3);
@@ -530,6 +548,7 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
     const size_t unit = (static_cast<size_t>(b) * a.Hkv + h) * a.S + s;
     float* part_o = a.part_o + unit * a.R * D;
     float* part_lse = a.part_lse + unit * a.R;
+    float* part_lseo = a.part_lseo + unit * a.R;
     const bool direct = a.S == 1;  // one unit per (request, kv head): final output
     (void)aborted;
 
@@ -539,7 +558,8 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
         const int r = 16 * wr + (lane >> 2) + 8 * ri;
         if (r < a.R) {
           const float l = l_run[ri];
-          const float inv = l > 0.f ? (FP8 ? a.out_mul : 1.f) / l : 0.f;
+          const float lr = lt[2 * ri];
+          const float inv = lr > 0.f ? (FP8 ? a.out_mul : 1.f) / lr : 0.f;
 #pragma unroll
           for (int n = 0; n < D / 8; ++n) {
             const float v0 = o[n][2 * ri] * inv, v1 = o[n][2 * ri + 1] * inv;
@@ -552,10 +572,12 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
           }
           if ((lane & 3) == 0) {
             const float lse = l > 0.f ? m_run[ri] + (FP8 ? log2f(l) - 7.f : log2f(l)) : neg_inf();
-            if (direct)
+            if (direct) {
               a.lse2[out_row_index(a, b, h, r)] = lse;
-            else
+            } else {
               part_lse[r] = lse;
+              part_lseo[r] = lr > 0.f ? m_run[ri] + (FP8 ? log2f(lr) - 7.f : log2f(lr)) : neg_inf();
+            }
           }
         }
       }
@@ -567,6 +589,7 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
       float* sc_o = reinterpret_cast<float*>(base);              // [cw][16][D]
       float* sc_m = sc_o + n_consumer_warps * 16 * D;            // [cw][16]
       float* sc_l = sc_m + n_consumer_warps * 16;                // [cw][16]
+      float* sc_lt = sc_l + n_consumer_warps * 16;               // [cw][16]
 #pragma unroll
       for (int ri = 0; ri < 2; ++ri) {
         const int rr = (lane >> 2) + 8 * ri;
@@ -577,6 +600,7 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
         if ((lane & 3) == 0) {
           sc_m[cw * 16 + rr] = m_run[ri];
           sc_l[cw * 16 + rr] = l_run[ri];
+          sc_lt[cw * 16 + rr] = lt[2 * ri];
         }
       }
       named_barrier(1, n_ct);
@@ -589,7 +613,7 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
         float M = neg_inf();
 #pragma unroll
         for (int w = 0; w < NWK; ++w) M = fmaxf(M, sc_m[(g * NWK + w) * 16 + rr]);
-        float num = 0.f, den = 0.f;
+        float num = 0.f, den = 0.f, dent = 0.f;
         if (M != neg_inf()) {
 #pragma unroll
           for (int w = 0; w < NWK; ++w) {
@@ -597,9 +621,10 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
             const float wt = exp2f(sc_m[cwi * 16 + rr] - M);
             num += wt * sc_o[(cwi * 16 + rr) * D + d];
             den += wt * sc_l[cwi * 16 + rr];
+            dent += wt * sc_lt[cwi * 16 + rr];
           }
         }
-        const float v = den > 0.f ? (FP8 ? num / den * a.out_mul : num / den) : 0.f;
+        const float v = dent > 0.f ? (FP8 ? num / dent * a.out_mul : num / dent) : 0.f;
         const float lse = den > 0.f ? M + (FP8 ? log2f(den) - 7.f : log2f(den)) : neg_inf();
         if (direct) {
           const size_t orow = out_row_index(a, b, h, r);
@@ -607,7 +632,10 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
           if (d == 0) a.lse2[orow] = lse;
         } else {
           part_o[static_cast<size_t>(r) * D + d] = v;
-          if (d == 0) part_lse[r] = lse;
+          if (d == 0) {
+            part_lse[r] = lse;
+            part_lseo[r] = dent > 0.f ? M + (FP8 ? log2f(dent) - 7.f : log2f(dent)) : neg_inf();
+          }
         }
       }
     }

@@ -40,9 +40,13 @@
 //                    (then O_g and the row sum are rescaled, exactly), and
 //                    writes P_j = 2^(s - m) in bf16 (f16 with fp8 context)
 //                    to its group's TMEM P columns, the A operand of the PV
-//                    MMA.  At the end of each segment both groups merge the
-//                    two states, each for half of the output columns, and
-//                    write them.
+//                    MMA and of a second MMA against an all-ones operand,
+//                    which sums the rounded P_j per row into TMEM (L_g).  At
+//                    the end of each segment both groups merge the two
+//                    states, each for half of the output columns, and write
+//                    them: the output divided by the rounded sum (so the
+//                    rounding of a dominant probability cancels), the LSE
+//                    from the exact one.
 // fp8 context (dense-suffix form over E4M3 pages): each tile's codes land by
 // TMA in the upper part of its ring stage and are widened there to the tile
 // the MMAs read -- the K tiles to bf16 by warps 0 and 11 (even and odd
@@ -90,13 +94,20 @@ struct TcCfg {
   // Dense-suffix form: per softmax group, the block's value rows in flight.
   static constexpr int kOffVStage = (kOffLc + 4 * kTcMaxBatch + 15) / 16 * 16;
   static constexpr int kVStageBytes = kMaxBlock * D * 2;
-  static constexpr int kSmem = kOffVStage + 2 * kVStageBytes + 1024;
+  // An all-ones 16 x 16 B operand (K-major, no swizzle: four 8 x 16-byte
+  // core matrices): P_j times it gives the row sums of the probabilities as
+  // rounded for the P.V product, in TMEM beside O.
+  static constexpr int kOffOnes = (kOffVStage + 2 * kVStageBytes + 127) / 128 * 128;
+  static constexpr int kOnesBytes = 512;
+  static constexpr int kSmem = kOffOnes + kOnesBytes + 1024;
   // TMEM columns: S0 [0,64) S1 [64,128) O0 [128,128+D) O1 [256,256+D)
-  // P0 [384,416) P1 [416,448) (bf16 pairs).
+  // P0 [384,416) P1 [416,448) (bf16 pairs), rounded row sums L0 [448,464)
+  // L1 [464,480) (16 equal columns each).
   static constexpr int kTmemCols = 512;
   static constexpr int kColO0 = 128;
   static constexpr int kColO1 = 256;
   static constexpr int kColP = 384;
+  static constexpr int kColL = 448;
   static constexpr int kThreads = 384;
 };
 
@@ -477,6 +488,11 @@ __global__ void __launch_bounds__(384, 1)
       *reinterpret_cast<uint4*>(gbase + C::kOffQ + swz_offset(row, c, 128)) =
           make_uint4(0u, 0u, 0u, 0u);
     }
+    // The all-ones operand of the row-sum MMA, in the P type (bf16, or f16
+    // with fp8 context).
+    constexpr uint32_t kOne2 = FP8 ? 0x3C003C00u : 0x3F803F80u;
+    for (int idx = threadIdx.x; idx < C::kOnesBytes / 16; idx += C::kThreads)
+      *reinterpret_cast<uint4*>(gbase + C::kOffOnes + 16 * idx) = make_uint4(kOne2, kOne2, kOne2, kOne2);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -677,6 +693,10 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
       const uint64_t dv = smem_desc_sw128(sV, T * 128, 1024);
+      // The ones operand: B of N = 16 rows x K = 16, K-major without
+      // swizzle, its four core matrices at 0, 128 (next K), 256 (next N).
+      const uint64_t d_ones = smem_desc_noswz(base + C::kOffOnes, 128, 256);
+      constexpr uint32_t idesc_l = FP8 ? idesc_f16_f32(128, 16, false) : idesc_bf16_f32(128, 16, false);
       Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
       int q_seg = -1;            // segment whose query tile has been waited for
       int seg_prev = 0;          // segment of tile j-1
@@ -738,6 +758,11 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < T / 16; ++kk)
           umma_bf16_ts(tmem + o_col, tmem + C::kColP + g * (T / 2) + kk * 8,
                        dv + ((v_off + kk * 16 * 128) >> 4), idesc_pv, (!fresh || kk > 0) ? 1u : 0u);
+        // L_g += P_j 1: the row sums of the rounded probabilities.
+#pragma unroll
+        for (int kk = 0; kk < T / 16; ++kk)
+          umma_bf16_ts(tmem + C::kColL + g * 16, tmem + C::kColP + g * (T / 2) + kk * 8, d_ones, idesc_l,
+                       (!fresh || kk > 0) ? 1u : 0u);
         umma_commit(v_empty(st));
         umma_commit(pv_done(g));
         last_pv = jj;
@@ -925,6 +950,11 @@ __global__ void __launch_bounds__(384, 1)
               for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
               tmem_st32(lane_addr + o_col + cc * 32, o);
             }
+            uint32_t lv[16];
+            tmem_ld16_wait(lane_addr + C::kColL + grp * 16, lv);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) lv[e] = __float_as_uint(__uint_as_float(lv[e]) * corr);
+            tmem_st16(lane_addr + C::kColL + grp * 16, lv);
             tmem_wait_st();
           }
         }
@@ -1000,7 +1030,17 @@ __global__ void __launch_bounds__(384, 1)
         const float w0 = (s0.x == ninf() || s0.y == 0.f) ? 0.f : fast_exp2(s0.x - M);
         const float w1 = (s1.x == ninf() || s1.y == 0.f) ? 0.f : fast_exp2(s1.x - M);
         const float l = w0 * s0.y + w1 * s1.y;
-        const float inv = l > 0.f ? a.out_mul / l : 0.f;
+        // The output is divided by the sum of the probabilities as rounded for
+        // the P.V product (the MMA against the ones operand), so the rounding
+        // of a dominant probability cancels; the LSE keeps the exact sum.  A
+        // group with no key in the segment holds a stale sum: select.
+        float lr = 0.f;
+        {
+          uint32_t r0[16], r1[16];
+          tmem_ld16x2_wait(lane_addr + C::kColL, lane_addr + C::kColL + 16, r0, r1);
+          lr = (w0 > 0.f ? w0 * __uint_as_float(r0[0]) : 0.f) + (w1 > 0.f ? w1 * __uint_as_float(r1[0]) : 0.f);
+        }
+        const float inv = lr > 0.f ? a.out_mul / lr : 0.f;
         // D = 128: group g writes columns [64g, 64g + 64); D = 64: group 0 all.
         if (grp * 64 < D)
           store_segment_rows<D>(a, &tm_out, &tm_part, gbase + C::kOffStage + grp * C::kStageBytes,
@@ -1008,10 +1048,12 @@ __global__ void __launch_bounds__(384, 1)
                                 inv, direct, sg.b, sg.h, static_cast<int>(unit));
         if (row < a.R && grp == 0) {
           const float lse = l > 0.f ? M + (FP8 ? log2f(l) - 7.f : log2f(l)) : ninf();
-          if (direct)
+          if (direct) {
             a.lse2[orow] = lse;
-          else
+          } else {
             a.part_lse[unit * a.R + row] = lse;
+            a.part_lseo[unit * a.R + row] = lr > 0.f ? M + (FP8 ? log2f(lr) - 7.f : log2f(lr)) : ninf();
+          }
         }
       }
       // Every softmax thread has read stop_word, the states and both
