@@ -106,11 +106,12 @@ typedef struct dflash_params {
 
 /*
  * What the planner chose for a parameter set (for tests and benchmarks).
- * mma.sync path: a grid of B * Hkv * max_splits units of split_tiles tiles.
- * tcgen05 path: `units` persistent CTAs (at most one per SM) that share the
- * key tiles of all (request, kv head) pairs laid end to end, split_tiles
- * each at max_ctx_len (fewer, from the actual lengths, on the device), with
- * max_splits = 2 partial slots per CTA.
+ * Flat split (flat = 1, the tcgen05 path): `units` persistent CTAs (at most
+ * one per SM unless force_split_tiles is set) that share the key tiles of
+ * all (request, kv head) pairs laid end to end, split_tiles each at
+ * max_ctx_len (fewer, from the actual lengths, on the device), with
+ * max_splits = 2 partial slots per CTA.  Unit grid (flat = 0, the mma.sync
+ * path): a grid of B * Hkv * max_splits units of split_tiles tiles.
  */
 typedef struct dflash_plan_info {
   int32_t path;              /* DFLASH_PATH_MMA or DFLASH_PATH_TCGEN05 */
@@ -123,7 +124,8 @@ typedef struct dflash_plan_info {
   int32_t threads;           /* threads per CTA of the split kernel */
   int32_t smem_bytes;        /* dynamic shared memory per CTA of the split kernel */
   int32_t num_sms;           /* SM count the plan was sized for */
-  int32_t reserved[3];
+  int32_t flat;              /* 1: persistent flat split; 0: unit grid */
+  int32_t reserved[2];
 } dflash_plan_info;
 
 /*

@@ -100,7 +100,8 @@ class PlanInfo(ctypes.Structure):
         ("threads", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
         ("num_sms", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("flat", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 

@@ -522,6 +522,7 @@ int dflash_plan(const dflash_params* p, dflash_plan_info* info) {
   info->threads = k.threads;
   info->smem_bytes = k.smem_bytes;
   info->num_sms = k.num_sms;
+  info->flat = k.path == DFLASH_PATH_TCGEN05 ? 1 : 0;
   return DFLASH_OK;
 }
 

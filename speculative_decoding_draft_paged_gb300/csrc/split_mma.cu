@@ -465,13 +465,13 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         mx *= FP8 ? sl2 : a.scale_log2;
-        corr[ri] = 1.f;
-        if (mx > m_run[ri] + 8.f) {
-          corr[ri] = (m_run[ri] == neg_inf()) ? 0.f : fast_exp2(m_run[ri] - mx);
-          l_run[ri] *= corr[ri];
-          m_run[ri] = mx;
-          any_resc = true;
-        }
+        // Selects, not a branch: the rows of a warp disagree on moving.
+        const bool up = mx > m_run[ri] + 8.f;
+        const float cr = (m_run[ri] == neg_inf()) ? 0.f : fast_exp2(m_run[ri] - mx);
+        corr[ri] = up ? cr : 1.f;
+        l_run[ri] *= corr[ri];
+        m_run[ri] = up ? mx : m_run[ri];
+        any_resc |= up;
         float neg_m = (m_run[ri] == neg_inf()) ? 0.f : -m_run[ri];
         if constexpr (FP8) neg_m += 7.f;  // f16 P: p * 2^7 <= 2^15
         float s4[4] = {0.f, 0.f, 0.f, 0.f};

@@ -911,13 +911,12 @@ __global__ void __launch_bounds__(384, 1)
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
         // The reference max moves only when this tile's max passes it by more
         // than 8 (p stays <= 2^8); O_g and l are rescaled then, which is exact.
+        // Selects, not a branch: rows of a warp disagree on moving.
         const bool resc = mt > m_ref + 8.f;
-        float corr = 1.f;
-        if (resc) {
-          corr = (m_ref == ninf()) ? 0.f : fast_exp2(m_ref - mt);
-          l_run *= corr;
-          m_ref = mt;
-        }
+        const float cr = (m_ref == ninf()) ? 0.f : fast_exp2(m_ref - mt);
+        const float corr = resc ? cr : 1.f;
+        l_run *= corr;
+        m_ref = resc ? mt : m_ref;
         float neg_m = (m_ref == ninf()) ? 0.f : -m_ref;
         if constexpr (FP8) neg_m += 7.f;  // f16 P: p * 2^7 <= 2^15
         float sm[4] = {0.f, 0.f, 0.f, 0.f};

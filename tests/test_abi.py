@@ -211,19 +211,22 @@ def test_planner_covers_every_length(dflash_lib, kw):
     R = p.num_q_heads // p.num_kv_heads * p.block_size
     assert pl["rows"] == R and pl["rows_padded"] >= R
     ws = d.workspace_size(p)
+    # Per partial row: D output values and two log-sums.
     if pl["path"] == d.PATH_TCGEN05:
+        assert pl["flat"] == 1
+    if pl["flat"]:
         # Flat split: `units` CTAs of C tiles cover every pair at max_ctx_len,
         # two partial slots per CTA, at most one CTA per SM unless forced.
         assert S == 2
         assert pl["units"] * C >= p.batch * p.num_kv_heads * worst
         if not kw.get("force_split_tiles"):
             assert pl["units"] <= pl["num_sms"]
-        assert ws >= 256 + 2 * pl["units"] * R * (p.head_dim + 1) * 4
+        assert ws >= 256 + 2 * pl["units"] * R * (p.head_dim + 2) * 4
     else:
         assert pl["units"] == p.batch * p.num_kv_heads * S
         assert S * C >= worst
         assert (S - 1) * C < worst + C
-        assert ws >= 256 + pl["units"] * R * (p.head_dim + 1) * 4
+        assert ws >= 256 + pl["units"] * R * (p.head_dim + 2) * 4
     if kw.get("force_split_tiles"):
         assert C == kw["force_split_tiles"]
 

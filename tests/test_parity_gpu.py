@@ -298,3 +298,19 @@ def test_cuda_graph_replay_with_new_lengths(cuda_device):
         torch.cuda.synchronize()
         ro, rl = run_oracle(spec, {k: v.cpu() for k, v in inp.items()}, ctx_lens=np.array(new, np.int32))
         assert_parity(metrics(out, lse, ro, rl), f"graph replay {new}")
+
+
+def test_mma_unit_grid_large_batch(cuda_device):
+    """800 short requests, more than the tcgen05 flat split takes: the
+    mma.sync unit grid (one CTA per (request, kv head, split))."""
+    rng = np.random.default_rng(12)
+    lens = [int(x) for x in rng.integers(0, 700, size=800)]
+    spec = W.CaseSpec("mma_grid_B800", B=len(lens), Hq=8, Hkv=2, D=64, K=7, P=32, window=0, future_keys=1,
+                      ctx_lens=lens, seed=13, poison=True)
+    p = dflash.make_params(batch=spec.B, num_q_heads=spec.Hq, num_kv_heads=spec.Hkv, head_dim=spec.D,
+                           page_size=spec.P, max_pages_per_req=spec.max_pages, num_pages=spec.num_pages,
+                           block_size=spec.K, window=spec.window, future_keys=spec.future_keys,
+                           scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len)
+    pl = dflash.plan(p)
+    assert pl["path"] == dflash.PATH_MMA and pl["flat"] == 0
+    check_case(spec, cuda_device)

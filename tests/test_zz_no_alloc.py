@@ -66,13 +66,17 @@ def test_static_scratch_matches_regular_entry_point_twice(cuda_device):
 
 
 def test_static_scratch_refuses_oversized_plans(cuda_device):
-    # Candidates from small to large; the long ragged batch needs far more
-    # partial state than the array holds.
-    for s in (W.adp(B=64, K=7, L=16384), W.ragged(B=64, lo=120000, hi=131072)):
+    # Candidates from small to large: the persistent splits need little
+    # partial state; one-tile ranges over a long batch, or the unit grid of
+    # a batch too large for the flat split, need far more than the array
+    # holds.
+    cands = [(W.adp(B=64, K=7, L=16384), 0), (W.ragged(B=64, lo=120000, hi=131072), 1),
+             (W.ragged(B=800, lo=120000, hi=131072), 0)]
+    for s, force in cands:
         p = dflash.make_params(batch=s.B, num_q_heads=s.Hq, num_kv_heads=s.Hkv, head_dim=s.D,
                                page_size=s.P, max_pages_per_req=s.max_pages, num_pages=s.num_pages,
                                block_size=s.K, window=s.window, future_keys=s.future_keys,
-                               scale=s.softmax_scale, max_ctx_len=s.max_ctx_len)
+                               scale=s.softmax_scale, max_ctx_len=s.max_ctx_len, force_split_tiles=force)
         need = dflash.workspace_size(p)
         if need <= STATIC_BYTES:
             continue
