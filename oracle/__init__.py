@@ -26,11 +26,14 @@ the bf16 block rows take no scale) -- PR #16150: the drafter's context may
 be stored as fp8.
 
 Also the block placement and the K/V append (the block's rows written into
-the pool slots of positions ``L .. L+K-1``), plain data movement.
+the pool slots of positions ``L .. L+K-1``), plain data movement; and the
+context-parallel form: one part of a request's keys (logical positions
+``[key_begin[b], key_end[b])``) and the base-2 log-sum-exp merge of parts.
 
 Pinned by ``tests/test_oracle_pins.py`` (dense brute force, causal decode,
 LSE merge of disjoint key sets, page-permutation invariance, closed forms,
-placement and append round trips).
+placement and append round trips, parts against the masked dense attention
+and their merge against the whole).
 """
 
 from __future__ import annotations
@@ -84,6 +87,12 @@ def load_library(path: str):
     f = lib.oracle_append_block_kv
     f.restype = ctypes.c_int
     f.argtypes = [i32] * 7 + [vp] * 6
+    f = lib.oracle_block_attn_part
+    f.restype = ctypes.c_int
+    f.argtypes = [i32] * 11 + [dbl] + [vp] * 8 + [i32] + [vp, vp, i32]
+    f = lib.oracle_combine_parts
+    f.restype = ctypes.c_int
+    f.argtypes = [i32, ctypes.c_int64, i32] + [vp] * 4
     return lib
 
 
@@ -140,6 +149,62 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size, window,
         _ptr(k_block), _ptr(v_block), _ptr(req_ids), n, _ptr(out), _ptr(lse2), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_block_attn failed with status {rc}")
+    return out, lse2
+
+
+def block_attn_part(q, k_pages, v_pages, page_table, ctx_lens, key_begin, key_end, *, block_size,
+                    window, future_keys, scale, right_window=0, req_ids=None, nthreads=0, lib=None):
+    """One context-parallel part: ``(out, lse2)`` in float64 over the visible
+    keys at logical positions ``[key_begin[b], key_end[b])`` (int32 ``[B]``);
+    rows that see none get 0 and -inf.  Arguments as ``block_attn``."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_pages = np.ascontiguousarray(k_pages, dtype=np.uint16)
+    v_pages = np.ascontiguousarray(v_pages, dtype=np.uint16)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    ctx_lens = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    key_begin = np.ascontiguousarray(key_begin, dtype=np.int32)
+    key_end = np.ascontiguousarray(key_end, dtype=np.int32)
+    B, K, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_pages.shape
+    if K != block_size or D2 != D or v_pages.shape != k_pages.shape:
+        raise ValueError("inconsistent shapes")
+    if page_table.shape[0] != B or ctx_lens.shape != (B,) or key_begin.shape != (B,) or \
+            key_end.shape != (B,):
+        raise ValueError("inconsistent batch")
+    if req_ids is not None:
+        req_ids = np.ascontiguousarray(req_ids, dtype=np.int32)
+        n = int(req_ids.shape[0])
+    else:
+        n = B
+    out = np.zeros((n, K, Hq, D), dtype=np.float64)
+    lse2 = np.zeros((n, K, Hq), dtype=np.float64)
+    rc = (lib or _load()).oracle_block_attn_part(
+        B, Hq, Hkv, D, P, page_table.shape[1], num_pages, K, int(window), int(future_keys),
+        int(right_window), float(scale), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+        _ptr(ctx_lens), _ptr(key_begin), _ptr(key_end), _ptr(req_ids), n, _ptr(out), _ptr(lse2),
+        int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_block_attn_part failed with status {rc}")
+    return out, lse2
+
+
+def combine_parts(part_out, part_lse2, lib=None):
+    """Merge of context-parallel parts: ``part_out [n, ..., D]`` and
+    ``part_lse2 [n, ...]`` (float64) -> ``(out [..., D], lse2 [...])`` by the
+    base-2 log-sum-exp combine."""
+    part_out = np.ascontiguousarray(part_out, dtype=np.float64)
+    part_lse2 = np.ascontiguousarray(part_lse2, dtype=np.float64)
+    n = part_out.shape[0]
+    D = part_out.shape[-1]
+    if part_lse2.shape != part_out.shape[:-1]:
+        raise ValueError("part_lse2 must match part_out without its last axis")
+    rows = int(np.prod(part_lse2.shape[1:])) if part_lse2.ndim > 1 else 1
+    out = np.zeros(part_out.shape[1:], dtype=np.float64)
+    lse2 = np.zeros(part_lse2.shape[1:], dtype=np.float64)
+    rc = (lib or _load()).oracle_combine_parts(int(n), rows, int(D), _ptr(part_out), _ptr(part_lse2),
+                                               _ptr(out), _ptr(lse2))
+    if rc != 0:
+        raise ValueError(f"oracle_combine_parts failed with status {rc}")
     return out, lse2
 
 

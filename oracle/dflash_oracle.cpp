@@ -37,6 +37,16 @@
 //   lse2 = (m + ln Z) / ln 2         (the base-2 log-sum-exp, PR #21130 change 1)
 // No blocking, splitting, merging or reordering beyond that definition.
 //
+// Context-parallel parts (the split of one request's keys across ranks that
+// exchange their partial (O, lse2) once, then merge them): a part covers the
+// logical key positions [key_begin[b], key_end[b]) of request b's L + K
+// positions (context and block alike), and its result is the same
+// definition over the visible positions that lie in that range -- out
+// normalised over them, lse2 their base-2 log-sum-exp; a row that sees none
+// of them gets out = 0 and lse2 = -inf.  Parts that tile [0, L+K) merge into
+// the whole attention by the base-2 log-sum-exp combine of PR #21130
+// (change 1): lse = log2 sum_s 2^lse_s, out = sum_s 2^(lse_s - lse) out_s.
+//
 // Inputs are bf16 bit patterns (uint16), widened exactly to double.
 
 #include <atomic>
@@ -80,6 +90,8 @@ struct Problem {
   const uint8_t* k_pages8;  // fp8 context pages (then k_pages / v_pages are unused), or null
   const uint8_t* v_pages8;
   double k_scale, v_scale;
+  const int32_t* key_begin;  // context-parallel part: keys [key_begin[b], key_end[b]), or null
+  const int32_t* key_end;
 };
 
 // A key or value row: bf16 bits (scale 1), or fp8 codes with their scale.
@@ -115,6 +127,17 @@ int attend_row(const Problem& pr, int b, int i, int hq, double* out_row, double*
   const int r = pr.future_keys ? pr.K - 1 : pr.right_window;
   const int j_last = std::min(pr.K - 1, i + r);
   for (int j = i + 1; j <= j_last; ++j) pos.push_back(L + j);
+  if (pr.key_begin != nullptr) {
+    std::vector<int64_t> kept;
+    for (int64_t p : pos)
+      if (p >= pr.key_begin[b] && p < pr.key_end[b]) kept.push_back(p);
+    pos.swap(kept);
+  }
+  if (pos.empty()) {  // nothing visible: the empty sum
+    for (int d = 0; d < pr.D; ++d) out_row[d] = 0.0;
+    *lse_row = -INFINITY;
+    return 0;
+  }
 
   const uint16_t* qrow = pr.q + ((static_cast<int64_t>(b) * pr.K + i) * pr.Hq + hq) * pr.D;
   std::vector<double> qd(pr.D);
@@ -223,8 +246,58 @@ int oracle_block_attn(int B, int Hq, int Hkv, int D, int P, int max_pages, int n
     return -1;
   if ((k_block == nullptr) != (v_block == nullptr)) return -1;
   Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, right_window, scale,
-             q, k_pages, v_pages, page_table, ctx_lens, k_block, v_block, nullptr, nullptr, 1.0, 1.0};
+             q, k_pages, v_pages, page_table, ctx_lens, k_block, v_block, nullptr, nullptr, 1.0, 1.0,
+             nullptr, nullptr};
   return run_items(pr, req_ids, n_req, out, lse2, nthreads);
+}
+
+// One context-parallel part: the attention over the visible keys whose
+// logical positions lie in [key_begin[b], key_end[b]) (int32 [B]); out is
+// normalised over them, lse2 is their base-2 log-sum-exp; a row that sees
+// none gets 0 and -inf.  Otherwise as oracle_block_attn (paged block rows).
+int oracle_block_attn_part(int B, int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
+                           int K, int W, int future_keys, int right_window, double scale,
+                           const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                           const int32_t* page_table, const int32_t* ctx_lens,
+                           const int32_t* key_begin, const int32_t* key_end,
+                           const int32_t* req_ids, int n_req, double* out, double* lse2,
+                           int nthreads) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0 || K <= 0 ||
+      W < 0 || max_pages <= 0 || num_pages <= 0 || right_window < 0)
+    return -1;
+  if (key_begin == nullptr || key_end == nullptr) return -1;
+  Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, right_window, scale,
+             q, k_pages, v_pages, page_table, ctx_lens, nullptr, nullptr, nullptr, nullptr, 1.0, 1.0,
+             key_begin, key_end};
+  return run_items(pr, req_ids, n_req, out, lse2, nthreads);
+}
+
+// The merge of n_parts partial results of the same rows: part s holds
+// out[s][row][0..D) and lse2[s][row] (rows = B*K*Hq).  Base-2 log-sum-exp
+// combine (PR #21130, change 1): lse = log2 sum_s 2^lse_s and
+// out = sum_s 2^(lse_s - lse) out_s; a row with every lse_s = -inf gets 0 and
+// -inf.  Returns 0, or -1 for bad sizes.
+int oracle_combine_parts(int n_parts, int64_t rows, int D, const double* part_out,
+                         const double* part_lse2, double* out, double* lse2) {
+  if (n_parts <= 0 || rows < 0 || D <= 0) return -1;
+  for (int64_t r = 0; r < rows; ++r) {
+    double m = -INFINITY;
+    for (int s = 0; s < n_parts; ++s) m = std::max(m, part_lse2[s * rows + r]);
+    for (int d = 0; d < D; ++d) out[r * D + d] = 0.0;
+    if (m == -INFINITY) {
+      lse2[r] = -INFINITY;
+      continue;
+    }
+    double z = 0.0;
+    for (int s = 0; s < n_parts; ++s) z += std::exp2(part_lse2[s * rows + r] - m);
+    const double lse = m + std::log2(z);
+    for (int s = 0; s < n_parts; ++s) {
+      const double w = std::exp2(part_lse2[s * rows + r] - lse);
+      for (int d = 0; d < D; ++d) out[r * D + d] += w * part_out[(s * rows + r) * D + d];
+    }
+    lse2[r] = lse;
+  }
+  return 0;
 }
 
 // The dense-suffix form over fp8 (E4M3) context pages: k_pages8 / v_pages8
@@ -245,7 +318,7 @@ int oracle_block_attn_fp8(int B, int Hq, int Hkv, int D, int P, int max_pages, i
     return -1;
   Problem pr{B, Hq, Hkv, D, P, max_pages, num_pages, K, W, future_keys ? 1 : 0, right_window, scale,
              q, nullptr, nullptr, page_table, ctx_lens, k_block, v_block, k_pages8, v_pages8,
-             k_scale, v_scale};
+             k_scale, v_scale, nullptr, nullptr};
   return run_items(pr, req_ids, n_req, out, lse2, nthreads);
 }
 

@@ -726,3 +726,145 @@ def test_move_pins_reject_planted_mistakes(oracle_mod, tmp_path):
         subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-pthread", str(path), "-o", so],
                        check=True)
         assert not _move_pins_pass(oracle.load_library(so)), f"planted mistake not caught: {name}"
+
+
+# ----------------------------------------------------------------------------
+# Context-parallel parts: a part covers logical keys [kb, ke) of L + K
+# ----------------------------------------------------------------------------
+
+def range_mask(L, K, kb, ke):
+    pos = np.arange(L + K)[None, :]
+    return np.broadcast_to((pos >= kb) & (pos < ke), (K, L + K))
+
+
+def _check_part_against_dense(out, lse2, q, dk, dv, scale, L, K, W, fk, kb, ke, rtol=1e-11, atol=1e-12):
+    """Rows that see a key of [kb, ke): torch SDPA over the masked sequence;
+    rows that see none: out 0, lse2 -inf."""
+    mask = visible_mask(L, K, W, fk) & range_mask(L, K, kb, ke)
+    seen = mask.any(axis=1)
+    if seen.any():
+        ro, rl = dense_attention(q, dk, dv, scale, np.where(seen[:, None], mask, True))
+        np.testing.assert_allclose(out[seen], ro[seen], rtol=rtol, atol=atol)
+        np.testing.assert_allclose(lse2[seen], rl[seen], rtol=rtol, atol=atol)
+    assert np.all(out[~seen] == 0.0) and np.all(np.isneginf(lse2[~seen]))
+
+
+def _part_ranges(rng, L, K):
+    """Ranges covering the interesting cases for a request of L + K keys."""
+    T = L + K
+    cuts = sorted(int(x) for x in rng.integers(0, T + 1, size=3))
+    out = [(0, T), (0, 0), (L, T), (0, L), (T, T + 5)]
+    out += [(a, b) for a, b in zip([0] + cuts, cuts + [T])]
+    return out
+
+
+@pytest.mark.parametrize("W,fk", [(0, 1), (6, 1), (0, 0), (4, 0)])
+def test_part_equals_masked_dense(oracle_mod, W, fk):
+    """A part is the attention over the visible keys inside its range."""
+    rng = np.random.default_rng(700 + W + 10 * fk)
+    Hq, Hkv, D, P, K = 4, 2, 8, 4, 3
+    lens = [0, 3, 9, 22]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    s = 0.55
+    per_req = [_part_ranges(rng, L, K) for L in lens]
+    for t in range(len(per_req[0])):
+        kb = np.array([r[t][0] for r in per_req], np.int32)
+        ke = np.array([r[t][1] for r in per_req], np.int32)
+        out, lse2 = oracle_mod.block_attn_part(q, kp, vp, tab, ctx, kb, ke, block_size=K, window=W,
+                                               future_keys=fk, scale=s)
+        for b, L in enumerate(lens):
+            _check_part_against_dense(out[b], lse2[b], q[b], dk[b], dv[b], s, L, K, W, fk, kb[b], ke[b])
+
+
+@pytest.mark.parametrize("n_parts", [1, 2, 3, 5])
+@pytest.mark.parametrize("W", [0, 7])
+def test_parts_merge_into_whole_attention(oracle_mod, n_parts, W):
+    """Parts that tile [0, L+K), merged by the base-2 LSE combine, give the
+    whole attention; the combine agrees with a plain logaddexp2 merge."""
+    rng = np.random.default_rng(800 + 11 * n_parts + W)
+    Hq, Hkv, D, P, K = 6, 2, 8, 3, 4
+    lens = [0, 1, 8, 19, 33]
+    q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+    s = 0.5
+    full, full_lse = oracle_mod.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W, future_keys=1,
+                                           scale=s)
+    bounds = []
+    for L in lens:
+        inner = sorted(int(x) for x in rng.integers(0, L + K + 1, size=n_parts - 1))
+        bounds.append([0] + inner + [L + K])
+    outs, lses = [], []
+    for r in range(n_parts):
+        kb = np.array([bd[r] for bd in bounds], np.int32)
+        ke = np.array([bd[r + 1] for bd in bounds], np.int32)
+        o, l = oracle_mod.block_attn_part(q, kp, vp, tab, ctx, kb, ke, block_size=K, window=W,
+                                          future_keys=1, scale=s)
+        outs.append(o)
+        lses.append(l)
+    mo, ml = oracle_mod.combine_parts(np.stack(outs), np.stack(lses))
+    np.testing.assert_allclose(mo, full, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(ml, full_lse, rtol=1e-12, atol=1e-12)
+    # The same merge written with numpy's logaddexp2, part by part.
+    acc_l = np.full(full_lse.shape, -np.inf)
+    for l in lses:
+        acc_l = np.logaddexp2(acc_l, l)
+    acc_o = sum(o * np.exp2(l - acc_l)[..., None] for o, l in zip(outs, lses))
+    np.testing.assert_allclose(mo, acc_o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ml, acc_l, rtol=1e-13, atol=1e-13)
+
+
+def test_combine_parts_of_nothing_is_empty(oracle_mod):
+    out, lse2 = oracle_mod.combine_parts(np.zeros((3, 2, 5, 4)), np.full((3, 2, 5), -np.inf))
+    assert np.all(out == 0.0) and np.all(np.isneginf(lse2))
+
+
+PART_MUTANTS = [
+    ("part range end inclusive", "p < pr.key_end[b]", "p <= pr.key_end[b]"),
+    ("part range begin exclusive", "p >= pr.key_begin[b]", "p > pr.key_begin[b]"),
+    ("merge weights from the max, not the sum", "std::exp2(part_lse2[s * rows + r] - lse)",
+     "std::exp2(part_lse2[s * rows + r] - m)"),
+    ("merge LSE natural log", "const double lse = m + std::log2(z);", "const double lse = m + std::log(z);"),
+]
+
+
+def _part_pins_pass(lib) -> bool:
+    import oracle
+
+    rng = np.random.default_rng(4321)
+    try:
+        Hq, Hkv, D, P, K, W = 4, 2, 8, 4, 3, 6
+        lens = [2, 9, 17]
+        q, dk, dv, kp, vp, tab, ctx = make_case(rng, len(lens), Hq, Hkv, D, K, P, lens)
+        full, full_lse = oracle.block_attn(q, kp, vp, tab, ctx, block_size=K, window=W, future_keys=1,
+                                           scale=0.5, lib=lib)
+        mid = np.array([L // 2 + 1 for L in lens], np.int32)
+        zero = np.zeros(len(lens), np.int32)
+        end = np.array([L + K for L in lens], np.int32)
+        o1, l1 = oracle.block_attn_part(q, kp, vp, tab, ctx, zero, mid, block_size=K, window=W,
+                                        future_keys=1, scale=0.5, lib=lib)
+        o2, l2 = oracle.block_attn_part(q, kp, vp, tab, ctx, mid, end, block_size=K, window=W,
+                                        future_keys=1, scale=0.5, lib=lib)
+        for b, L in enumerate(lens):
+            _check_part_against_dense(o1[b], l1[b], q[b], dk[b], dv[b], 0.5, L, K, W, 1, 0, mid[b],
+                                      rtol=1e-10, atol=1e-11)
+        mo, ml = oracle.combine_parts(np.stack([o1, o2]), np.stack([l1, l2]), lib=lib)
+        if not (np.allclose(mo, full, rtol=1e-10, atol=1e-11) and np.allclose(ml, full_lse, rtol=1e-10,
+                                                                              atol=1e-11)):
+            return False
+    except (ValueError, AssertionError):
+        return False
+    return True
+
+
+def test_part_pins_reject_planted_mistakes(oracle_mod, tmp_path):
+    import oracle
+
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "dflash_oracle.cpp")).read()
+    assert _part_pins_pass(oracle._load()), "the unmodified oracle must pass the part pins"
+    for name, old, new in PART_MUTANTS:
+        assert src.count(old) == 1, name
+        path = tmp_path / (name.replace(" ", "_").replace(",", "") + ".cpp")
+        path.write_text(src.replace(old, new))
+        so = str(path) + ".so"
+        subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-pthread", str(path), "-o", so],
+                       check=True)
+        assert not _part_pins_pass(oracle.load_library(so)), f"planted mistake not caught: {name}"
