@@ -317,6 +317,52 @@ int dflash_block_attn_fp8_context_timed(const dflash_params* p, const void* q, c
                                         void* workspace, size_t workspace_bytes, void* stream,
                                         void* split_start, void* split_done);
 
+/*
+ * Context-parallel split of one call over ranks that each hold part of every
+ * request's keys: the base-2 log-sum-exp merge of partial softmax states of
+ * PR #21130 (change 1), applied across ranks, with one all-gather of the
+ * parts' (out, lse2) between the two calls below.
+ *
+ * A part covers the logical key positions [key_begin[b], key_end[b]) of
+ * request b's L_b + K positions (context positions 0 .. L_b-1, then the block
+ * keys L_b .. L_b+K-1); each row sees the keys of its usual visible set that
+ * lie in that range.  Parts whose ranges tile [0, L_b + K) for every request
+ * merge into exactly the result of dflash_block_attn.  A rank's page table
+ * need only name pages for the positions its part reads.
+ *
+ * dflash_partial_workspace_size: workspace bytes for dflash_block_attn_partial
+ * with *p (0 when invalid; kv_dtype must be DFLASH_KV_BF16 and force_path
+ * DFLASH_PATH_AUTO or DFLASH_PATH_MMA: parts run on the mma.sync kernel).
+ */
+size_t dflash_partial_workspace_size(const dflash_params* p);
+
+/*
+ * One part.  Arguments as dflash_block_attn, plus
+ *   key_begin, key_end  int32 [B], device: the part's key range per request
+ *              (any values; an empty or disjoint range gives empty rows)
+ *   part_out   fp32 [B, K, Hq, D], device, 16-byte aligned: the output
+ *              normalised over the part's keys (0 for a row that sees none)
+ *   part_lse2  fp32 [B, K, Hq]: the base-2 LSE over the part's keys (-inf
+ *              for a row that sees none)
+ * in place of out / lse2.  Same return codes as dflash_block_attn.
+ */
+int dflash_block_attn_partial(const dflash_params* p, const void* q, const void* k_pages,
+                              const void* v_pages, const int32_t* page_table, const int32_t* ctx_lens,
+                              const int32_t* key_begin, const int32_t* key_end, float* part_out,
+                              float* part_lse2, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Merge of n_parts parts (PR #21130 change 1: lse = log2 sum_s 2^lse_s,
+ * out = sum_s 2^(lse_s - lse) out_s): part_out fp32 [n_parts, B, K, Hq, D]
+ * (16-byte aligned) and part_lse2 fp32 [n_parts, B, K, Hq], as an all-gather
+ * of the parts' outputs lays them out, into out bf16 [B, K, Hq, D] (nearest
+ * even) and lse2 fp32 [B, K, Hq].  Uses batch, num_q_heads, block_size and
+ * head_dim of *p.  No workspace; stream-ordered.  Returns DFLASH_OK,
+ * DFLASH_ERR_INVALID, DFLASH_ERR_DEVICE or DFLASH_ERR_LAUNCH.
+ */
+int dflash_combine_partials(const dflash_params* p, int n_parts, const float* part_out,
+                            const float* part_lse2, void* out, float* lse2, void* stream);
+
 /* Static text for a return code. */
 const char* dflash_status_string(int status);
 

@@ -27,6 +27,7 @@ __all__ = [
     "block_placement", "append_block_kv", "block_attn_append", "block_attn_append_raw",
     "block_attn_dense_suffix", "block_attn_dense_suffix_raw",
     "block_attn_fp8_context", "block_attn_fp8_context_raw", "block_attn_fp8_context_timed_raw",
+    "partial_workspace_size", "block_attn_partial", "combine_partials",
     "KV_BF16", "KV_FP8_E4M3",
     "PATH_MMA", "PATH_TCGEN05", "DFLASH_OK", "DFLASH_ERR_INVALID", "DFLASH_ERR_WORKSPACE",
     "DFLASH_ERR_DEVICE", "DFLASH_ERR_LAUNCH", "DFLASH_STATUS_BAD_PAGE",
@@ -155,6 +156,74 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size: int, wi
                         page_table.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
                         lse2.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                         _stream_handle(stream))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+    return out, lse2
+
+
+def partial_workspace_size(p: Params) -> int:
+    """Workspace bytes of ``block_attn_partial`` for ``p`` (0: invalid)."""
+    return int(_lib.load().dflash_partial_workspace_size(ctypes.byref(p)))
+
+
+def block_attn_partial(q, k_pages, v_pages, page_table, ctx_lens, key_begin, key_end, *, block_size: int,
+                       window: int, future_keys: int, scale: float, max_ctx_len: int, right_window: int = 0,
+                       part_out=None, part_lse2=None, workspace=None, stream=None, force_split_tiles: int = 0):
+    """One context-parallel part: the attention over the keys at logical
+    positions ``[key_begin[b], key_end[b])`` (int32 ``[B]`` device tensors) of
+    each request's ``L + K`` positions.  Returns ``(part_out, part_lse2)``,
+    fp32 ``[B,K,Hq,D]`` and ``[B,K,Hq]``; other arguments as ``block_attn``."""
+    import torch
+
+    p = params_for(q, k_pages, page_table, block_size=block_size, window=window,
+                   future_keys=future_keys, scale=scale, max_ctx_len=max_ctx_len,
+                   force_split_tiles=force_split_tiles, right_window=right_window)
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_pages", k_pages, torch.bfloat16),
+                        ("v_pages", v_pages, torch.bfloat16), ("page_table", page_table, torch.int32),
+                        ("ctx_lens", ctx_lens, torch.int32), ("key_begin", key_begin, torch.int32),
+                        ("key_end", key_end, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if part_out is None:
+        part_out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if part_lse2 is None:
+        part_lse2 = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    need = partial_workspace_size(p)
+    if need == 0:
+        raise DflashError(DFLASH_ERR_INVALID)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    rc = _lib.load().dflash_block_attn_partial(
+        ctypes.byref(p), q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), page_table.data_ptr(),
+        ctx_lens.data_ptr(), key_begin.data_ptr(), key_end.data_ptr(), part_out.data_ptr(),
+        part_lse2.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    if rc != DFLASH_OK:
+        raise DflashError(rc)
+    return part_out, part_lse2
+
+
+def combine_partials(part_out, part_lse2, *, out=None, lse2=None, stream=None):
+    """Merge of ``n`` parts: ``part_out [n,B,K,Hq,D]`` and ``part_lse2
+    [n,B,K,Hq]`` (fp32, contiguous, CUDA) -> ``(out bf16 [B,K,Hq,D], lse2 fp32
+    [B,K,Hq])``."""
+    import torch
+
+    if part_out.dtype != torch.float32 or part_lse2.dtype != torch.float32 or not part_out.is_cuda:
+        raise ValueError("part_out / part_lse2 must be fp32 CUDA tensors")
+    if part_out.dim() != 5 or part_lse2.shape != part_out.shape[:4]:
+        raise ValueError("part_out [n,B,K,Hq,D] and part_lse2 [n,B,K,Hq] expected")
+    part_out = part_out.contiguous()
+    part_lse2 = part_lse2.contiguous()
+    n, B, K, Hq, D = part_out.shape
+    p = make_params(batch=B, num_q_heads=Hq, num_kv_heads=1, head_dim=D, page_size=16, max_pages_per_req=K,
+                    num_pages=1, block_size=K, window=0, future_keys=1, scale=1.0, max_ctx_len=0)
+    if out is None:
+        out = torch.empty((B, K, Hq, D), dtype=torch.bfloat16, device=part_out.device)
+    if lse2 is None:
+        lse2 = torch.empty((B, K, Hq), dtype=torch.float32, device=part_out.device)
+    rc = _lib.load().dflash_combine_partials(ctypes.byref(p), int(n), part_out.data_ptr(), part_lse2.data_ptr(),
+                                             out.data_ptr(), lse2.data_ptr(), _stream_handle(stream))
     if rc != DFLASH_OK:
         raise DflashError(rc)
     return out, lse2

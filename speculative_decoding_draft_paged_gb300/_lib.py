@@ -59,6 +59,9 @@ EXPORTS = (
     "dflash_block_attn_dense_suffix",
     "dflash_block_attn_fp8_context",
     "dflash_block_attn_fp8_context_timed",
+    "dflash_partial_workspace_size",
+    "dflash_block_attn_partial",
+    "dflash_combine_partials",
     "dflash_status_string",
     "dflash_read_device_status",
     "dflash_clear_device_status",
@@ -152,6 +155,13 @@ def load() -> ctypes.CDLL:
             lib.dflash_block_attn_fp8_context_timed.argtypes = \
                 lib.dflash_block_attn_fp8_context.argtypes + [vp, vp]
             lib.dflash_block_attn_fp8_context_timed.restype = i32
+            lib.dflash_partial_workspace_size.argtypes = [ctypes.POINTER(Params)]
+            lib.dflash_partial_workspace_size.restype = ctypes.c_size_t
+            lib.dflash_block_attn_partial.argtypes = [ctypes.POINTER(Params)] + [vp] * 10 + \
+                [ctypes.c_size_t, vp]
+            lib.dflash_block_attn_partial.restype = i32
+            lib.dflash_combine_partials.argtypes = [ctypes.POINTER(Params), i32] + [vp] * 5
+            lib.dflash_combine_partials.restype = i32
             lib.dflash_status_string.argtypes = [i32]
             lib.dflash_status_string.restype = ctypes.c_char_p
             lib.dflash_read_device_status.argtypes = [vp, vp]

@@ -384,11 +384,40 @@ struct Fp8Scales {
   float k_scale, v_scale;
 };
 
-int run_attention(const dflash_params* p, const void* q, const void* k_pages, const void* v_pages,
+// A context-parallel part: the key range per request and the fp32 output.
+struct PartArgs {
+  const int32_t* key_begin;
+  const int32_t* key_end;
+  float* out_f32;
+};
+
+// The parameters a context-parallel part runs with: the mma.sync unit grid,
+// whose empty units and combine handle a pair that has no key in the part.
+bool part_params(const dflash_params* p, dflash_params* pp) {
+  if (!params_valid(p) || p->kv_dtype != DFLASH_KV_BF16) return false;
+  if (p->force_path != DFLASH_PATH_AUTO && p->force_path != DFLASH_PATH_MMA) return false;
+  *pp = *p;
+  pp->force_path = DFLASH_PATH_MMA;
+  return true;
+}
+
+int run_attention(const dflash_params* p_in, const void* q, const void* k_pages, const void* v_pages,
                   const int32_t* page_table, const int32_t* ctx_lens, void* out, float* lse2,
                   void* workspace, size_t workspace_bytes, void* stream, void* split_start,
                   void* split_done, const AppendArgs* append, const void* dense_k = nullptr,
-                  const void* dense_v = nullptr, const Fp8Scales* fp8 = nullptr) {
+                  const void* dense_v = nullptr, const Fp8Scales* fp8 = nullptr,
+                  const PartArgs* part = nullptr) {
+  dflash_params pp;
+  const dflash_params* p = p_in;
+  if (part != nullptr) {
+    if (!part_params(p_in, &pp) || append != nullptr || dense_k != nullptr || fp8 != nullptr)
+      return DFLASH_ERR_INVALID;
+    if (!part->key_begin || !part->key_end || !part->out_f32 || !aligned(part->key_begin, 4) ||
+        !aligned(part->key_end, 4) || !aligned(part->out_f32, 16))
+      return DFLASH_ERR_INVALID;
+    p = &pp;
+    out = part->out_f32;  // checked for presence below; the bf16 output is not written
+  }
   if (!params_valid(p)) return DFLASH_ERR_INVALID;
   if ((fp8 != nullptr) != (p->kv_dtype == DFLASH_KV_FP8_E4M3)) return DFLASH_ERR_INVALID;
   if (fp8 != nullptr) {
@@ -467,6 +496,13 @@ int run_attention(const dflash_params* p, const void* q, const void* k_pages, co
   a.kblk_mul = 1.f;
   a.pblk_mul = 1.f;
   a.out_mul = 1.f;
+  if (part != nullptr) {
+    a.out = nullptr;
+    a.key_begin = part->key_begin;
+    a.key_end = part->key_end;
+    a.keep_partials = 1;
+    a.out_f32 = part->out_f32;
+  }
   if (fp8 != nullptr) {
     a.scale_log2 *= fp8->k_scale;
     a.kblk_mul = 1.f / fp8->k_scale;
@@ -488,7 +524,7 @@ int run_attention(const dflash_params* p, const void* q, const void* k_pages, co
   // With one unit per (request, kv head) the mma.sync kernel wrote the final
   // output itself; otherwise merge the partial states (the flat split of the
   // tcgen05 kernel always may cut a pair).
-  if (tc || k.S > 1) {
+  if (tc || k.S > 1 || part != nullptr) {
     err = launch_combine(a, s, split_done == nullptr, tc);
     if (err != cudaSuccess) return DFLASH_ERR_LAUNCH;
   }
@@ -616,6 +652,45 @@ int dflash_block_attn_append(const dflash_params* p, const void* q, const void* 
       append_args(p, k_block, v_block, k_pages, v_pages, page_table, ctx_lens, workspace);
   return run_attention(p, q, k_pages, v_pages, page_table, ctx_lens, out, lse2, workspace,
                        workspace_bytes, stream, nullptr, nullptr, &ap);
+}
+
+size_t dflash_partial_workspace_size(const dflash_params* p) {
+  dflash_params pp;
+  if (!part_params(p, &pp)) return 0;
+  return dflash_workspace_size(&pp);
+}
+
+int dflash_block_attn_partial(const dflash_params* p, const void* q, const void* k_pages,
+                              const void* v_pages, const int32_t* page_table, const int32_t* ctx_lens,
+                              const int32_t* key_begin, const int32_t* key_end, float* part_out,
+                              float* part_lse2, void* workspace, size_t workspace_bytes, void* stream) {
+  const PartArgs part{key_begin, key_end, part_out};
+  return run_attention(p, q, k_pages, v_pages, page_table, ctx_lens, nullptr, part_lse2, workspace,
+                       workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, &part);
+}
+
+int dflash_combine_partials(const dflash_params* p, int n_parts, const float* part_out,
+                            const float* part_lse2, void* out, float* lse2, void* stream) {
+  if (!params_valid(p) || n_parts < 1 || !part_out || !part_lse2 || !out || !lse2) return DFLASH_ERR_INVALID;
+  if (!aligned(part_out, 16) || !aligned(part_lse2, 4) || !aligned(out, 16) || !aligned(lse2, 4))
+    return DFLASH_ERR_INVALID;
+  const int64_t rows = static_cast<int64_t>(p->batch) * p->block_size * p->num_q_heads;
+  if (rows > 0x7fffffff) return DFLASH_ERR_INVALID;
+  const int rc = check_device();
+  if (rc != DFLASH_OK) return rc;
+  AttnArgs a{};
+  a.part_o = const_cast<float*>(part_out);
+  a.part_lse = const_cast<float*>(part_lse2);
+  a.part_lseo = const_cast<float*>(part_lse2);  // outputs weighted by the parts' LSEs
+  a.out = static_cast<uint16_t*>(out);
+  a.lse2 = lse2;
+  a.B = p->batch;
+  a.K = p->block_size;
+  a.Hq = p->num_q_heads;
+  a.D = p->head_dim;
+  a.R = static_cast<int>(rows);
+  return launch_combine_parts(a, n_parts, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DFLASH_OK
+                                                                                          : DFLASH_ERR_LAUNCH;
 }
 
 const char* dflash_status_string(int status) {

@@ -131,6 +131,16 @@ __device__ __forceinline__ void write_row(const AttnArgs& a, long long row_id, i
                                           const float (&acc)[D / 32], float M, float den, float deno) {
   constexpr int V = D / 32;
   const float inv = deno > 0.f ? 1.f / deno : 0.f;
+  if (a.out_f32 != nullptr) {
+    // A context-parallel part: its output in fp32, for the exchange.
+    float* dst = a.out_f32 + static_cast<size_t>(row_id) * D + lane * V;
+    if constexpr (V == 2)
+      *reinterpret_cast<float2*>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
+    else
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    if (lane == 0) a.lse2[row_id] = den > 0.f ? M + log2f(den) : neg_inf_f();
+    return;
+  }
   uint16_t* dst = a.out + static_cast<size_t>(row_id) * D + lane * V;
   if constexpr (V == 2) {
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
@@ -163,8 +173,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const AttnArgs a) {
   if (active) row_coords(a, row_id, b, i, hq);
   const int h = hq / a.G;
   const int r = i * a.G + (hq - h * a.G);
-  const Geometry geo = make_geometry(active ? __ldg(&a.ctx_lens[b]) : 0, a.max_ctx_len, a.K, a.W,
-                                     a.T, a.C);
+  Geometry geo = make_geometry(active ? __ldg(&a.ctx_lens[b]) : 0, a.max_ctx_len, a.K, a.W, a.T, a.C);
+  if (active && a.key_begin != nullptr)
+    narrow_geometry(geo, __ldg(&a.key_begin[b]), __ldg(&a.key_end[b]), a.T, a.C);
   const int ns = geo.n_splits;
   const size_t unit0 = (static_cast<size_t>(b) * a.Hkv + h) * a.S;
 
@@ -209,6 +220,23 @@ __global__ void __launch_bounds__(kThreads, 6) combine_flat_kernel(const AttnArg
   write_row<D>(a, row_id, lane, acc, M, den, deno);
 }
 
+// Merge of exchanged context-parallel parts (the base-2 log-sum-exp combine
+// of PR #21130 change 1, across the parts of one call): one warp per output
+// row; part s of row r sits at s * rows + r.  The parts' outputs are weighted
+// by their LSEs.
+template <int D>
+__global__ void __launch_bounds__(kThreads) combine_parts_kernel(const AttnArgs a, int n_parts) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long row_id = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
+  const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
+  if (row_id >= rows) return;
+  float acc[D / 32], M, den, deno;
+  combine_row<D>(a, static_cast<int>(row_id), n_parts, [](int sp) -> size_t { return static_cast<size_t>(sp); },
+                 lane, acc, M, den, deno);
+  write_row<D>(a, row_id, lane, acc, M, den, deno);
+}
+
 template <int D>
 int launch_t(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat) {
   const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
@@ -233,6 +261,15 @@ int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat) 
   if (a.D == 64) return launch_t<64>(a, stream, pdl, flat);
   if (a.D == 128) return launch_t<128>(a, stream, pdl, flat);
   return cudaErrorInvalidValue;
+}
+
+int launch_combine_parts(const AttnArgs& a, int n_parts, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
+  const unsigned grid = static_cast<unsigned>((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  if (a.D == 64) combine_parts_kernel<64><<<grid, kThreads, 0, stream>>>(a, n_parts);
+  else if (a.D == 128) combine_parts_kernel<128><<<grid, kThreads, 0, stream>>>(a, n_parts);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 }  // namespace dflash

@@ -76,6 +76,16 @@ struct AttnArgs {
   // otherwise.
   int fp8;
   float kblk_mul, pblk_mul, out_mul;
+  // Context-parallel part (mma.sync unit grid): only the keys at logical
+  // positions [key_begin[b], key_end[b]) of each request's L + K positions,
+  // or null for all of them.  keep_partials: every unit writes its partial
+  // state (no direct output) and the combine writes the part's fp32 output
+  // out_f32 ([B, K, Hq, D], normalised over the part's keys) and its LSE
+  // to lse2, instead of bf16 out.
+  const int32_t* key_begin;
+  const int32_t* key_end;
+  int keep_partials;
+  float* out_f32;
 };
 
 // Per-(request, kv head) key-range geometry of the split kernel, which covers
@@ -106,6 +116,19 @@ DF_HD Geometry make_geometry(int L_raw, int max_ctx_len, int K, int W, int T, in
   g.n_tiles = t_end - g.t_begin;
   g.n_splits = (g.n_tiles + C - 1) / C;
   return g;
+}
+
+// A context-parallel part sees only the keys at logical positions [kb, ke):
+// the union interval narrows to its intersection with them, and a part that
+// meets it nowhere has no tiles.
+DF_HD void narrow_geometry(Geometry& g, int kb, int ke, int T, int C) {
+  const int lo = g.lo_min > kb ? g.lo_min : kb;
+  const int hi = g.hi_max < ke ? g.hi_max : ke;
+  g.lo_min = lo;
+  g.hi_max = hi > lo ? hi : lo;
+  g.t_begin = lo / T;
+  g.n_tiles = hi > lo ? (hi + T - 1) / T - g.t_begin : 0;
+  g.n_splits = (g.n_tiles + C - 1) / C;
 }
 
 // Upper bound of Geometry::n_tiles over every L in [0, max_ctx_len].
@@ -168,6 +191,9 @@ int launch_split_tc(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap
                     const CUtensorMap& tm_v, const CUtensorMap& tm_q, const CUtensorMap& tm_out,
                     const CUtensorMap& tm_part, cudaStream_t stream);
 int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat);
+// Merge of n_parts context-parallel parts: a.part_o / a.part_lse hold part s
+// of row r at s * rows + r (rows = B*K*Hq); writes bf16 out and lse2.
+int launch_combine_parts(const AttnArgs& a, int n_parts, cudaStream_t stream);
 
 // Shared-memory bytes of each split kernel for a plan (used by the planner).
 int split_mma_smem_bytes(int D, int R_pad, int kpw, bool fp8);

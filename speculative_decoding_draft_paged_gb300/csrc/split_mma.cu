@@ -182,7 +182,14 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
   const int b = blockIdx.z;
 
   const int L_raw = __ldg(&a.ctx_lens[b]);
-  const Geometry geo = make_geometry(L_raw, a.max_ctx_len, a.K, a.W, T, a.C);
+  Geometry geo = make_geometry(L_raw, a.max_ctx_len, a.K, a.W, T, a.C);
+  // Context-parallel part: the keys [part_lo, part_hi) only.
+  int part_lo = 0, part_hi = 0x7fffffff;
+  if (a.key_begin != nullptr) {
+    part_lo = __ldg(&a.key_begin[b]);
+    part_hi = __ldg(&a.key_end[b]);
+    narrow_geometry(geo, part_lo, part_hi, T, a.C);
+  }
   if (threadIdx.x == 0 && s == 0 && h == 0 && (L_raw < 0 || L_raw > a.max_ctx_len))
     flag_status(a.status, DFLASH_STATUS_BAD_CTX_LEN);
   if (s >= geo.n_splits) return;  // empty split unit (uniform over the CTA)
@@ -368,8 +375,8 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
           lo = L + i - a.W + 1;
           if (lo < 0) lo = 0;
         }
-        lo_r[e] = lo;
-        hi_r[e] = L + min(a.K, i + 1 + a.rw);
+        lo_r[e] = max(lo, part_lo);
+        hi_r[e] = min(L + min(a.K, i + 1 + a.rw), part_hi);
       } else {
         lo_r[e] = 0x7fffffff;
         hi_r[e] = -0x7fffffff;
@@ -380,7 +387,8 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
       lo_rows_max = L + a.K - a.W;
       if (lo_rows_max < 0) lo_rows_max = 0;
     }
-    const int hi_rows_min = L + min(a.K, 1 + a.rw);  // smallest row upper bound (row 0)
+    lo_rows_max = max(lo_rows_max, part_lo);
+    const int hi_rows_min = min(L + min(a.K, 1 + a.rw), part_hi);  // smallest row upper bound (row 0)
 
     float m_run[2] = {neg_inf(), neg_inf()};
     float l_run[2] = {0.f, 0.f};
@@ -549,7 +557,9 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
     float* part_o = a.part_o + unit * a.R * D;
     float* part_lse = a.part_lse + unit * a.R;
     float* part_lseo = a.part_lseo + unit * a.R;
-    const bool direct = a.S == 1;  // one unit per (request, kv head): final output
+    // One unit per (request, kv head): the final output, unless every unit
+    // keeps its partial state (a context-parallel part).
+    const bool direct = a.S == 1 && !a.keep_partials;
     (void)aborted;
 
     if constexpr (NWK == 1) {
