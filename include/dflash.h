@@ -71,6 +71,13 @@ extern "C" {
 #define DFLASH_KV_FP8_E4M3           1  /* E4M3 codes with per-tensor scales:
                                            dflash_block_attn_fp8_context only */
 
+/* dflash_params.test_flags (tests only; 0 in use). */
+#define DFLASH_TEST_WITHHOLD_LOADS   1  /* the split kernels' producers issue no K/V loads, so every
+                                           pipeline wait runs out (after its 4 s bound): the call
+                                           finishes with DFLASH_STATUS_TIMEOUT set and nothing in
+                                           flight; its outputs are not meaningful.  Exercises the
+                                           bounded-wait failure path without a fault or a hang. */
+
 /* Kernel-path selection for dflash_params.force_path. */
 #define DFLASH_PATH_AUTO             0
 #define DFLASH_PATH_MMA              1  /* warp-level mma.sync tiles (any R <= 128) */
@@ -101,7 +108,8 @@ typedef struct dflash_params {
   int32_t right_window;      /* with future_keys = 0: row i also sees block keys
                                 i+1 .. i+right_window (0 .. K-1); 0 when future_keys = 1 */
   int32_t kv_dtype;          /* DFLASH_KV_BF16 or DFLASH_KV_FP8_E4M3 (pool element type) */
-  int32_t reserved[2];       /* must be zero */
+  int32_t test_flags;        /* 0, or DFLASH_TEST_WITHHOLD_LOADS (tests of the failure path) */
+  int32_t reserved[1];       /* must be zero */
 } dflash_params;
 
 /*

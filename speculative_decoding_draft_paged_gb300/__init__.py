@@ -18,7 +18,7 @@ from typing import Optional
 from . import _lib
 from ._lib import (DFLASH_ERR_DEVICE, DFLASH_ERR_INVALID, DFLASH_ERR_LAUNCH, DFLASH_ERR_WORKSPACE,
                    DFLASH_OK, DFLASH_STATUS_BAD_CTX_LEN, DFLASH_STATUS_BAD_PAGE,
-                   DFLASH_STATUS_TIMEOUT, DFLASH_STATUS_FP8_RANGE, KV_BF16, KV_FP8_E4M3, PATH_AUTO, PATH_MMA, PATH_TCGEN05,
+                   DFLASH_STATUS_TIMEOUT, DFLASH_STATUS_FP8_RANGE, DFLASH_TEST_WITHHOLD_LOADS, KV_BF16, KV_FP8_E4M3, PATH_AUTO, PATH_MMA, PATH_TCGEN05,
                    Params, PlanInfo)
 
 __all__ = [
@@ -32,6 +32,7 @@ __all__ = [
     "PATH_MMA", "PATH_TCGEN05", "DFLASH_OK", "DFLASH_ERR_INVALID", "DFLASH_ERR_WORKSPACE",
     "DFLASH_ERR_DEVICE", "DFLASH_ERR_LAUNCH", "DFLASH_STATUS_BAD_PAGE",
     "DFLASH_STATUS_BAD_CTX_LEN", "DFLASH_STATUS_TIMEOUT", "DFLASH_STATUS_FP8_RANGE",
+    "DFLASH_TEST_WITHHOLD_LOADS",
 ]
 
 
@@ -43,7 +44,7 @@ class DflashError(RuntimeError):
 
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_req,
                 num_pages, block_size, window, future_keys, scale, max_ctx_len, force_path=0,
-                force_split_tiles=0, right_window=0, kv_dtype=0) -> Params:
+                force_split_tiles=0, right_window=0, kv_dtype=0, test_flags=0) -> Params:
     p = Params()
     p.batch = batch
     p.num_q_heads = num_q_heads
@@ -61,11 +62,12 @@ def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pa
     p.force_split_tiles = force_split_tiles
     p.right_window = right_window
     p.kv_dtype = kv_dtype
+    p.test_flags = test_flags
     return p
 
 
 def params_for(q, k_pages, page_table, *, block_size, window, future_keys, scale, max_ctx_len,
-               force_path=0, force_split_tiles=0, right_window=0, kv_dtype=0) -> Params:
+               force_path=0, force_split_tiles=0, right_window=0, kv_dtype=0, test_flags=0) -> Params:
     B, K, Hq, D = q.shape
     num_pages, Hkv, P, _ = k_pages.shape
     if K != block_size:
@@ -75,7 +77,7 @@ def params_for(q, k_pages, page_table, *, block_size, window, future_keys, scale
                        block_size=block_size, window=window, future_keys=future_keys, scale=scale,
                        max_ctx_len=max_ctx_len, force_path=force_path,
                        force_split_tiles=force_split_tiles, right_window=right_window,
-                       kv_dtype=kv_dtype)
+                       kv_dtype=kv_dtype, test_flags=test_flags)
 
 
 def workspace_size(p: Params) -> int:
@@ -121,7 +123,7 @@ def block_attn_timed_raw(p: Params, q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, ou
 def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size: int, window: int,
                future_keys: int, scale: float, max_ctx_len: int, out=None, lse2=None,
                workspace=None, stream=None, force_path: int = 0, force_split_tiles: int = 0,
-               right_window: int = 0):
+               right_window: int = 0, test_flags: int = 0):
     """Draft-block attention over a paged bf16 KV cache.  Returns ``(out, lse2)``.
 
     ``q [B,K,Hq,D]`` bf16, ``k_pages``/``v_pages [num_pages,Hkv,P,D]`` bf16,
@@ -135,7 +137,7 @@ def block_attn(q, k_pages, v_pages, page_table, ctx_lens, *, block_size: int, wi
     p = params_for(q, k_pages, page_table, block_size=block_size, window=window,
                    future_keys=future_keys, scale=scale, max_ctx_len=max_ctx_len,
                    force_path=force_path, force_split_tiles=force_split_tiles,
-                   right_window=right_window)
+                   right_window=right_window, test_flags=test_flags)
     for name, t, dt in (("q", q, torch.bfloat16), ("k_pages", k_pages, torch.bfloat16),
                         ("v_pages", v_pages, torch.bfloat16), ("page_table", page_table, torch.int32),
                         ("ctx_lens", ctx_lens, torch.int32)):

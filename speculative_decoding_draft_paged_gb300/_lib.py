@@ -24,6 +24,8 @@ DFLASH_STATUS_BAD_CTX_LEN = 2
 DFLASH_STATUS_TIMEOUT = 4
 DFLASH_STATUS_FP8_RANGE = 8
 
+DFLASH_TEST_WITHHOLD_LOADS = 1
+
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 
@@ -87,7 +89,8 @@ class Params(ctypes.Structure):
         ("force_split_tiles", ctypes.c_int32),
         ("right_window", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("test_flags", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
 

@@ -95,6 +95,7 @@ bool params_valid(const dflash_params* p) {
   if (p->force_path < DFLASH_PATH_AUTO || p->force_path > DFLASH_PATH_TCGEN05) return false;
   if (p->force_split_tiles < 0 || p->force_split_tiles > kMaxSplitTiles) return false;
   if (p->kv_dtype != DFLASH_KV_BF16 && p->kv_dtype != DFLASH_KV_FP8_E4M3) return false;
+  if (p->test_flags != 0 && p->test_flags != DFLASH_TEST_WITHHOLD_LOADS) return false;
   return true;
 }
 
@@ -493,6 +494,7 @@ int run_attention(const dflash_params* p_in, const void* q, const void* k_pages,
   a.qn_min = kTcMinTiles;
   a.seg_cost = tc ? k.seg_cost : 0;
   a.fp8 = fp8 != nullptr ? 1 : 0;
+  a.withhold_loads = p->test_flags == DFLASH_TEST_WITHHOLD_LOADS ? 1 : 0;
   a.kblk_mul = 1.f;
   a.pblk_mul = 1.f;
   a.out_mul = 1.f;

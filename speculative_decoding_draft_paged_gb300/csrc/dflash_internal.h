@@ -86,6 +86,9 @@ struct AttnArgs {
   const int32_t* key_end;
   int keep_partials;
   float* out_f32;
+  // Tests of the failure path: the producers issue no K/V loads, so every
+  // pipeline wait runs out and the kernels wind down with nothing in flight.
+  int withhold_loads;
 };
 
 // Per-(request, kv head) key-range geometry of the split kernel, which covers

@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
       pdl_wait_primary();
       // K/V rows are read once: evict them first.
       const uint64_t kv_policy = l2_policy_evict_first();
-      for (int it = 0; it < ntiles; ++it) {
+      const int n_issue = a.withhold_loads ? 0 : ntiles;  // tests of the failure path
+      for (int it = 0; it < n_issue; ++it) {
         const int st = it % NS;
         if (it >= NS) {
           if (!mbar_wait(empty_bar(st), ((it / NS) - 1) & 1)) {

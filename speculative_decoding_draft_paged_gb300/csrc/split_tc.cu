@@ -548,7 +548,8 @@ __global__ void __launch_bounds__(384, 1)
     // K/V rows are read once: evict them first, so that the partial states
     // (read back by the combine kernel), queries and page table stay in L2.
     const uint64_t kv_policy = l2_policy_evict_first();
-    for (int j = 0; j < n; ++j) {
+    const int n_issue = a.withhold_loads ? 0 : n;  // tests of the failure path
+    for (int j = 0; j < n_issue; ++j) {
       while (j >= sg.j1) seg_next(sg, PB, a.Hkv, start, end);
       const int k = j / tpc;
       if (k != cur_k) {

@@ -314,3 +314,34 @@ def test_mma_unit_grid_large_batch(cuda_device):
     pl = dflash.plan(p)
     assert pl["path"] == dflash.PATH_MMA and pl["flat"] == 0
     check_case(spec, cuda_device)
+
+
+@pytest.mark.parametrize("path", [dflash.PATH_MMA, dflash.PATH_TCGEN05])
+def test_bounded_wait_runs_out_and_device_recovers(cuda_device, path):
+    """The failure path: with the producers withholding every K/V load
+    (DFLASH_TEST_WITHHOLD_LOADS) each pipeline wait runs out after its bound,
+    the call finishes with DFLASH_STATUS_TIMEOUT set and nothing in flight,
+    and the next normal call on the same device is parity-green."""
+    import time
+
+    spec = W.minimax(B=2, K=7, ctx_lens=[3000, 700])
+    inp = {k: v.to(cuda_device) for k, v in W.make_inputs(spec, "cpu").items()}
+    p = dflash.params_for(inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K, window=spec.window,
+                          future_keys=spec.future_keys, scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len,
+                          force_path=path)
+    ws = torch.zeros(dflash.workspace_size(p), dtype=torch.uint8, device=cuda_device)
+    t0 = time.perf_counter()
+    run_lib(spec, inp, force_path=path, workspace=ws, test_flags=dflash.DFLASH_TEST_WITHHOLD_LOADS)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    st = dflash.read_device_status(ws)
+    assert st & dflash.DFLASH_STATUS_TIMEOUT, st
+    assert waited < 60.0
+    # The context is usable and the same workspace serves a correct call.
+    dflash.clear_device_status(ws)
+    out, lse = run_lib(spec, inp, force_path=path, workspace=ws)
+    torch.cuda.synchronize()
+    assert dflash.read_device_status(ws) == 0
+    host = {k: v.cpu() for k, v in inp.items()}
+    ro, rl = run_oracle(spec, host)
+    assert_parity(metrics(out, lse, ro, rl), f"after the timeout, path {path}")
