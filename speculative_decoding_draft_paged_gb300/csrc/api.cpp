@@ -203,8 +203,10 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
       const double units = pairs * S;
       const double waves = std::ceil(units / slots);
       // The combine walks a row's S partials eight at a time, each round
-      // about one memory latency (~ one tile time); only when S > 1.
-      const double combine = S > 1 ? std::ceil(S / 8.0) : 0.0;
+      // about one memory latency (~ one tile time); only when S > 1.  Its
+      // block-per-row form takes two rounds whatever S.
+      const long long rows = static_cast<long long>(p->batch) * p->block_size * p->num_q_heads;
+      const double combine = S > 1 ? (combine_wide(S, rows) ? 2.0 : std::ceil(S / 8.0)) : 0.0;
       const double cost = waves * (c + 2.0) + units * partial_tiles / slots + combine;
       if (cost <= best * (1.0 + 1e-12)) {
         best = cost;

@@ -220,6 +220,105 @@ __global__ void __launch_bounds__(kThreads, 6) combine_flat_kernel(const AttnArg
   write_row<D>(a, row_id, lane, acc, M, den, deno);
 }
 
+// The same merge for few rows with many partials (mma.sync unit grid, small
+// batches): one block of eight warps per output row, warp w taking the
+// partials w, w+8, w+16, ... with all of its row loads in flight together,
+// then a shared-memory merge of the eight warps' states -- two dependent
+// rounds of loads instead of one per four partials.  ns <= kWideMaxPartials.
+constexpr int kWideMaxPartials = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) combine_wide_kernel(const AttnArgs a) {
+  constexpr int V = D / 32;
+  __shared__ float s_m[kWarpsPerBlock], s_den[kWarpsPerBlock], s_deno[kWarpsPerBlock];
+  __shared__ float s_acc[kWarpsPerBlock][D];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long row_id = blockIdx.x;
+  int b, i, hq;
+  row_coords(a, row_id, b, i, hq);
+  const int h = hq / a.G;
+  const int r = i * a.G + (hq - h * a.G);
+  Geometry geo = make_geometry(__ldg(&a.ctx_lens[b]), a.max_ctx_len, a.K, a.W, a.T, a.C);
+  if (a.key_begin != nullptr)
+    narrow_geometry(geo, __ldg(&a.key_begin[b]), __ldg(&a.key_end[b]), a.T, a.C);
+  const int ns = min(geo.n_splits, kWideMaxPartials);
+  const size_t unit0 = (static_cast<size_t>(b) * a.Hkv + h) * a.S;
+
+  pdl_wait_primary();
+  // This warp's partials sp = warp + 8k, k < nk <= 32: lane k holds the LSEs.
+  const int nk = ns > warp ? (ns - warp + 7) / 8 : 0;
+  const size_t u = lane < nk ? (unit0 + warp + 8 * lane) * a.R + r : 0;
+  const float ls = lane < nk ? a.part_lse[u] : neg_inf_f();
+  const float lo = lane < nk ? a.part_lseo[u] : neg_inf_f();
+  float M = ls;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+  const float w = (ls == neg_inf_f() || M == neg_inf_f()) ? 0.f : exp2f(ls - M);
+  const float wo = (lo == neg_inf_f() || M == neg_inf_f()) ? 0.f : exp2f(lo - M);
+  float den = w, deno = wo;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    den += __shfl_xor_sync(0xffffffffu, den, m);
+    deno += __shfl_xor_sync(0xffffffffu, deno, m);
+  }
+  float acc[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+  for (int k0 = 0; k0 < nk; k0 += 8) {
+    float ov[8][V];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int k = k0 + t < nk ? k0 + t : nk - 1;
+      const float* po = a.part_o + ((unit0 + warp + 8 * k) * a.R + r) * D + lane * V;
+      if constexpr (V == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(po);
+        ov[t][0] = v.x;
+        ov[t][1] = v.y;
+      } else {
+        const float4 v = *reinterpret_cast<const float4*>(po);
+        ov[t][0] = v.x;
+        ov[t][1] = v.y;
+        ov[t][2] = v.z;
+        ov[t][3] = v.w;
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const float wt = __shfl_sync(0xffffffffu, wo, (k0 + t) & 31);
+      const float wv = k0 + t < nk ? wt : 0.f;
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = fmaf(wv, ov[t][e], acc[e]);
+    }
+  }
+  if (lane == 0) {
+    s_m[warp] = M;
+    s_den[warp] = den;
+    s_deno[warp] = deno;
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) s_acc[warp][lane * V + e] = acc[e];
+  __syncthreads();
+  if (warp != 0) return;
+  float Mb = neg_inf_f();
+#pragma unroll
+  for (int ww = 0; ww < kWarpsPerBlock; ++ww) Mb = fmaxf(Mb, s_m[ww]);
+  float denb = 0.f, denob = 0.f, accb[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) accb[e] = 0.f;
+  if (Mb != neg_inf_f()) {
+#pragma unroll
+    for (int ww = 0; ww < kWarpsPerBlock; ++ww) {
+      const float f = s_m[ww] == neg_inf_f() ? 0.f : exp2f(s_m[ww] - Mb);
+      denb += f * s_den[ww];
+      denob += f * s_deno[ww];
+#pragma unroll
+      for (int e = 0; e < V; ++e) accb[e] = fmaf(f, s_acc[ww][lane * V + e], accb[e]);
+    }
+  }
+  write_row<D>(a, row_id, lane, accb, Mb, denb, denob);
+}
+
 // Merge of exchanged context-parallel parts (the base-2 log-sum-exp combine
 // of PR #21130 change 1, across the parts of one call): one warp per output
 // row; part s of row r sits at s * rows + r.  The parts' outputs are weighted
@@ -240,7 +339,9 @@ __global__ void __launch_bounds__(kThreads) combine_parts_kernel(const AttnArgs 
 template <int D>
 int launch_t(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat) {
   const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
-  const unsigned grid = static_cast<unsigned>((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  const bool wide = !flat && combine_wide(a.S, rows);
+  const unsigned grid = wide ? static_cast<unsigned>(rows)
+                             : static_cast<unsigned>((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -252,6 +353,7 @@ int launch_t(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (flat) return cudaLaunchKernelEx(&cfg, combine_flat_kernel<D>, a);
+  if (wide) return cudaLaunchKernelEx(&cfg, combine_wide_kernel<D>, a);
   return cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
 }
 

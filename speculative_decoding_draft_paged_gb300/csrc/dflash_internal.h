@@ -169,6 +169,13 @@ struct AppendArgs {
   int B, K, Hkv, D, P, max_pages, num_pages, max_ctx_len;
 };
 
+// mma.sync unit grid: the combine runs one block per output row (its
+// partials spread over eight warps) when rows are few and partials many, one
+// warp per row otherwise.
+DF_HD bool combine_wide(int max_splits, long long rows) {
+  return max_splits > 8 && max_splits <= 256 && rows <= 1024;
+}
+
 // Kernel launch with an optional programmatic-dependent-launch attribute.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

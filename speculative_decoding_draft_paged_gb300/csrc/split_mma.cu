@@ -616,35 +616,52 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
       }
       named_barrier(1, n_ct);
       const int ct = threadIdx.x - 32;
-      for (int e = ct; e < a.R * D; e += n_ct) {
-        const int r = e / D;
-        const int d = e - r * D;
+      // One item = 8 consecutive columns of one row: the row's merge weights
+      // (one base-2 exponential per key-slice warp) are computed once per
+      // item, and its values move as 16-byte pieces.
+      for (int e = ct; e < a.R * (D / 8); e += n_ct) {
+        const int r = e / (D / 8);
+        const int d = (e - r * (D / 8)) * 8;
         const int g = r >> 4;
         const int rr = r & 15;
         float M = neg_inf();
 #pragma unroll
         for (int w = 0; w < NWK; ++w) M = fmaxf(M, sc_m[(g * NWK + w) * 16 + rr]);
-        float num = 0.f, den = 0.f, dent = 0.f;
+        float num[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float den = 0.f, dent = 0.f;
         if (M != neg_inf()) {
 #pragma unroll
           for (int w = 0; w < NWK; ++w) {
             const int cwi = g * NWK + w;
-            const float wt = exp2f(sc_m[cwi * 16 + rr] - M);
-            num += wt * sc_o[(cwi * 16 + rr) * D + d];
-            den += wt * sc_l[cwi * 16 + rr];
-            dent += wt * sc_lt[cwi * 16 + rr];
+            const float mw = sc_m[cwi * 16 + rr];
+            const float wt = mw == neg_inf() ? 0.f : fast_exp2(mw - M);
+            const float4 o0 = *reinterpret_cast<const float4*>(sc_o + (cwi * 16 + rr) * D + d);
+            const float4 o1 = *reinterpret_cast<const float4*>(sc_o + (cwi * 16 + rr) * D + d + 4);
+            num[0] = fmaf(wt, o0.x, num[0]);
+            num[1] = fmaf(wt, o0.y, num[1]);
+            num[2] = fmaf(wt, o0.z, num[2]);
+            num[3] = fmaf(wt, o0.w, num[3]);
+            num[4] = fmaf(wt, o1.x, num[4]);
+            num[5] = fmaf(wt, o1.y, num[5]);
+            num[6] = fmaf(wt, o1.z, num[6]);
+            num[7] = fmaf(wt, o1.w, num[7]);
+            den = fmaf(wt, sc_l[cwi * 16 + rr], den);
+            dent = fmaf(wt, sc_lt[cwi * 16 + rr], dent);
           }
         }
-        const float v = dent > 0.f ? (FP8 ? num / dent * a.out_mul : num / dent) : 0.f;
-        const float lse = den > 0.f ? M + (FP8 ? log2f(den) - 7.f : log2f(den)) : neg_inf();
+        const float inv = dent > 0.f ? (FP8 ? a.out_mul : 1.f) / dent : 0.f;
         if (direct) {
           const size_t orow = out_row_index(a, b, h, r);
-          a.out[orow * D + d] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
-          if (d == 0) a.lse2[orow] = lse;
+          *reinterpret_cast<uint4*>(a.out + orow * D + d) =
+              make_uint4(pack_bf16x2(num[0] * inv, num[1] * inv), pack_bf16x2(num[2] * inv, num[3] * inv),
+                         pack_bf16x2(num[4] * inv, num[5] * inv), pack_bf16x2(num[6] * inv, num[7] * inv));
+          if (d == 0) a.lse2[orow] = den > 0.f ? M + (FP8 ? log2f(den) - 7.f : log2f(den)) : neg_inf();
         } else {
-          part_o[static_cast<size_t>(r) * D + d] = v;
+          float* dst = part_o + static_cast<size_t>(r) * D + d;
+          *reinterpret_cast<float4*>(dst) = make_float4(num[0] * inv, num[1] * inv, num[2] * inv, num[3] * inv);
+          *reinterpret_cast<float4*>(dst + 4) = make_float4(num[4] * inv, num[5] * inv, num[6] * inv, num[7] * inv);
           if (d == 0) {
-            part_lse[r] = lse;
+            part_lse[r] = den > 0.f ? M + (FP8 ? log2f(den) - 7.f : log2f(den)) : neg_inf();
             part_lseo[r] = dent > 0.f ? M + (FP8 ? log2f(dent) - 7.f : log2f(dent)) : neg_inf();
           }
         }
