@@ -320,9 +320,11 @@ __device__ __forceinline__ int chunk_page(const AttnArgs& a, const int* PB, cons
 // swizzle, and one thread hands the box to the TMA engine, which writes it
 // asynchronously: bf16 as one box (64 columns, G heads, K tokens) of the
 // output, fp32 as two boxes (32 columns, R rows) of the partial slot.  The
-// threads only wait until the box has been read out of shared memory.  Kept
-// out of line: it runs once per segment, and inlined it would crowd the tile
-// loop's registers.
+// engine's read of a box is waited for only where the buffer is written
+// again: at the next call (the previous segment's box) and, for fp32,
+// between the two boxes, after the second half's accumulator columns have
+// been fetched.  Kept out of line: it runs once per segment, and inlined it
+// would crowd the tile loop's registers.
 template <int D>
 __device__ __noinline__ void store_segment_rows(const AttnArgs& a, const CUtensorMap* tm_out,
                                                 const CUtensorMap* tm_part, uint8_t* stg,
@@ -333,10 +335,18 @@ __device__ __noinline__ void store_segment_rows(const AttnArgs& a, const CUtenso
   const int bar_id = 4 + grp;
   uint8_t* srow = stg + row * 128;
   const int sw = row & 7;
+  // The previous segment's box may still be reading this buffer.
+  if (leader) bulk_wait_read_all();
+  named_barrier(bar_id, 128);
 #pragma unroll 1
   for (int cc = 0; cc < 2; ++cc) {
     uint32_t o0[32], o1[32];
     tmem_ld32x2_wait(lane_addr + kColO0 + col0 + cc * 32, lane_addr + kColO1 + col0 + cc * 32, o0, o1);
+    if (!direct && cc == 1) {
+      // The first fp32 box reads the buffer until here.
+      if (leader) bulk_wait_read_all();
+      named_barrier(bar_id, 128);
+    }
     // A group that saw no key of this segment holds a stale or
     // uninitialised accumulator: select, so it cannot leak in.
     auto val = [&](int e) {
@@ -365,9 +375,7 @@ __device__ __noinline__ void store_segment_rows(const AttnArgs& a, const CUtenso
         else
           tma_store_3d(tm_part, stg_u32, col0 + cc * 32, 0, unit);
         bulk_commit();
-        bulk_wait_read_all();
       }
-      named_barrier(bar_id, 128);  // the staging rows may be written again
     }
   }
 }
