@@ -103,8 +103,9 @@ typedef struct dflash_params {
                                 or D = 128 with R > 32 and B*Hkv > 32; else mma.sync
                                 (tcgen05 also when an fp8 mma.sync plan would not
                                 fit shared memory) */
-  int32_t force_split_tiles; /* 1..64: key tiles per split unit, or per CTA range on
-                                the tcgen05 path (tests); 0 = planner */
+  int32_t force_split_tiles; /* 1..256: key tiles per split unit (as many as leave the
+                                unit's page ids room in shared memory), or per CTA
+                                range on the tcgen05 path (tests); 0 = planner */
   int32_t right_window;      /* with future_keys = 0: row i also sees block keys
                                 i+1 .. i+right_window (0 .. K-1); 0 when future_keys = 1 */
   int32_t kv_dtype;          /* DFLASH_KV_BF16 or DFLASH_KV_FP8_E4M3 (pool element type) */

@@ -132,7 +132,11 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   const bool fp8 = p->kv_dtype == DFLASH_KV_FP8_E4M3;
   const bool tc_pref = (k.R > 64 && pairs > 8) || (D == 128 && k.R > 32 && pairs > 32);
   const int R_pad_mma = (k.R + 15) / 16 * 16;
-  const bool mma_ok = split_mma_smem_bytes(D, R_pad_mma, split_mma_kpw(D, R_pad_mma), fp8) <= kMaxSmemPerCta;
+  // The mma.sync kernel keeps its unit's page ids in shared memory: at least
+  // one tile's must fit.
+  const int mma_ppt = split_mma_tile_keys(D) / p->page_size;  // pages per tile
+  const bool mma_ok =
+      split_mma_smem_bytes(D, R_pad_mma, split_mma_kpw(D, R_pad_mma), fp8, mma_ppt) <= kMaxSmemPerCta;
   int path = p->force_path;
   if (path == DFLASH_PATH_AUTO)
     path = ((tc_pref || !mma_ok) && tc_ok) ? DFLASH_PATH_TCGEN05 : DFLASH_PATH_MMA;
@@ -146,7 +150,7 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
     const int consumer_warps = (k.R_pad / 16) * (k.T / k.kpw);
     k.threads = 32 * (1 + consumer_warps);
     if (fp8) k.threads += 32 * mma_widen_warps(D, k.kpw, k.threads);
-    k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8);
+    k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8, 0);  // page ids added below
   } else {
     k.R_pad = 128;
     k.T = split_tc_tile_keys(D);
@@ -181,7 +185,13 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
     *out = k;
     return true;
   }
+  // Tiles per unit: at most kMaxSplitTiles, and as many as leave the unit's
+  // page ids room in shared memory.
+  const int smem_base = k.smem_bytes;
+  int c_cap = (kMaxSmemPerCta - smem_base) / (4 * mma_ppt);
+  if (c_cap > kMaxSplitTiles) c_cap = kMaxSplitTiles;
   int C = p->force_split_tiles;
+  if (C > c_cap) return false;
   if (C <= 0) {
     // Cost in tile-times of one SM: the waves of units, each C tiles plus a
     // pipeline fill of about two tiles, plus the partial state every unit
@@ -196,7 +206,7 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
     const double partial_tiles = 2.0 * k.R / k.T;
     double best = 1e300;
     C = 1;
-    const int c_hi = mt < kMaxSplitTiles ? mt : kMaxSplitTiles;
+    const int c_hi = mt < c_cap ? mt : c_cap;
     for (int c = 1; c <= c_hi; ++c) {
       const int S = (mt + c - 1) / c;
       if (S > 65535) continue;
@@ -217,6 +227,7 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   k.C = C;
   k.S = (mt + C - 1) / C;
   k.units = static_cast<int64_t>(p->batch) * p->num_kv_heads * k.S;
+  k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8, C * mma_ppt);
   if (k.S > 65535 || p->num_kv_heads > 65535 || p->batch > 65535) return false;
   *out = k;
   return true;

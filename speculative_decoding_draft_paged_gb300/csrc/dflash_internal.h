@@ -29,8 +29,7 @@ constexpr int kStages = 4;             // TMA pipeline depth of the split kernel
 DF_HD constexpr int mma_widen_warps(int D, int kpw, int base_threads) {
   return base_threads > 288 ? 3 : ((D == 64 && kpw <= 32) ? 4 : 3);
 }
-constexpr int kMaxSplitTiles = 64;     // key tiles per split unit, at most
-constexpr int kMaxUnitSlots = 512;     // page-table slots one unit can touch (64 tiles x 8 pages)
+constexpr int kMaxSplitTiles = 256;    // key tiles per split unit, at most
 constexpr int kTcMaxBatch = 768;       // tcgen05 kernel: requests whose tile prefix fits shared memory
 constexpr int kTcMinTiles = 4;         // tcgen05 kernel: fewest tiles one CTA's range takes
 
@@ -206,7 +205,7 @@ int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat);
 int launch_combine_parts(const AttnArgs& a, int n_parts, cudaStream_t stream);
 
 // Shared-memory bytes of each split kernel for a plan (used by the planner).
-int split_mma_smem_bytes(int D, int R_pad, int kpw, bool fp8);
+int split_mma_smem_bytes(int D, int R_pad, int kpw, bool fp8, int page_slots);
 int split_tc_smem_bytes(int D);
 
 }  // namespace dflash

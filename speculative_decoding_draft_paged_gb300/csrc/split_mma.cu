@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
   uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + a.R_pad * D * 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + (FP8 ? 3 : 2) * NS);
   volatile int* issued_count = abort_flag + 1;
-  int* pg_smem = const_cast<int*>(abort_flag) + 4;  // kMaxUnitSlots page ids
+  int* pg_smem = const_cast<int*>(abort_flag) + 4;  // the unit's page ids: C * T / P
   auto full_bar = [&](int st) { return bar_u32 + 8u * st; };
   auto empty_bar = [&](int st) { return bar_u32 + 8u * (NS + st); };
   // fp8 context: every widening warp has widened its share of stage st.
@@ -701,10 +701,10 @@ int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
 
 }  // namespace
 
-int split_mma_smem_bytes(int D, int R_pad, int /*kpw*/, bool fp8) {
+int split_mma_smem_bytes(int D, int R_pad, int /*kpw*/, bool fp8, int page_slots) {
   const int stage = (D == 64) ? MmaTile<64>::kStageBytes : MmaTile<128>::kStageBytes;
   const int codes = fp8 ? kStages * ((D == 64) ? MmaTile<64>::kCodeStageBytes : MmaTile<128>::kCodeStageBytes) : 0;
-  return 1024 + kStages * stage + codes + R_pad * D * 2 + 8 * (fp8 ? 3 : 2) * kStages + 16 + 4 * kMaxUnitSlots;
+  return 1024 + kStages * stage + codes + R_pad * D * 2 + 8 * (fp8 ? 3 : 2) * kStages + 16 + 4 * page_slots;
 }
 
 int split_mma_kpw(int D, int R_pad) { return kpw_for(D, R_pad); }

@@ -93,10 +93,8 @@ def base_params(**kw):
     dict(future_keys=0, right_window=-1), dict(future_keys=0, right_window=7),
     dict(future_keys=1, right_window=2),
     dict(scale=float("nan")), dict(scale=0.0), dict(scale=-0.125), dict(max_ctx_len=-1), dict(max_ctx_len=40 * 32 - 6),
-    dict(num_pages=0), dict(force_path=3), dict(force_split_tiles=-1), dict(force_split_tiles=65),
+    dict(num_pages=0), dict(force_path=3), dict(force_split_tiles=-1), dict(force_split_tiles=257),
     dict(kv_dtype=2), dict(kv_dtype=-1), dict(test_flags=2), dict(test_flags=-1),
-    dict(kv_dtype=1, force_path=1, head_dim=128, page_size=64, num_q_heads=16, num_kv_heads=1,
-         block_size=8, max_pages_per_req=30),
 ])
 def test_invalid_params_rejected(dflash_lib, bad):
     d = dflash_lib

@@ -111,6 +111,7 @@ def test_fp8_minimax(cuda_device, path, win, fk, r):
     (128, 16, 3, 4, 2),    # R = 6
     (128, 32, 4, 64, 4),   # R = 64
     (64, 64, 16, 8, 1),    # K = 16, R = 128
+    (128, 64, 8, 32, 2),   # R = 128 at D = 128: the largest code ring of the mma.sync grid
 ])
 @pytest.mark.parametrize("path", PATHS)
 def test_fp8_shapes(cuda_device, path, D, P, K, Hq, Hkv):
