@@ -34,11 +34,12 @@ __device__ __forceinline__ float neg_inf_f() { return __int_as_float(0xff800000)
 // divided by the sum of its rounded probabilities, are weighted by those
 // rounded sums (part_lseo), so the result is divided by the row's whole
 // rounded sum as it would be without a split.  Few partials (the usual
-// case): one partial per lane for the weights, then the partial rows four
-// at a time with their loads in flight together.  Otherwise lanes take
+// case): one partial per lane for the weights, then the partial rows GROUP
+// at a time with their loads in flight together (8 for the unit grid; 4 for
+// the flat split, whose six blocks per SM leave fewer registers).  Otherwise lanes take
 // partials lane, lane+32, ... for the max and the sums, and the rows eight
 // at a time.
-template <int D, typename UnitOf>
+template <int D, int GROUP, typename UnitOf>
 __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, UnitOf unit_of,
                                             int lane, float (&acc)[D / 32], float& M_out,
                                             float& den_out, float& deno_out) {
@@ -80,12 +81,19 @@ __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, Un
     den_out = warp_sum(w);
     deno_out = warp_sum(wo);
     if (M == neg_inf_f()) return;
-    for (int s0 = 0; s0 < ns; s0 += 4) {
-      float ov[4][V];
+    for (int s0 = 0; s0 < ns; s0 += GROUP) {
+      float ov[GROUP][V];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) load_row(s0 + t < ns ? s0 + t : ns - 1, ov[t]);
+      for (int t = 0; t < GROUP; ++t) {
+        if (s0 + t < ns) {
+          load_row(s0 + t, ov[t]);
+        } else {
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+          for (int e = 0; e < V; ++e) ov[t][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) {
         const float wt = __shfl_sync(0xffffffffu, wo, (s0 + t) & 31);
         const float wv = s0 + t < ns ? wt : 0.f;
 #pragma unroll
@@ -182,7 +190,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const AttnArgs a) {
   pdl_wait_primary();
   if (!active) return;
   float acc[D / 32], M, den, deno;
-  combine_row<D>(a, r, ns, [&](int sp) -> size_t { return unit0 + sp; }, lane, acc, M, den, deno);
+  combine_row<D, 8>(a, r, ns, [&](int sp) -> size_t { return unit0 + sp; }, lane, acc, M, den, deno);
   write_row<D>(a, row_id, lane, acc, M, den, deno);
 }
 
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 6) combine_flat_kernel(const AttnArg
 
   pdl_wait_primary();
   float acc[D / 32], M, den, deno;
-  combine_row<D>(
+  combine_row<D, 4>(
       a, r, c1 - c0 + 1,
       [&](int sp) -> size_t { return static_cast<size_t>(c0 + sp) * 2 + (sp == 0 ? slot0 : 0); },
       lane, acc, M, den, deno);
@@ -331,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) combine_parts_kernel(const AttnArgs 
   const long long rows = static_cast<long long>(a.B) * a.K * a.Hq;
   if (row_id >= rows) return;
   float acc[D / 32], M, den, deno;
-  combine_row<D>(a, static_cast<int>(row_id), n_parts, [](int sp) -> size_t { return static_cast<size_t>(sp); },
+  combine_row<D, 8>(a, static_cast<int>(row_id), n_parts, [](int sp) -> size_t { return static_cast<size_t>(sp); },
                  lane, acc, M, den, deno);
   write_row<D>(a, row_id, lane, acc, M, den, deno);
 }

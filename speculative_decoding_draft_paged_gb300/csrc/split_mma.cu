@@ -234,6 +234,22 @@ __global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAX
     prefetch_tensormap(&tm_v);
   }
 
+  // The first 128 CTAs pull the page table and the queries into L2 (each a
+  // share), so that the units of later waves find their page ids and query
+  // rows there rather than in DRAM.
+  {
+    const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (cta < 128u) {
+      const size_t tab_lines = (static_cast<size_t>(a.B) * a.max_pages * 4 + 127) / 128;
+      const size_t q_lines = (static_cast<size_t>(a.B) * a.K * a.Hq * D * 2 + 127) / 128;
+      const size_t per = (tab_lines + q_lines + 127) / 128;
+      const size_t l0 = cta * per;
+      const size_t l1 = l0 + per < tab_lines + q_lines ? l0 + per : tab_lines + q_lines;
+      for (size_t l = l0 + threadIdx.x; l < l1; l += blockDim.x)
+        prefetch_l2(l < tab_lines ? reinterpret_cast<const uint8_t*>(a.page_table) + l * 128
+                                  : reinterpret_cast<const uint8_t*>(a.q) + (l - tab_lines) * 128);
+    }
+  }
   const int pages_per_tile = T / a.P;
   load_unit_pages(a, b, tile0 * pages_per_tile, ntiles * pages_per_tile, geo.lo_min / a.P,
                   (paged_end(a, geo) + a.P - 1) / a.P, pg_smem, threadIdx.x, blockDim.x);
