@@ -200,9 +200,11 @@ def time_oracle_sample(spec, budget_s: float = 15.0, device_inputs=None, fp8: bo
     from speculative_decoding_draft_paged_gb300 import workloads as W
 
     threads = os.cpu_count() or 1
-    # Estimated oracle cost: ~4 flops per (row, key, dim), ~0.5 GFLOP/s per core.
+    # Estimated oracle cost: ~4 flops per (row, key, dim) at ~2.5 GFLOP/s per
+    # core (measured on a 16-core Arm host: 127 GFLOP of ragged_B256 requests
+    # in 3.1 s), so that the sample takes about budget_s seconds.
     per_req = [spec.Hq * spec.K * (spec.visible_ctx(L) + spec.K) * spec.D * 4 for L in spec.ctx_lens]
-    rate = 0.5e9 * threads
+    rate = 2.5e9 * threads
     ids, cost = [], 0.0
     for b in range(spec.B):
         if ids and cost + per_req[b] / rate > budget_s:

@@ -213,9 +213,8 @@ int dflash_block_attn_timed(const dflash_params* p, const void* q, const void* k
  *     nothing is launched.
  *   - The first call in a device's context looks up the array's device
  *     address there (cudaGetSymbolAddress, which may also load the library's
- *     device code) and caches it for that context; make that first call
- *     before capturing a stream.  A context created anew (after
- *     cudaDeviceReset, say) gets a fresh lookup on its first call.
+ *     device code) and caches it for that context.  A context created anew
+ *     (after cudaDeviceReset, say) gets a fresh lookup on its first call.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind.  The kernels need no part of it to start at zero, and the
  *     device status word inside it is not reported here.  Calls whose work
