@@ -71,6 +71,22 @@ __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, Un
     return x;
   };
   if (ns <= 32) {
+    // The first GROUP partial rows are loaded beside the LSEs (their
+    // addresses do not depend on the weights): one round of loads before
+    // the first products instead of two.
+    float ov[GROUP][V];
+    auto load_group = [&](int s0) {
+#pragma unroll
+      for (int t = 0; t < GROUP; ++t) {
+        if (s0 + t < ns) {
+          load_row(s0 + t, ov[t]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < V; ++e) ov[t][e] = 0.f;
+        }
+      }
+    };
+    load_group(0);
     const size_t u = lane < ns ? unit_of(lane) * a.R + r : 0;
     const float ls = lane < ns ? a.part_lse[u] : neg_inf_f();
     const float lo = lane < ns ? a.part_lseo[u] : neg_inf_f();
@@ -82,16 +98,7 @@ __device__ __forceinline__ void combine_row(const AttnArgs& a, int r, int ns, Un
     deno_out = warp_sum(wo);
     if (M == neg_inf_f()) return;
     for (int s0 = 0; s0 < ns; s0 += GROUP) {
-      float ov[GROUP][V];
-#pragma unroll
-      for (int t = 0; t < GROUP; ++t) {
-        if (s0 + t < ns) {
-          load_row(s0 + t, ov[t]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < V; ++e) ov[t][e] = 0.f;
-        }
-      }
+      if (s0 > 0) load_group(s0);
 #pragma unroll
       for (int t = 0; t < GROUP; ++t) {
         const float wt = __shfl_sync(0xffffffffu, wo, (s0 + t) & 31);
@@ -196,10 +203,6 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const AttnArgs a) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 6) combine_flat_kernel(const AttnArgs a) {
-  __shared__ int PB[kTcMaxBatch + 1];
-  __shared__ int Lc[kTcMaxBatch];
-  __shared__ int warp_sums[kWarpsPerBlock];
-  flat_tile_prefix<kThreads>(a, PB, Lc, warp_sums, false);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long row_id = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
@@ -209,15 +212,34 @@ __global__ void __launch_bounds__(kThreads, 6) combine_flat_kernel(const AttnArg
   row_coords(a, row_id, b, i, hq);
   const int h = hq / a.G;
   const int r = i * a.G + (hq - h * a.G);
-  const FlatMap fmap = flat_map(a, PB);
-  const int nb = PB[b + 1] - PB[b];
-  const int g0 = a.Hkv * PB[b] + h * nb;
-  const long long cp = flat_pair_cost(a, PB, fmap, b, h);
-  const int c0 = static_cast<int>(cp / fmap.q);
-  const int c1 = static_cast<int>((cp + nb - 1) / fmap.q);
+  // The three entries of the split kernel's tile prefix this row needs (the
+  // tiles of the requests before b, of b, of all requests), from the same
+  // per-request tile counts as flat_tile_prefix, by a warp reduction.
+  int before = 0, own = 0, all = 0;
+  for (int bb = lane; bb < a.B; bb += 32) {
+    const int nt = make_geometry(__ldg(&a.ctx_lens[bb]), a.max_ctx_len, a.K, a.W, kFlatTileKeys, 1).n_tiles;
+    all += nt;
+    before += bb < b ? nt : 0;
+    own += bb == b ? nt : 0;
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    all += __shfl_xor_sync(0xffffffffu, all, m);
+    before += __shfl_xor_sync(0xffffffffu, before, m);
+    own += __shfl_xor_sync(0xffffffffu, own, m);
+  }
+  const FlatMap fmap = flat_map_total(a, all);
+  const int nb = own;
+  // Cost position of the pair's first tile (flat_pair_cost).
+  const long long cp = static_cast<long long>(a.Hkv) * before + static_cast<long long>(h) * nb +
+                       static_cast<long long>(fmap.w) * (static_cast<long long>(b) * a.Hkv + h);
+  const int c0 = static_cast<int>(div_nonneg(cp, fmap.q));
+  const int c1 = static_cast<int>(div_nonneg(cp + nb - 1, fmap.q));
   if (c0 == c1) return;  // the split kernel wrote this row
-  // Slot 1 of c0 when c0's range starts before this pair.
-  const int slot0 = flat_tile_at(a, PB, fmap, static_cast<long long>(c0) * fmap.q) < g0 ? 1 : 0;
+  // Slot 1 of c0 when c0's range starts before this pair, i.e. at or before
+  // the previous pair's last tile: the cost positions between that tile and
+  // this pair's first are the previous pair's end (fmap.w of them).
+  const int slot0 = static_cast<long long>(c0) * fmap.q < cp - fmap.w ? 1 : 0;
 
   pdl_wait_primary();
   float acc[D / 32], M, den, deno;

@@ -325,9 +325,17 @@ struct FlatMap {
   int total;  // tiles of all pairs
 };
 
-__device__ __forceinline__ FlatMap flat_map(const AttnArgs& a, const int* PB) {
+// a / b for 0 <= a and 0 < b, in 32 bits when both fit (the 64-bit division
+// is a long instruction sequence).
+__device__ __forceinline__ long long div_nonneg(long long a, long long b) {
+  if (((a | b) >> 31) == 0) return static_cast<unsigned>(a) / static_cast<unsigned>(b);
+  return a / b;
+}
+
+// The map from the tiles of all requests (tiles_all = PB[B]).
+__device__ __forceinline__ FlatMap flat_map_total(const AttnArgs& a, int tiles_all) {
   FlatMap m;
-  m.total = a.Hkv * PB[a.B];
+  m.total = a.Hkv * tiles_all;
   if (a.qn_force > 0) {
     m.q = a.qn_force;
     m.w = 0;
@@ -335,11 +343,13 @@ __device__ __forceinline__ FlatMap flat_map(const AttnArgs& a, const int* PB) {
   }
   m.w = a.seg_cost;
   const long long cost = static_cast<long long>(m.total) + static_cast<long long>(m.w) * a.B * a.Hkv;
-  long long q = (cost + a.ncta - 1) / a.ncta;
+  long long q = div_nonneg(cost + a.ncta - 1, a.ncta);
   if (q < a.qn_min) q = a.qn_min;
   m.q = static_cast<int>(q);
   return m;
 }
+
+__device__ __forceinline__ FlatMap flat_map(const AttnArgs& a, const int* PB) { return flat_map_total(a, PB[a.B]); }
 
 // Cost position of the first tile of pair (b, h).
 __device__ __forceinline__ long long flat_pair_cost(const AttnArgs& a, const int* PB, const FlatMap& m,
