@@ -277,7 +277,33 @@ __global__ void __launch_bounds__(kThreads) combine_wide_kernel(const AttnArgs a
 
   pdl_wait_primary();
   // This warp's partials sp = warp + 8k, k < nk <= 32: lane k holds the LSEs.
+  // Its first eight partial rows are loaded beside the LSEs (their addresses
+  // do not depend on the weights).
   const int nk = ns > warp ? (ns - warp + 7) / 8 : 0;
+  float ov[8][V];
+  auto load_group = [&](int k0) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      if (k0 + t < nk) {
+        const float* po = a.part_o + ((unit0 + warp + 8 * (k0 + t)) * a.R + r) * D + lane * V;
+        if constexpr (V == 2) {
+          const float2 v = *reinterpret_cast<const float2*>(po);
+          ov[t][0] = v.x;
+          ov[t][1] = v.y;
+        } else {
+          const float4 v = *reinterpret_cast<const float4*>(po);
+          ov[t][0] = v.x;
+          ov[t][1] = v.y;
+          ov[t][2] = v.z;
+          ov[t][3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) ov[t][e] = 0.f;
+      }
+    }
+  };
+  load_group(0);
   const size_t u = lane < nk ? (unit0 + warp + 8 * lane) * a.R + r : 0;
   const float ls = lane < nk ? a.part_lse[u] : neg_inf_f();
   const float lo = lane < nk ? a.part_lseo[u] : neg_inf_f();
@@ -296,23 +322,7 @@ __global__ void __launch_bounds__(kThreads) combine_wide_kernel(const AttnArgs a
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
   for (int k0 = 0; k0 < nk; k0 += 8) {
-    float ov[8][V];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int k = k0 + t < nk ? k0 + t : nk - 1;
-      const float* po = a.part_o + ((unit0 + warp + 8 * k) * a.R + r) * D + lane * V;
-      if constexpr (V == 2) {
-        const float2 v = *reinterpret_cast<const float2*>(po);
-        ov[t][0] = v.x;
-        ov[t][1] = v.y;
-      } else {
-        const float4 v = *reinterpret_cast<const float4*>(po);
-        ov[t][0] = v.x;
-        ov[t][1] = v.y;
-        ov[t][2] = v.z;
-        ov[t][3] = v.w;
-      }
-    }
+    if (k0 > 0) load_group(k0);
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       const float wt = __shfl_sync(0xffffffffu, wo, (k0 + t) & 31);
