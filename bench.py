@@ -252,7 +252,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     spec = workload_spec(args.workload)
-    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    # About 90 s of oracle work for the whole run, at least 1 s per step.
+    budget = max(1.0, 90.0 / max(1, args.steps + args.warmup))
     vals, times = [], []
     cores = None
     desc = ""
