@@ -81,8 +81,9 @@ struct TcCfg {
   static constexpr int kOffStage = kOffV + NSV * kTileBytes;
   static constexpr int kOffBar = kOffStage + 2 * kStageBytes;
   // k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
-  // s_free[2], p_full[2], pv_done[2], q_full, q_free, k_fix[NSK], v_read[2]
-  static constexpr int kNumBars = 3 * NSK + 2 * NSV + 12;
+  // s_free[2], p_full[2], pv_done[2], q_full, q_free, k_fix[NSK], v_read[2],
+  // q_free1 (two-issuer path: group 1's release of the query tile)
+  static constexpr int kNumBars = 3 * NSK + 2 * NSV + 13;
   // fp8 context: a stage's codes sit at byte kCodeOff of the stage, row r in
   // [kCodeOff + r*D, +D) (the bf16 tile's second half for D = 128), its
   // 16-byte words permuted by the TMA swizzle.
@@ -100,6 +101,7 @@ struct TcCfg {
   static constexpr int kOffOnes = (kOffVStage + 2 * kVStageBytes + 127) / 128 * 128;
   static constexpr int kOnesBytes = 512;
   static constexpr int kSmem = kOffOnes + kOnesBytes + 1024;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
   // TMEM columns: S0 [0,64) S1 [64,128) O0 [128,128+D) O1 [256,256+D)
   // P0 [384,416) P1 [416,448) (bf16 pairs), rounded row sums L0 [448,464)
   // L1 [464,480) (16 equal columns each).
@@ -380,7 +382,138 @@ __device__ __noinline__ void store_segment_rows(const AttnArgs& a, const CUtenso
   }
 }
 
-template <int D, bool FP8>
+// The MMA issue of one softmax group on the two-issuer path (bf16 pages, no
+// dense suffix): warp 1 issues for group 0 and warp 11 for group 1, each the
+// QK^T of its tiles j = g, g+2, ... of the CTA's range and the PV of each
+// tile after the group's next QK^T.  A group's next scores are then ready
+// when its softmax of the current tile ends, whatever the other group is
+// doing: one thread issuing for both serialises the two chains, since an
+// MMA's issue lasts about as long as its execution (a single issuer measured
+// 85.0 us against 64.6 us for two on the MiniMax shape at 65 tiles per CTA).
+// Across a segment boundary the previous segment's PV goes first, so that
+// segment's output does not wait for the next query tile.  The group
+// releases each segment's query tile by one arrival on its own barrier
+// (q_free for group 0, q_free1 for group 1), once its last QK^T there has
+// completed (or at once when it has no tile there), and always after that
+// query tile has landed: no release runs a phase ahead of the K producer,
+// which reloads the query tile once both groups have released it.  Returns
+// false when a wait ran out.
+template <int D>
+__device__ __noinline__ bool tc_issue_group(int g, int n, int start, int end, const int* PB, const AttnArgs& a,
+                                            uint32_t tmem, uint32_t base, volatile int* abort_flag) {
+  using C = TcCfg<D>;
+  constexpr int T = C::T;
+  constexpr int NSK = C::NSK;
+  constexpr int NSV = C::NSV;
+  const uint32_t bars = base + C::kOffBar;
+  auto k_full = [&](int st) { return bars + 8u * st; };
+  auto k_empty = [&](int st) { return bars + 8u * (NSK + st); };
+  auto v_full = [&](int st) { return bars + 8u * (2 * NSK + st); };
+  auto v_empty = [&](int st) { return bars + 8u * (2 * NSK + NSV + st); };
+  constexpr int kB0 = 2 * NSK + 2 * NSV;
+  const uint32_t s_full = bars + 8u * (kB0 + g);
+  const uint32_t s_free = bars + 8u * (kB0 + 2 + g);
+  const uint32_t p_full = bars + 8u * (kB0 + 4 + g);
+  const uint32_t pv_done = bars + 8u * (kB0 + 6 + g);
+  const uint32_t q_full = bars + 8u * (kB0 + 8);
+  const uint32_t q_rel = bars + 8u * (g == 0 ? kB0 + 9 : kB0 + 12 + NSK);
+  constexpr uint32_t idesc_qk = idesc_bf16_f32(128, T, false);
+  constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+  constexpr uint32_t idesc_l = idesc_bf16_f32(128, 16, false);
+  const uint64_t dq = smem_desc_sw128(base + C::kOffQ, 16, 1024);
+  const uint64_t dk = smem_desc_sw128(base + C::kOffK, 16, 1024);
+  const uint64_t dv = smem_desc_sw128(base + C::kOffV, T * 128, 1024);
+  const uint64_t d_ones = smem_desc_noswz(base + C::kOffOnes, 128, 256);
+  const uint32_t o_col = g ? C::kColO1 : C::kColO0;
+  // This thread's latest commit (s_full or pv_done: barriers no other thread
+  // moves, so its phase can be waited for at the end).
+  uint32_t last_bar = 0, last_par = 0;
+  int pv_seg = -1;                      // segment of the group's latest PV
+  // O_g += P_j V_j (and L_g += P_j 1); the group's first PV in a segment
+  // overwrites O_g: its P arrives only after every softmax thread has read
+  // the previous segment's accumulators.
+  auto pv = [&](int jj, int seg) -> bool {
+    const int st = jj % NSV;
+    if (!mbar_wait(p_full, (jj >> 1) & 1)) return false;
+    if (!mbar_wait(v_full(st), (jj / NSV) & 1)) return false;
+    tc_fence_after();
+    const bool fresh = pv_seg != seg;
+    pv_seg = seg;
+    const uint32_t v_off = st * C::kTileBytes;
+#pragma unroll
+    for (int kk = 0; kk < T / 16; ++kk)
+      umma_bf16_ts(tmem + o_col, tmem + C::kColP + g * (T / 2) + kk * 8, dv + ((v_off + kk * 16 * 128) >> 4),
+                   idesc_pv, (!fresh || kk > 0) ? 1u : 0u);
+#pragma unroll
+    for (int kk = 0; kk < T / 16; ++kk)
+      umma_bf16_ts(tmem + C::kColL + g * 16, tmem + C::kColP + g * (T / 2) + kk * 8, d_ones, idesc_l,
+                   (!fresh || kk > 0) ? 1u : 0u);
+    umma_commit(v_empty(st));
+    umma_commit(pv_done);
+    last_bar = pv_done;
+    last_par = (jj >> 1) & 1;
+    return true;
+  };
+  Seg sg = seg_first(PB, a.B, a.Hkv, start, end);
+  int pend = -1, pend_seg = -1;  // the group's tile whose PV is still to go
+  bool ok = true;
+  for (;;) {
+    if (pend >= 0 && pend_seg != sg.idx) {
+      ok = pv(pend, pend_seg);
+      pend = -1;
+      if (!ok) break;
+    }
+    if (*abort_flag) break;
+    if (!mbar_wait(q_full, sg.idx & 1)) {
+      ok = false;
+      break;
+    }
+    int last_here = -1;
+    for (int j = sg.j0 + (((sg.j0 & 1) != g) ? 1 : 0); j < sg.j1; j += 2) {
+      if (*abort_flag) break;
+      const int st = j % NSK;
+      if (!mbar_wait(k_full(st), (j / NSK) & 1) || (j >= 2 && !mbar_wait(s_free, ((j >> 1) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t k_off = st * C::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t x = kk >> 2;
+        const uint32_t within = (kk & 3) * 32;
+        umma_bf16(tmem + g * T, dq + ((x * (128 * 128) + within) >> 4),
+                  dk + ((k_off + x * (T * 128) + within) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(k_empty(st));
+      umma_commit(s_full);
+      last_bar = s_full;
+      last_par = (j >> 1) & 1;
+      last_here = j;
+      if (pend >= 0 && !pv(pend, pend_seg)) {
+        ok = false;
+        break;
+      }
+      pend = j;
+      pend_seg = sg.idx;
+    }
+    if (!ok || *abort_flag || sg.j1 >= n) break;
+    // Release the query tile once this group's QK^T products have read it.
+    if (last_here >= 0 && !mbar_wait(s_full, (last_here >> 1) & 1)) {
+      ok = false;
+      break;
+    }
+    mbar_arrive(q_rel);
+    seg_next(sg, PB, a.Hkv, start, end);
+  }
+  if (ok && pend >= 0 && !*abort_flag) ok = pv(pend, pend_seg);
+  // This thread's MMAs have completed before the CTA winds down: its latest
+  // commit (which covers all of them) has arrived.
+  if (last_bar != 0) (void)mbar_wait(last_bar, last_par);
+  return ok;
+}
+
+template <int D, bool FP8, bool DUAL>
 __global__ void __launch_bounds__(384, 1)
     split_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
@@ -440,6 +573,8 @@ __global__ void __launch_bounds__(384, 1)
   // fp8 context: every thread of softmax group g has read its codes of the
   // group's current V tile.
   auto v_read = [&](int g) { return bars + 8u * (kB0 + 10 + NSK + g); };
+  // Two-issuer path: group 1's release of the query tile (group 0's is q_free).
+  const uint32_t q_free1 = bars + 8u * (kB0 + 12 + NSK);
   const bool dense = a.k_block != nullptr;
   uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile uint32_t* tmem_slot = misc;          // TMEM base address from tcgen05.alloc
@@ -467,6 +602,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(q_free, 1);
+    mbar_init(q_free1, 1);
     for (int st = 0; st < NSK; ++st) mbar_init(k_fix(st), 1);
     mbar_init(v_read(0), 4);
     mbar_init(v_read(1), 4);
@@ -559,6 +695,27 @@ __global__ void __launch_bounds__(384, 1)
     const int n_issue = a.withhold_loads ? 0 : n;  // tests of the failure path
     for (int j = 0; j < n_issue; ++j) {
       while (j >= sg.j1) seg_next(sg, PB, a.Hkv, start, end);
+      if (DUAL && !is_v && j == sg.j0) {
+        // Two-issuer path: the K producer loads each segment's query tile,
+        // once both groups have released the previous one.  Box (64
+        // columns, G heads, K tokens) lands as rows r = i*G + g with the
+        // 128-byte swizzle, one box per 64-column half.
+        if (lane == 0) {
+          if (sg.idx > 0 &&
+              (!mbar_wait(q_free, (sg.idx - 1) & 1) || !mbar_wait(q_free1, (sg.idx - 1) & 1))) {
+            flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+            *abort_flag = 1;
+          } else {
+            mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(a.R * D * 2));
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x)
+              tma_load_3d(sQ + x * 128 * 128, &tm_q, x * 64, sg.h * a.G, sg.b * a.K, q_full);
+            *issued_q = sg.idx + 1;
+          }
+        }
+        __syncwarp();
+        if (*abort_flag != 0) break;
+      }
       const int k = j / tpc;
       if (k != cur_k) {
         // The next chunk's table loads were issued a chunk ago.
@@ -609,6 +766,12 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
       }
       if (*abort_flag != 0) break;
+    }
+  } else if (DUAL && (warp == 1 || warp == 11)) {
+    // ------------------------------------------------------------ MMA issuers, one per group
+    if (lane == 0 && !tc_issue_group<D>(warp == 1 ? 0 : 1, n, start, end, PB, a, tmem, base, abort_flag)) {
+      flag_status(a.status, DFLASH_STATUS_TIMEOUT);
+      *abort_flag = 1;
     }
   } else if (warp == 11) {
     // ------------------------------------------------------------ query loader
@@ -1100,7 +1263,10 @@ template <int D, bool FP8>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
              const CUtensorMap& tm_v, const CUtensorMap& tm_q, const CUtensorMap& tm_out,
              const CUtensorMap& tm_part, cudaStream_t stream) {
-  auto kern = split_tc_kernel<D, FP8>;
+  // bf16 pages without a dense suffix: one MMA issuer per softmax group
+  // (the other forms keep warp 11 for their query loads, K fixes or
+  // widening, and one issuer).
+  auto kern = (!FP8 && a.k_block == nullptr) ? split_tc_kernel<D, FP8, !FP8> : split_tc_kernel<D, FP8, false>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
   if (err != cudaSuccess) return err;
