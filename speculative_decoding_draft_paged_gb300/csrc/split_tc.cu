@@ -71,7 +71,14 @@ template <int D>
 struct TcCfg {
   static constexpr int T = 64;               // keys per tile
   static constexpr int NSK = 4;              // K ring stages
-  static constexpr int NSV = 5;              // V ring stages (V slots are held longer)
+  static constexpr int NSV = 4;              // V ring stages
+  // Tile j sits in stage j % NS of each ring.  With one MMA issuer per
+  // softmax group (tiles j and j+1 in different groups), an even stage count
+  // gives every stage to one group, so each stage's barriers are waited for
+  // phase by phase by one thread.  With an odd count a group running ahead
+  // could wait (by parity) for a stage's next phase before the other group's
+  // current one has completed, pass early, and release the stage twice.
+  static_assert(NSK % 2 == 0 && NSV % 2 == 0, "ring stages per group");
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kTileBytes = T * D * 2;  // one K or V tile
   static constexpr int kStageBytes = 128 * T * 2;   // one group's output staging buffer
