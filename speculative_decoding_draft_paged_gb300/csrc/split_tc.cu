@@ -67,18 +67,19 @@
 namespace dflash {
 namespace {
 
-template <int D>
+template <int D, bool DUAL = false>
 struct TcCfg {
   static constexpr int T = 64;               // keys per tile
   static constexpr int NSK = 4;              // K ring stages
-  static constexpr int NSV = 4;              // V ring stages
+  static constexpr int NSV = DUAL ? 4 : 5;   // V ring stages (one issuer: V slots are held longer)
   // Tile j sits in stage j % NS of each ring.  With one MMA issuer per
   // softmax group (tiles j and j+1 in different groups), an even stage count
   // gives every stage to one group, so each stage's barriers are waited for
   // phase by phase by one thread.  With an odd count a group running ahead
   // could wait (by parity) for a stage's next phase before the other group's
   // current one has completed, pass early, and release the stage twice.
-  static_assert(NSK % 2 == 0 && NSV % 2 == 0, "ring stages per group");
+  // One issuer waits in tile order, which any count allows.
+  static_assert(!DUAL || (NSK % 2 == 0 && NSV % 2 == 0), "ring stages per group");
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kTileBytes = T * D * 2;  // one K or V tile
   static constexpr int kStageBytes = 128 * T * 2;   // one group's output staging buffer
@@ -408,7 +409,7 @@ __device__ __noinline__ void store_segment_rows(const AttnArgs& a, const CUtenso
 template <int D>
 __device__ __noinline__ bool tc_issue_group(int g, int n, int start, int end, const int* PB, const AttnArgs& a,
                                             uint32_t tmem, uint32_t base, volatile int* abort_flag) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, true>;
   constexpr int T = C::T;
   constexpr int NSK = C::NSK;
   constexpr int NSV = C::NSV;
@@ -526,7 +527,7 @@ __global__ void __launch_bounds__(384, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_out,
                     const __grid_constant__ CUtensorMap tm_part) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, DUAL>;
   constexpr int T = C::T;
   constexpr int NSK = C::NSK;
   constexpr int NSV = C::NSV;
@@ -1273,12 +1274,13 @@ int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
   // bf16 pages without a dense suffix: one MMA issuer per softmax group
   // (the other forms keep warp 11 for their query loads, K fixes or
   // widening, and one issuer).
-  auto kern = (!FP8 && a.k_block == nullptr) ? split_tc_kernel<D, FP8, !FP8> : split_tc_kernel<D, FP8, false>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
+  const bool dual = !FP8 && a.k_block == nullptr;
+  auto kern = dual ? split_tc_kernel<D, FP8, !FP8> : split_tc_kernel<D, FP8, false>;
+  const int smem = dual ? TcCfg<D, true>::kSmem : TcCfg<D, false>::kSmem;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  return launch_kernel(kern, dim3(static_cast<unsigned>(plan.units)), dim3(TcCfg<D>::kThreads),
-                       TcCfg<D>::kSmem, stream, plan.pdl, a, tm_k, tm_v, tm_q, tm_out, tm_part);
+  return launch_kernel(kern, dim3(static_cast<unsigned>(plan.units)), dim3(TcCfg<D>::kThreads), smem, stream,
+                       plan.pdl, a, tm_k, tm_v, tm_q, tm_out, tm_part);
 }
 
 }  // namespace
