@@ -137,6 +137,15 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
+// The same by reading one word of the line (the value is not used; the
+// thread does not wait for it).  For the page-table rows the producers read
+// a few microseconds later this measured faster than prefetch_l2: the rows
+// were then in L2 when read.
+__device__ __forceinline__ void touch_l2(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(p));
+}
+
 // Pull a box of a 3-D tensor map into L2 (no shared-memory destination).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
