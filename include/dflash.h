@@ -134,7 +134,8 @@ typedef struct dflash_plan_info {
   int32_t smem_bytes;        /* dynamic shared memory per CTA of the split kernel */
   int32_t num_sms;           /* SM count the plan was sized for */
   int32_t flat;              /* 1: persistent flat split; 0: unit grid */
-  int32_t reserved[2];
+  int32_t ctas_per_sm;       /* split-kernel CTAs one SM holds at once */
+  int32_t reserved[1];
 } dflash_plan_info;
 
 /*

@@ -107,7 +107,8 @@ class PlanInfo(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("num_sms", ctypes.c_int32),
         ("flat", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("ctas_per_sm", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
 

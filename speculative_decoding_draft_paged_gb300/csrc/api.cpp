@@ -181,36 +181,40 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
       if (k.C < kTcMinTiles) k.C = kTcMinTiles;
     }
     k.S = 2;
+    k.ctas_per_sm = 1;
     if (k.units > 0x7fffffff) return false;
     *out = k;
     return true;
   }
   // Tiles per unit: at most kMaxSplitTiles, and as many as leave the unit's
-  // page ids room in shared memory.
-  const int smem_base = k.smem_bytes;
-  int c_cap = (kMaxSmemPerCta - smem_base) / (4 * mma_ppt);
-  if (c_cap > kMaxSplitTiles) c_cap = kMaxSplitTiles;
-  int C = p->force_split_tiles;
-  if (C > c_cap) return false;
-  if (C <= 0) {
-    // Cost in tile-times of one SM: the waves of units, each C tiles plus a
-    // pipeline fill of about two tiles, plus the partial state every unit
-    // writes and the combine reads back (2*R*D*4 bytes, 2R/T tiles' worth of
-    // K/V bytes), plus the combine's latency.  Sized for every request at max_ctx_len; shorter requests
-    // leave units empty and the block scheduler fills the gaps.
-    int ctas_per_sm = kSmemPerSm / (k.smem_bytes + 1024);
-    if (ctas_per_sm > 2048 / k.threads) ctas_per_sm = 2048 / k.threads;
-    if (ctas_per_sm < 1) ctas_per_sm = 1;
+  // page ids room in shared memory.  Cost in tile-times of one SM: the waves
+  // of units, each C tiles plus a pipeline fill of about two tiles, plus the
+  // partial state every unit writes and the combine reads back (2*R*D*4
+  // bytes, 2R/T tiles' worth of K/V bytes), plus the combine's latency.
+  // Sized for every request at max_ctx_len; shorter requests leave units
+  // empty and the block scheduler fills the gaps.  Returns 0 when a forced
+  // C is above the cap.
+  const double npairs = static_cast<double>(pairs);
+  auto ctas_per_sm_for = [&](int smem) {
+    int c = kSmemPerSm / (smem + 1024);
+    if (c > 2048 / k.threads) c = 2048 / k.threads;
+    return c < 1 ? 1 : c;
+  };
+  auto choose_C = [&](int smem_base, int ctas_per_sm) {
+    // Every CTA an SM holds keeps its page ids (and 1 KB the system reserves).
+    const int budget = ctas_per_sm > 1 ? kSmemPerSm / ctas_per_sm - 1024 : kMaxSmemPerCta;
+    int c_cap = (budget - smem_base) / (4 * mma_ppt);
+    if (c_cap > kMaxSplitTiles) c_cap = kMaxSplitTiles;
+    if (p->force_split_tiles > 0) return p->force_split_tiles <= c_cap ? p->force_split_tiles : 0;
     const double slots = static_cast<double>(num_sms) * ctas_per_sm;
-    const double pairs = static_cast<double>(p->batch) * p->num_kv_heads;
     const double partial_tiles = 2.0 * k.R / k.T;
     double best = 1e300;
-    C = 1;
+    int best_c = 1;
     const int c_hi = mt < c_cap ? mt : c_cap;
     for (int c = 1; c <= c_hi; ++c) {
       const int S = (mt + c - 1) / c;
       if (S > 65535) continue;
-      const double units = pairs * S;
+      const double units = npairs * S;
       const double waves = std::ceil(units / slots);
       // The combine walks a row's S partials eight at a time, each round
       // about one memory latency (~ one tile time); only when S > 1.  Its
@@ -220,14 +224,36 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
       const double cost = waves * (c + 2.0) + units * partial_tiles / slots + combine;
       if (cost <= best * (1.0 + 1e-12)) {
         best = cost;
-        C = c;
+        best_c = c;
       }
+    }
+    return best_c;
+  };
+  k.ctas_per_sm = ctas_per_sm_for(k.smem_bytes);
+  int C = choose_C(k.smem_bytes, k.ctas_per_sm);
+  if (C <= 0) return false;
+  // A plan of more than one wave takes the two-CTAs-per-SM form where there
+  // is one: each CTA's prologue and merge then overlap the other's streaming
+  // (the 64/16-head batch of 256 requests: 10.88 -> 10.30 ms; 8/2 heads 32K
+  // at 16 requests 64.7 -> 61.0 us).  Single-wave plans keep one CTA per SM,
+  // whose 4-stage ring and 140 registers run a short unit faster (8/2 heads
+  // 32K at 1 request: 19.5 against 21.5 us).
+  if (split_mma_two_ctas_ok(D, k.R_pad, k.kpw, fp8) &&
+      npairs * ((mt + C - 1) / C) > static_cast<double>(num_sms) * k.ctas_per_sm) {
+    const int smem2 = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8, 0, true);
+    const int cps2 = ctas_per_sm_for(smem2);
+    const int C2 = choose_C(smem2, cps2);
+    if (cps2 >= 2 && C2 > 0) {
+      k.two_ctas = true;
+      k.ctas_per_sm = cps2;
+      k.smem_bytes = smem2;
+      C = C2;
     }
   }
   k.C = C;
   k.S = (mt + C - 1) / C;
   k.units = static_cast<int64_t>(p->batch) * p->num_kv_heads * k.S;
-  k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8, C * mma_ppt);
+  k.smem_bytes = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8, C * mma_ppt, k.two_ctas);
   if (k.S > 65535 || p->num_kv_heads > 65535 || p->batch > 65535) return false;
   *out = k;
   return true;
@@ -574,6 +600,7 @@ int dflash_plan(const dflash_params* p, dflash_plan_info* info) {
   info->smem_bytes = k.smem_bytes;
   info->num_sms = k.num_sms;
   info->flat = k.path == DFLASH_PATH_TCGEN05 ? 1 : 0;
+  info->ctas_per_sm = k.ctas_per_sm;
   return DFLASH_OK;
 }
 

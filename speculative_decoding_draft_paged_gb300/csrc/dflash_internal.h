@@ -152,6 +152,8 @@ struct KernelPlan {
   int seg_cost;     // tcgen05 path: cost units of a segment's end
   bool pdl;         // launch the split kernel as a programmatic dependent of the
                     // preceding kernel (its producers wait before the first K/V load)
+  bool two_ctas;    // mma path: the two-CTAs-per-SM form (3-stage ring, 96 registers)
+  int ctas_per_sm;  // split-kernel CTAs one SM holds at once
   int num_sms;
 };
 
@@ -205,7 +207,9 @@ int launch_combine(const AttnArgs& a, cudaStream_t stream, bool pdl, bool flat);
 int launch_combine_parts(const AttnArgs& a, int n_parts, cudaStream_t stream);
 
 // Shared-memory bytes of each split kernel for a plan (used by the planner).
-int split_mma_smem_bytes(int D, int R_pad, int kpw, bool fp8, int page_slots);
+int split_mma_smem_bytes(int D, int R_pad, int kpw, bool fp8, int page_slots, bool two_ctas = false);
+// Whether the mma.sync kernel has a two-CTAs-per-SM form for this shape.
+bool split_mma_two_ctas_ok(int D, int R_pad, int kpw, bool fp8);
 int split_tc_smem_bytes(int D);
 
 }  // namespace dflash

@@ -15,12 +15,13 @@
 //
 // Roles: warp 0 lane 0 is the producer: it looks page ids up in the page table
 // and issues one 128-byte-swizzled TMA box per (page, 64-column half) for K and
-// V into a 4-stage ring (full/empty mbarriers).  Pages outside the unit's
-// visible range are fetched with page coordinate -1, which the TMA unit fills
-// with zeros.  Consumer warps form an (R_pad/16) x (T/KPW) grid: warp (wr, wk)
-// owns query rows [16 wr, 16 wr + 16) and keys [wk KPW, (wk+1) KPW) of every
-// tile, keeps its own online-softmax state in registers (base 2), and the
-// warps of a row group merge their states through shared memory at the end.
+// V into a 4-stage ring (3 in the two-CTAs-per-SM form; full/empty
+// mbarriers).  Pages outside the unit's visible range are fetched with page
+// coordinate -1, which the TMA unit fills with zeros.  Consumer warps form
+// an (R_pad/16) x (T/KPW) grid: warp (wr, wk) owns query rows [16 wr,
+// 16 wr + 16) and keys [wk KPW, (wk+1) KPW) of every tile, keeps its own
+// online-softmax state in registers (base 2), and the warps of a row group
+// merge their states through shared memory at the end.
 // Two row sums are kept: the exact one (for the LSE) and the sum of the
 // probabilities as rounded for the P.V product (one more MMA per 16 keys,
 // against an all-ones B fragment), which the output is divided by, so that
@@ -164,13 +165,17 @@ __device__ __noinline__ void write_slice_suffix(uint8_t* k_tile, uint8_t* v_tile
 }
 
 // MAXT: threads of the block without the widening warps (288 or 416).
-template <int D, int KPW, int MAXT, bool FP8>
-__global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAXT) : 0), 1)
+// TWO: the form that two CTAs share an SM with (a 3-stage ring and at most
+// 96 registers per thread), for plans of more than one wave: one CTA's
+// prologue and key-slice merge then run while the other streams, and the
+// SM holds twice the warps.
+template <int D, int KPW, int MAXT, bool FP8, bool TWO>
+__global__ void __launch_bounds__(MAXT + (FP8 ? 32 * mma_widen_warps(D, KPW, MAXT) : 0), TWO ? 2 : 1)
     split_mma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
   constexpr int T = MmaTile<D>::T;
   constexpr int NWK = T / KPW;              // key-slice warps per row group
-  constexpr int NS = kStages;
+  constexpr int NS = TWO ? 3 : kStages;
   constexpr int kTileBytes = MmaTile<D>::kTileBytes;
   constexpr int kStageBytes = MmaTile<D>::kStageBytes;
   constexpr int NT = KPW / 8;               // 8-key accumulator tiles per warp
@@ -702,10 +707,12 @@ int kpw_for(int D, int R_pad) {
   return mt == 1 ? 16 : (mt == 2 ? 32 : 64);
 }
 
-template <int D, int KPW, int MAXT = 288>
+template <int D, int KPW, int MAXT = 288, bool TWO = false>
 int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
              const CUtensorMap& tm_v, cudaStream_t stream) {
-  auto kern = a.fp8 ? split_mma_kernel<D, KPW, MAXT, true> : split_mma_kernel<D, KPW, MAXT, false>;
+  // The two-CTA form exists for bf16 pages only.
+  auto kern = TWO ? split_mma_kernel<D, KPW, MAXT, false, TWO>
+                  : (a.fp8 ? split_mma_kernel<D, KPW, MAXT, true, false> : split_mma_kernel<D, KPW, MAXT, false, false>);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          plan.smem_bytes);
   if (err != cudaSuccess) return err;
@@ -717,10 +724,18 @@ int launch_t(const AttnArgs& a, const KernelPlan& plan, const CUtensorMap& tm_k,
 
 }  // namespace
 
-int split_mma_smem_bytes(int D, int R_pad, int /*kpw*/, bool fp8, int page_slots) {
+int split_mma_smem_bytes(int D, int R_pad, int /*kpw*/, bool fp8, int page_slots, bool two_ctas) {
+  const int ns = two_ctas ? 3 : kStages;
   const int stage = (D == 64) ? MmaTile<64>::kStageBytes : MmaTile<128>::kStageBytes;
-  const int codes = fp8 ? kStages * ((D == 64) ? MmaTile<64>::kCodeStageBytes : MmaTile<128>::kCodeStageBytes) : 0;
-  return 1024 + kStages * stage + codes + R_pad * D * 2 + 8 * (fp8 ? 3 : 2) * kStages + 16 + 4 * page_slots;
+  const int codes = fp8 ? ns * ((D == 64) ? MmaTile<64>::kCodeStageBytes : MmaTile<128>::kCodeStageBytes) : 0;
+  return 1024 + ns * stage + codes + R_pad * D * 2 + 8 * (fp8 ? 3 : 2) * ns + 16 + 4 * page_slots;
+}
+
+// bf16 pages at D = 64 with two row groups of four 32-key warps (R_pad = 32:
+// the 64/16- and 8/2-head shapes, 288 threads): that form holds 96 registers
+// per thread with a few bytes of spill; the others would spill heavily.
+bool split_mma_two_ctas_ok(int D, int R_pad, int kpw, bool fp8) {
+  return D == 64 && R_pad == 32 && kpw == 32 && !fp8;
 }
 
 int split_mma_kpw(int D, int R_pad) { return kpw_for(D, R_pad); }
@@ -735,6 +750,7 @@ int launch_split_mma(const AttnArgs& a, const KernelPlan& plan, const CUtensorMa
       case 32:
         // Three row groups of four key-slice warps need 416 threads; keep
         // the register budget of the 288-thread form otherwise.
+        if (plan.two_ctas) return launch_t<64, 32, 288, true>(a, plan, tm_k, tm_v, stream);
         return 32 * (1 + plan.R_pad / 16 * (MmaTile<64>::T / 32)) > 288 ? launch_t<64, 32, 416>(a, plan, tm_k, tm_v, stream)
                                   : launch_t<64, 32, 288>(a, plan, tm_k, tm_v, stream);
       case 64: return launch_t<64, 64>(a, plan, tm_k, tm_v, stream);

@@ -182,6 +182,32 @@ def test_status_strings(dflash_lib):
     assert dflash_lib.version() >= 100
 
 
+def test_two_ctas_per_sm_plan(dflash_lib):
+    """The mma.sync plan takes its two-CTAs-per-SM form (3-stage ring, both
+    CTAs' shared memory in one SM) only for bf16 pages at D = 64 with R in
+    17..32 and more than one wave of units; every other plan holds one CTA
+    per SM."""
+    d = dflash_lib
+    sm_bytes = 228 * 1024
+    big = dict(num_q_heads=64, num_kv_heads=16, batch=256, max_ctx_len=131072, max_pages_per_req=4100)
+    pl = d.plan(base_params(**big))
+    assert pl["path"] == d.PATH_MMA and pl["threads"] == 288 and pl["ctas_per_sm"] == 2
+    assert 2 * (pl["smem_bytes"] + 1024) <= sm_bytes
+    one_wave = dict(num_q_heads=8, num_kv_heads=2, batch=1, max_ctx_len=32768, max_pages_per_req=1030)
+    assert d.plan(base_params(**one_wave))["ctas_per_sm"] == 1
+    for kw in (dict(big, num_q_heads=96),                 # R = 42: 416 threads
+               dict(big, kv_dtype=d.KV_FP8_E4M3),         # fp8 pages
+               dict(big, head_dim=128, page_size=64, max_pages_per_req=2060),
+               dict(big, force_path=d.PATH_TCGEN05, batch=64)):
+        pl = d.plan(base_params(**kw))
+        assert pl["ctas_per_sm"] == 1, kw
+        assert pl["smem_bytes"] + 1024 <= sm_bytes
+    # A forced unit length follows the same rule.
+    pl = d.plan(base_params(num_q_heads=8, num_kv_heads=2, batch=24, max_ctx_len=5000,
+                            max_pages_per_req=160, force_split_tiles=1))
+    assert pl["ctas_per_sm"] == 2 and pl["split_tiles"] == 1
+
+
 def touched_tiles(L, K, W, T):
     lo = max(0, L - W + 1) if W > 0 else 0
     return (L + K + T - 1) // T - lo // T

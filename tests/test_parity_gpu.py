@@ -79,6 +79,24 @@ def test_paths_agree(cuda_device):
     assert (l1 - l2).abs().max().item() < 1e-3
 
 
+@pytest.mark.parametrize("n_tiles", [1, 3, 0])
+def test_mma_two_ctas_per_sm(cuda_device, n_tiles):
+    """The mma.sync kernel's two-CTAs-per-SM form (a plan of more than one
+    wave at 8/2 heads, D = 64): boundary lengths, poisoned slots, forced and
+    planned unit lengths."""
+    lens = [0, 1, 6, 7, 31, 32, 33, 127, 128, 129, 255, 256, 1000, 2047, 2048, 2049, 3001, 4095, 4096, 4097,
+            4500, 4999, 5000, 321]
+    spec = W.CaseSpec(f"two_ctas_{n_tiles}", B=len(lens), Hq=8, Hkv=2, D=64, K=7, P=32, window=0,
+                      future_keys=1, ctx_lens=lens, seed=91, poison=True, extra_pages=3, extra_table_slots=2)
+    p = dflash.make_params(batch=spec.B, num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=32,
+                           max_pages_per_req=(spec.max_ctx_len + spec.K + 31) // 32 + 2,
+                           num_pages=spec.B * 200, block_size=7, window=0, future_keys=1, scale=0.125,
+                           max_ctx_len=spec.max_ctx_len, force_split_tiles=n_tiles)
+    if n_tiles:
+        assert dflash.plan(p)["ctas_per_sm"] == 2
+    check_case(spec, cuda_device, force_path=dflash.PATH_MMA, force_split_tiles=n_tiles)
+
+
 @pytest.mark.parametrize("n_tiles", [1, 2, 3, 4, 5, 9])
 def test_tcgen05_unit_tile_counts(cuda_device, n_tiles):
     """Units of 1..9 tiles: both softmax groups, one of them empty, uneven."""
