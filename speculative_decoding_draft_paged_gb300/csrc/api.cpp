@@ -232,21 +232,25 @@ bool make_plan(const dflash_params* p, int num_sms, KernelPlan* out) {
   k.ctas_per_sm = ctas_per_sm_for(k.smem_bytes);
   int C = choose_C(k.smem_bytes, k.ctas_per_sm);
   if (C <= 0) return false;
-  // A plan of more than one wave takes the two-CTAs-per-SM form where there
-  // is one: each CTA's prologue and merge then overlap the other's streaming
-  // (the 64/16-head batch of 256 requests: 10.88 -> 10.30 ms; 8/2 heads 32K
-  // at 16 requests 64.7 -> 61.0 us).  Single-wave plans keep one CTA per SM,
-  // whose 4-stage ring and 140 registers run a short unit faster (8/2 heads
-  // 32K at 1 request: 19.5 against 21.5 us).
+  // A plan of more than one wave takes the two-CTAs-per-SM form where the
+  // kernel has one, with the unit length re-chosen for twice the slots: each
+  // CTA's prologue and merge then overlap the other's streaming, and an SM
+  // holds twice the warps and twice the loads in flight (the 64/16-head
+  // batch of 256 requests: 10.88 -> 10.18 ms; 8/2 heads 32K at 16 requests
+  // 64.3 -> 61.3 us).  Not where that would more than halve the unit length
+  // (8/2 heads 128K at 32 requests, 147 -> 54 tiles: 349 -> 364 us), nor with
+  // the one-CTA units kept (1.5 waves of pairs of CTAs: 349 -> 402 us).
+  // Single-wave plans keep one CTA per SM, whose 4-stage ring and 140
+  // registers run a short unit faster (8/2 heads 32K at 1 request: 19.5
+  // against 21.5 us).
   if (split_mma_two_ctas_ok(D, k.R_pad, k.kpw, fp8) &&
       npairs * ((mt + C - 1) / C) > static_cast<double>(num_sms) * k.ctas_per_sm) {
     const int smem2 = split_mma_smem_bytes(D, k.R_pad, k.kpw, fp8, 0, true);
     const int cps2 = ctas_per_sm_for(smem2);
     const int C2 = choose_C(smem2, cps2);
-    if (cps2 >= 2 && C2 > 0) {
+    if (cps2 >= 2 && C2 > 0 && 2 * C2 >= C) {
       k.two_ctas = true;
       k.ctas_per_sm = cps2;
-      k.smem_bytes = smem2;
       C = C2;
     }
   }
