@@ -167,12 +167,14 @@ def _dense_suffix_case(spec, device, seed):
 @pytest.mark.parametrize("shape,win,fk,r,split", [
     ("gqa8", 0, 1, 0, 0), ("gqa8", 300, 1, 0, 0), ("gqa8", 3, 0, 2, 0),
     ("minimax", 4096, 1, 0, 0), ("minimax", 0, 0, 0, 0), ("minimax", 0, 1, 0, 1),
-    ("minimax", 2, 0, 4, 3),
+    ("minimax", 2, 0, 4, 3), ("gqa4", 0, 1, 0, 1),
 ])
 def test_dense_suffix(cuda_device, path, shape, win, fk, r, split):
-    if shape == "gqa8":
-        spec = _spec("dense_gqa8", [0, 5, 25, 32, 33, 700, 2000], Hq=16, Hkv=2, K=7, P=32,
-                     window=win, future_keys=fk, right_window=r)
+    if shape in ("gqa8", "gqa4"):
+        # gqa4 with one-tile units: a plan of more than one wave, which the
+        # mma.sync kernel runs two CTAs per SM.
+        spec = _spec(f"dense_{shape}", [0, 5, 25, 32, 33, 700, 2000], Hq=16 if shape == "gqa8" else 8,
+                     Hkv=2, K=7, P=32, window=win, future_keys=fk, right_window=r)
     else:
         spec = W.CaseSpec("dense_minimax", B=4, Hq=16, Hkv=1, D=128, K=7, P=64, window=win,
                           future_keys=fk, right_window=r, ctx_lens=[5000, 64, 0, 121], seed=71,
@@ -182,6 +184,11 @@ def test_dense_suffix(cuda_device, path, shape, win, fk, r, split):
         inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K, window=spec.window,
         future_keys=spec.future_keys, scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len,
         force_path=path, force_split_tiles=split, right_window=spec.right_window))
+    if shape == "gqa4" and path == dflash.PATH_MMA:
+        assert dflash.plan(dflash.params_for(
+            inp["q"], inp["k_pages"], inp["page_table"], block_size=spec.K, window=spec.window,
+            future_keys=spec.future_keys, scale=spec.softmax_scale, max_ctx_len=spec.max_ctx_len,
+            force_path=path, force_split_tiles=split, right_window=spec.right_window))["ctas_per_sm"] == 2
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda_device)
     out, lse = dflash.block_attn_dense_suffix(
         inp["q"], kb.to(cuda_device), vb.to(cuda_device), inp["k_pages"], inp["v_pages"],
