@@ -208,6 +208,44 @@ def test_two_ctas_per_sm_plan(dflash_lib):
     assert pl["ctas_per_sm"] == 2 and pl["split_tiles"] == 1
 
 
+def test_every_plan_fits_its_sm(dflash_lib):
+    """Over a seeded sample of valid parameter sets: the split kernel's
+    shared memory fits one CTA (227 KB) and, as many CTAs as the plan says an
+    SM holds, the SM (228 KB, 1 KB reserved per CTA); the two-CTA form only
+    where the kernel has it."""
+    import random
+    d = dflash_lib
+    rng = random.Random(20260)
+    checked = 0
+    for _ in range(400):
+        D = rng.choice([64, 128])
+        Hkv = rng.choice([1, 2, 4, 16])
+        G = rng.choice([1, 2, 4, 6, 8, 16])
+        K = rng.choice([1, 3, 5, 7, 8, 16])
+        if G * K > 128:
+            continue
+        P = rng.choice([16, 32, 64])
+        L = rng.choice([100, 2048, 16384, 32768, 131072])
+        kw = dict(batch=rng.choice([1, 2, 8, 16, 32, 64, 256]), num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                  head_dim=D, page_size=P, block_size=K, max_ctx_len=L,
+                  max_pages_per_req=(L + K + P - 1) // P + 1, num_pages=10 ** 6,
+                  window=rng.choice([0, 0, 4096]), kv_dtype=rng.choice([0, 0, 1]),
+                  force_split_tiles=rng.choice([0, 0, 0, 1, 7]))
+        p = base_params(**kw)
+        if d.workspace_size(p) == 0:
+            continue  # a shape no kernel takes (e.g. an fp8 code ring that does not fit)
+        pl = d.plan(p)
+        checked += 1
+        assert pl["smem_bytes"] <= 227 * 1024, kw
+        assert pl["ctas_per_sm"] * (pl["smem_bytes"] + 1024) <= 228 * 1024, (kw, pl)
+        if pl["ctas_per_sm"] == 2:
+            assert (pl["path"], D, pl["rows_padded"], pl["threads"], kw["kv_dtype"]) == \
+                (d.PATH_MMA, 64, 32, 288, 0), (kw, pl)
+        else:
+            assert pl["ctas_per_sm"] == 1, (kw, pl)
+    assert checked > 100
+
+
 def touched_tiles(L, K, W, T):
     lo = max(0, L - W + 1) if W > 0 else 0
     return (L + K + T - 1) // T - lo // T
